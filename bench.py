@@ -1,0 +1,434 @@
+"""Benchmark: Q4_0 matmul effective weight GB/s on Qwen2.5-7B decode linears.
+
+Workload (one "step"): the 28-layer stack of Qwen2.5-7B linear shapes
+(q/o 3584x3584, k/v 512x3584, gate/up 18944x3584, down 3584x18944 as N x K),
+all stored as Q4_0 (3.67 GB of packed weights, far larger than L2), each
+multiplied by M activation rows for every M in {1, 2, 3, 4, 5, 8}: 6 x 196
+q4mm_forward calls.  Weights are N(0, 0.02^2) and activations N(0, 1), seeded
+(synthetic; no checkpoint).  value = weight bytes streamed per step / step time.
+
+Per step, for each M and each linear type, the 28 calls of that type are one
+CUDA graph replay bracketed by CUDA events on the launching stream; those
+events give each kernel's average launch duration for the roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (fp64, OpenMP on the host cores) on a
+bounded sample of the same workload.  Under torchrun each rank runs its own
+replica of the workload (the path does not shard: replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_SWEEP = (1, 2, 3, 4, 5, 8)
+TYPES = ("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
+DOMINANT = ("gate_proj", "up_proj", "down_proj")
+METRIC = "Q4 matmul effective weight GB/s and token-rows/s vs M (1-256); % of HBM peak"
+WORKLOAD = "qwen2.5-7b decode linears, Q4_0, 28-layer stack (q,k,v,o,gate,up,down), M sweep 1,2,3,4,5,8"
+BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
+
+# DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
+# hash of the kernel source it was taken on (null once the kernel changes).
+TRAFFIC = {}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_matmul_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "q4mm_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def cpu_oracle_sample(layers=1, Ms=M_SWEEP):
+    """Time the oracle (as it stands) on `layers` layers of the stack at each M."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+
+    work = []
+    for layer in range(layers):
+        for t_i, name in enumerate(TYPES):
+            N, K = synthetic.QWEN7B_LINEARS[name]
+            w = synthetic.normal(synthetic.weight_seed(100 + layer, t_i), (N, K), sigma=0.02)
+            work.append((name, N, K, oracle.quantize(w)))
+    xs = {(M, K): synthetic.normal(synthetic.act_seed(1, M) + K, (M, K))
+          for M in Ms for K in (3584, 18944)}
+    t0 = time.perf_counter()
+    wbytes = 0.0
+    rows = 0
+    for M in Ms:
+        for name, N, K, blocks in work:
+            oracle.matmul(blocks, xs[(M, K)])
+            wbytes += N * K * BLOCK_BYTES_PER_WEIGHT
+        rows += M
+    dt = time.perf_counter() - t0
+    return {"value": wbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt, "rows_per_s": rows / dt,
+            "sample": "%d layer(s) of the 7 Qwen2.5-7B linears at M in %s (fp64 oracle, OpenMP over "
+                      "(m,n)), weights quantized beforehand" % (layers, list(Ms))}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    # each step: one layer of the stack at every M of the sweep (~1-3 s on 16 cores)
+    import oracle  # noqa: F401
+
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(layers=1)
+        if i >= args.warmup:
+            samples.append(r)
+    value = statistics.median(s["value"] for s in samples)
+    secs = sum(s["seconds"] for s in samples)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(samples),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "layers_per_step": 1,
+                                        "note": "bounded sample: one layer of the stack per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": samples[0]["cores"],
+                         "kind": "oracle", "sample": samples[0]["sample"]},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def build_stack(q4, torch, dev, layers):
+    """Quantize the 28-layer stack on the device (seeded host draws)."""
+    import synthetic
+
+    stack = {name: [] for name in TYPES}
+    for layer in range(layers):
+        for t_i, name in enumerate(TYPES):
+            N, K = synthetic.QWEN7B_LINEARS[name]
+            w = synthetic.normal(synthetic.weight_seed(1000 + layer, t_i), (N, K), sigma=0.02)
+            wd = torch.from_numpy(w).to(dev)
+            stack[name].append(q4.q4_quantize(wd))
+            del wd
+    torch.cuda.synchronize(dev)
+    return stack
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import bit_quantized_matmul_gb300 as q4
+    import synthetic
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    layers = args.layers
+    stack = build_stack(q4, torch, dev, layers)
+    stream = torch.cuda.Stream(dev)
+
+    # activations: x for K=3584 inputs and K=18944 (down_proj) per M
+    xs = {}
+    for M in M_SWEEP:
+        for K in (3584, 18944):
+            xs[(M, K)] = torch.from_numpy(synthetic.normal(synthetic.act_seed(1, M) + K, (M, K))).to(dev)
+    ys = {}
+    for M in M_SWEEP:
+        for name in TYPES:
+            N, _ = synthetic.QWEN7B_LINEARS[name]
+            ys[(M, name)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    def issue(M, name):
+        K = synthetic.QWEN7B_LINEARS[name][1]
+        x = xs[(M, K)]
+        y = ys[(M, name)]
+        for W in stack[name]:
+            q4.q4mm_forward(W, x, y=y, stream=stream)
+
+    # warm the library (scratch allocation) before capture
+    with torch.cuda.stream(stream):
+        for M in M_SWEEP:
+            for name in TYPES:
+                issue(M, name)
+    torch.cuda.synchronize(dev)
+
+    graphs = {}
+    for M in M_SWEEP:
+        for name in TYPES:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue(M, name)
+            graphs[(M, name)] = g
+    torch.cuda.synchronize(dev)
+
+    plan = {}
+    launches_per_step = 0
+    for M in M_SWEEP:
+        for name in TYPES:
+            p, l, s = q4.q4mm_plan_info(stack[name][0], M)
+            plan[(M, name)] = {"path": p, "launches": l, "splits": s}
+            launches_per_step += l * layers
+
+    wbytes = {name: synthetic.QWEN7B_LINEARS[name][0] * synthetic.QWEN7B_LINEARS[name][1]
+              * BLOCK_BYTES_PER_WEIGHT for name in TYPES}
+    step_wbytes = sum(wbytes[n] * layers for n in TYPES) * len(M_SWEEP)
+
+    def algo_bytes(M, name):
+        N, K = synthetic.QWEN7B_LINEARS[name]
+        return wbytes[name] + 4.0 * M * K + 4.0 * M * N
+
+    ev = {}
+
+    def step(record):
+        for M in M_SWEEP:
+            for name in TYPES:
+                if record:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    graphs[(M, name)].replay()
+                    b.record(stream)
+                    ev.setdefault((M, name), []).append((a, b))
+                else:
+                    graphs[(M, name)].replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(False)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = step_wbytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # per-(M, type) kernel durations over the timed region
+    per = {}
+    for key, pairs in ev.items():
+        per[key] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) / layers  # ms per launch
+    peak, peak_kind = _peaks()
+    dom_bytes = sum(algo_bytes(M, n) for M in M_SWEEP for n in DOMINANT)
+    dom_ms = sum(per[(M, n)] for M in M_SWEEP for n in DOMINANT)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = None
+    if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash():
+        traffic = TRAFFIC.get("bytes_per_launch")
+    per_m = {}
+    for M in M_SWEEP:
+        t = sum(per[(M, n)] * layers for n in TYPES)
+        b = sum(wbytes[n] * layers for n in TYPES)
+        per_m[str(M)] = {
+            "weight_gbs": b / (t * 1e-3) / 1e9,
+            "token_rows_per_s": M / (t * 1e-3),
+            "frac_of_measured_hbm": b / (t * 1e-3) / 1e9 / peak,
+            "paths": sorted({plan[(M, n)]["path"] for n in TYPES}),
+            "gate_us": per[(M, "gate_proj")] * 1e3,
+            "down_us": per[(M, "down_proj")] * 1e3,
+            "q_us": per[(M, "q_proj")] * 1e3,
+            "k_us": per[(M, "k_proj")] * 1e3,
+        }
+
+    # ---- end to end through the public API: pinned host x in, host y out ----
+    pin_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    out_host = {M: torch.empty((M, 3584), dtype=torch.float32).pin_memory() for M in M_SWEEP}
+    h2d = sum(v.numel() * 4 for v in pin_x.values())
+    d2h = sum(v.numel() * 4 for v in out_host.values())
+
+    def e2e_step():
+        for M in M_SWEEP:
+            xs[(M, 3584)].copy_(pin_x[(M, 3584)], non_blocking=True)
+            xs[(M, 18944)].copy_(pin_x[(M, 18944)], non_blocking=True)
+            for name in TYPES:
+                graphs[(M, name)].replay()
+            out_host[M].copy_(ys[(M, "down_proj")], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_value = step_wbytes * world / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(layers=1)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": layers, "M_sweep": list(M_SWEEP),
+                       "weights": "Q4_0 (18 B per 32 weights), N(0,0.02^2)", "activations": "fp32 N(0,1)",
+                       "l2": "inputs larger than L2 (%.2f GB packed weight stack, streamed once per M)"
+                             % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "m_threshold": q4.q4mm_get_m_threshold()},
+            "token_rows_per_s": sum(M_SWEEP) * world / (ms_per_step * 1e-3),
+            "per_M": per_m,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "kernel": "q4mm gate/up/down launches (all M of the sweep)",
+                         "algorithmic_bytes_per_launch": "0.5625*N*K + 4*M*K + 4*M*N"},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    for name in TYPES:
+        for W in stack[name]:
+            W.free()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

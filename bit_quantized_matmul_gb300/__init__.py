@@ -1,0 +1,281 @@
+"""Thin Python binding over the C ABI of ``libq4mm.so`` (``include/q4mm.h``).
+
+Argument marshalling only: tensors are passed as raw device pointers with the
+current PyTorch CUDA stream, and every step of the computation runs in the
+library's CUDA kernels.  There is no CPU or PyTorch fallback: if the library
+is missing, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch  # device memory and streams; loads the CUDA runtime first
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq4mm.so")
+
+Q4_OK = 0
+Q4_ERR_INVALID_ARG = 1
+Q4_ERR_SHAPE = 2
+Q4_ERR_ALIGN = 3
+Q4_ERR_NONFINITE = 4
+Q4_ERR_RANGE = 5
+Q4_ERR_CUDA = 6
+Q4_ERR_TIMEOUT = 7
+Q4_ERR_NOMEM = 8
+Q4_ERR_UNSUPPORTED = 9
+
+Q4MM_BATCH_INVARIANT = 0x1
+Q4MM_FORCE_SIMT = 0x2
+Q4MM_FORCE_TC = 0x4
+Q4MM_ROW_BY_ROW = 0x8
+Q4MM_M_MAX = 4096
+Q4MM_PATH_SIMT = 1
+Q4MM_PATH_TC = 2
+Q4MM_PATH_ROW_BY_ROW = 3
+
+BLOCK = 32
+BLOCK_BYTES = 18
+
+# Every symbol the header declares; the CPU test checks the library exports them.
+EXPORTS = (
+    "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
+    "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
+    "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
+    "q4_status_string",
+)
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libq4mm.so is not built (%s); run __graft_entry__.build() or "
+                      "python bit_quantized_matmul_gb300/build.py" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_u32 = ctypes.c_uint32
+_sig = {
+    "q4_quantize": [_p, _i64, _i64, ctypes.POINTER(_p), _p],
+    "q4_import_blocks": [_p, _i64, _i64, ctypes.POINTER(_p), _p],
+    "q4_export_blocks": [_p, _p, ctypes.c_size_t],
+    "q4_weight_free": [_p],
+    "q4_weight_shape": [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64)],
+    "q4_weight_device_bytes": [_p, ctypes.POINTER(ctypes.c_size_t)],
+    "q4mm_forward": [_p, _p, _p, _i64, _p],
+    "q4mm_forward_ex": [_p, _p, _p, _i64, _u32, _p],
+    "q4mm_argmax": [_p, _p, _p, _p, _i64, _p],
+    "q4mm_argmax_ex": [_p, _p, _p, _p, _i64, _u32, _p],
+    "q4mm_select_path": [_p, _i64, _u32],
+    "q4mm_plan_info": [_p, _i64, _u32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                       ctypes.POINTER(ctypes.c_int)],
+    "q4mm_set_m_threshold": [_i64],
+    "q4mm_get_m_threshold": [],
+    "q4_device_status": [],
+    "q4_status_string": [ctypes.c_int],
+}
+for _name, _args in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.q4mm_get_m_threshold.restype = ctypes.c_int64
+_lib.q4_status_string.restype = ctypes.c_char_p
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        msg = "%s: %s (status %d)" % (what, q4_status_string(status), status)
+        super().__init__(msg)
+        self.status = status
+
+
+def _check(status: int, what: str):
+    if status != Q4_OK:
+        raise Q4Error(status, what)
+
+
+def q4_status_string(status: int) -> str:
+    return _lib.q4_status_string(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev_f32(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise ValueError("%s must be a contiguous float32 CUDA tensor" % name)
+    return t
+
+
+class Q4Weight:
+    """Owning wrapper of a ``q4_weight*`` handle (freed on ``free()`` / GC)."""
+
+    def __init__(self, handle: int, N: int, K: int, device: torch.device):
+        self._h = ctypes.c_void_p(handle)
+        self.N, self.K, self.device = N, K, device
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise ValueError("Q4Weight already freed")
+        return self._h
+
+    def free(self):
+        if self._h:
+            torch.cuda.synchronize(self.device)
+            _check(_lib.q4_weight_free(self._h), "q4_weight_free")
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            if self._h:
+                _lib.q4_weight_free(self._h)
+        except Exception:
+            pass
+
+    def device_bytes(self) -> int:
+        b = ctypes.c_size_t(0)
+        _check(_lib.q4_weight_device_bytes(self.handle, ctypes.byref(b)), "q4_weight_device_bytes")
+        return int(b.value)
+
+    @property
+    def packed_bytes(self) -> int:
+        """Algorithmic size of the Q4_0 weights: N*K/32 blocks of 18 bytes."""
+        return self.N * (self.K // BLOCK) * BLOCK_BYTES
+
+
+def q4_quantize(w: torch.Tensor, stream=None) -> Q4Weight:
+    """Quantize an fp32 [N, K] CUDA tensor into a library-owned Q4_0 weight."""
+    _dev_f32(w, "w")
+    N, K = w.shape
+    h = ctypes.c_void_p(0)
+    with torch.cuda.device(w.device):
+        _check(_lib.q4_quantize(w.data_ptr(), N, K, ctypes.byref(h), _stream(stream)), "q4_quantize")
+    return Q4Weight(h.value, N, K, w.device)
+
+
+def q4_import_blocks(blocks, N: int, K: int, device=None, stream=None) -> Q4Weight:
+    """Create a weight from canonical blocks (uint8 numpy array / bytes, N*K/32*18 bytes)."""
+    import numpy as np
+
+    arr = np.ascontiguousarray(np.frombuffer(bytes(blocks), np.uint8) if isinstance(blocks, (bytes, bytearray))
+                               else blocks, dtype=np.uint8)
+    if arr.size != N * (K // BLOCK) * BLOCK_BYTES:
+        raise ValueError("blocks size does not match N, K")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    h = ctypes.c_void_p(0)
+    with torch.cuda.device(device):
+        _check(_lib.q4_import_blocks(arr.ctypes.data_as(ctypes.c_void_p), N, K, ctypes.byref(h),
+                                     _stream(stream)), "q4_import_blocks")
+    return Q4Weight(h.value, N, K, device)
+
+
+def q4_export_blocks(W: Q4Weight):
+    """Canonical blocks of W as a uint8 numpy array [N, K/32, 18]."""
+    import numpy as np
+
+    out = np.empty((W.N, W.K // BLOCK, BLOCK_BYTES), np.uint8)
+    with torch.cuda.device(W.device):
+        _check(_lib.q4_export_blocks(W.handle, out.ctypes.data_as(ctypes.c_void_p), out.nbytes),
+               "q4_export_blocks")
+    return out
+
+
+def q4_weight_free(W: Q4Weight):
+    W.free()
+
+
+def q4mm_forward_ex(W: Q4Weight, x: torch.Tensor, flags: int = 0, y: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ W^T (fp32) with Q4MM_* flags."""
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [M, %d]" % W.K)
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.float32, device=x.device)
+    _dev_f32(y, "y")
+    if tuple(y.shape) != (M, W.N):
+        raise ValueError("y must be [M, %d]" % W.N)
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_forward_ex(W.handle, x.data_ptr(), y.data_ptr(), M, int(flags), _stream(stream)),
+               "q4mm_forward_ex")
+    return y
+
+
+def q4mm_forward(W: Q4Weight, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [M, %d]" % W.K)
+    if y is None:
+        y = torch.empty((M, W.N), dtype=torch.float32, device=x.device)
+    _dev_f32(y, "y")
+    if tuple(y.shape) != (M, W.N):
+        raise ValueError("y must be [M, %d]" % W.N)
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_forward(W.handle, x.data_ptr(), y.data_ptr(), M, _stream(stream)), "q4mm_forward")
+    return y
+
+
+def q4mm_argmax_ex(W: Q4Weight, x: torch.Tensor, flags: int = 0, want_max: bool = True, stream=None):
+    """Fused greedy pick: (idx int32 [M], maxval fp32 [M] or None)."""
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [M, %d]" % W.K)
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    mx = torch.empty(M, dtype=torch.float32, device=x.device) if want_max else None
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_argmax_ex(W.handle, x.data_ptr(), idx.data_ptr(), mx.data_ptr() if mx is not None else None,
+                                   M, int(flags), _stream(stream)), "q4mm_argmax_ex")
+    return idx, mx
+
+
+def q4mm_argmax(W: Q4Weight, x: torch.Tensor, want_max: bool = True, stream=None):
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [M, %d]" % W.K)
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    mx = torch.empty(M, dtype=torch.float32, device=x.device) if want_max else None
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_argmax(W.handle, x.data_ptr(), idx.data_ptr(), mx.data_ptr() if mx is not None else None,
+                                M, _stream(stream)), "q4mm_argmax")
+    return idx, mx
+
+
+def q4mm_select_path(W: Q4Weight, M: int, flags: int = 0) -> int:
+    with torch.cuda.device(W.device):
+        r = _lib.q4mm_select_path(W.handle, M, int(flags))
+    if r < 0:
+        raise Q4Error(-r, "q4mm_select_path")
+    return r
+
+
+def q4mm_plan_info(W: Q4Weight, M: int, flags: int = 0):
+    """(path, kernel launches, K splits) that a call would use."""
+    p, l, s = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    with torch.cuda.device(W.device):
+        _check(_lib.q4mm_plan_info(W.handle, M, int(flags), ctypes.byref(p), ctypes.byref(l), ctypes.byref(s)),
+               "q4mm_plan_info")
+    return p.value, l.value, s.value
+
+
+def q4mm_set_m_threshold(m: int):
+    _check(_lib.q4mm_set_m_threshold(int(m)), "q4mm_set_m_threshold")
+
+
+def q4mm_get_m_threshold() -> int:
+    return int(_lib.q4mm_get_m_threshold())
+
+
+def q4_device_status() -> int:
+    return int(_lib.q4_device_status())
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded ctypes library (for callers that marshal pointers themselves)."""
+    return _lib

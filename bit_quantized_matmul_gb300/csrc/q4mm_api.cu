@@ -1,0 +1,435 @@
+// q4mm_api.cu — the C ABI: argument checks, handle and scratch management,
+// and the choice of kernel path.
+//
+// The path choice follows the lesson of "Why Continuous Batching Slowed Down
+// My LLM Inference Engine" (§"Row-by-Row GEMV to the Rescue", §"Takeaways"):
+// the switch between the streaming small-M kernel and the tensor-core kernel
+// is a measured M threshold, not "one row vs. more than one"; and in
+// batch-invariant mode the path and the K partition never depend on M
+// (§"The Other Request Already Finished — So Why Is It Still Having an
+// Effect?").
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "q4mm_internal.h"
+
+struct q4_weight {
+  q4::Weight w;
+};
+
+namespace q4 {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceScratch {
+  std::mutex mu;
+  bool init = false;
+  Workspace ws;
+  unsigned int* format_flag = nullptr;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+DeviceScratch g_dev[MAX_DEVICES];
+
+// Measured on GB300: below this M the CUDA-core streaming kernel is used,
+// at or above it the tensor-core kernel.
+constexpr int64_t DEFAULT_M_THRESHOLD = 2;
+std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int init_device_locked(int dev, DeviceScratch& ds) {
+  if (ds.init) return Q4_OK;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return Q4_ERR_CUDA;
+  ds.num_sms = prop.multiProcessorCount;
+  ds.cc_major = prop.major;
+  ds.cc_minor = prop.minor;
+  const size_t small = 256 + MAX_COUNTERS * sizeof(unsigned) + Q4MM_M_MAX * sizeof(unsigned long long) + 256;
+  char* base = nullptr;
+  if (cudaMalloc(&base, small) != cudaSuccess) return Q4_ERR_NOMEM;
+  if (cudaMemset(base, 0, small) != cudaSuccess) return Q4_ERR_CUDA;
+  ds.ws.status = reinterpret_cast<unsigned*>(base);
+  ds.ws.argmax_done = reinterpret_cast<unsigned*>(base + 4);
+  ds.format_flag = reinterpret_cast<unsigned*>(base + 8);
+  ds.ws.keys = reinterpret_cast<unsigned long long*>(base + 256);
+  ds.ws.counters = reinterpret_cast<unsigned*>(base + 256 + Q4MM_M_MAX * sizeof(unsigned long long));
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
+  ds.init = true;
+  return Q4_OK;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return Q4_ERR_CUDA;
+  if (*dev < 0 || *dev >= MAX_DEVICES) return Q4_ERR_UNSUPPORTED;
+  return Q4_OK;
+}
+
+bool tc_supported(const DeviceScratch& ds) {
+  return tc_kernel_built() && ds.cc_major == 10 && ds.cc_minor == 3;
+}
+
+int alloc_weight(int64_t N, int64_t K, int dev, Weight* W) {
+  W->N = N;
+  W->K = K;
+  W->N_pad = pad_n(N);
+  W->KB = K / BLOCK_K;
+  W->tiles = W->N_pad / TILE_N;
+  W->device = dev;
+  const size_t nib_bytes = (size_t)W->tiles * W->KB * TILE_N * 16;
+  const size_t d_bytes = (size_t)W->tiles * W->KB * TILE_N * 2;
+  const size_t off = (nib_bytes + 255) / 256 * 256;
+  W->alloc_bytes = off + d_bytes;
+  if (cudaMalloc(&W->alloc, W->alloc_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return Q4_ERR_NOMEM;
+  }
+  W->nib = static_cast<uint8_t*>(W->alloc);
+  W->d = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(W->alloc) + off);
+  return Q4_OK;
+}
+
+int check_shape(int64_t N, int64_t K) {
+  if (N < 1 || K < BLOCK_K || (K % BLOCK_K) != 0) return Q4_ERR_SHAPE;
+  if (N > (int64_t)1 << 31 || K / BLOCK_K > 65535) return Q4_ERR_SHAPE;  // grid.y = K/32
+  return Q4_OK;
+}
+
+// Path choice.  Deterministic in (flags, M, device); in batch-invariant mode
+// it ignores M entirely.
+int choose_path(const DeviceScratch& ds, int64_t M, uint32_t flags) {
+  const bool tc = tc_supported(ds);
+  if (flags & Q4MM_ROW_BY_ROW) return Q4MM_PATH_ROW_BY_ROW;
+  if (flags & Q4MM_FORCE_SIMT) return Q4MM_PATH_SIMT;
+  if (flags & Q4MM_FORCE_TC) return tc ? Q4MM_PATH_TC : -Q4_ERR_UNSUPPORTED;
+  if (flags & Q4MM_BATCH_INVARIANT) return tc ? Q4MM_PATH_TC : Q4MM_PATH_SIMT;
+  return (tc && M >= g_m_threshold.load()) ? Q4MM_PATH_TC : Q4MM_PATH_SIMT;
+}
+
+constexpr uint32_t KNOWN_FLAGS =
+    Q4MM_BATCH_INVARIANT | Q4MM_FORCE_SIMT | Q4MM_FORCE_TC | Q4MM_ROW_BY_ROW;
+
+int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxval, int64_t M,
+        uint32_t flags, cudaStream_t s) {
+  if (!Wh || !x || (!y && !idx)) return Q4_ERR_INVALID_ARG;
+  if (flags & ~KNOWN_FLAGS) return Q4_ERR_INVALID_ARG;
+  const int forced = !!(flags & Q4MM_FORCE_SIMT) + !!(flags & Q4MM_FORCE_TC) + !!(flags & Q4MM_ROW_BY_ROW);
+  if (forced > 1) return Q4_ERR_INVALID_ARG;
+  if (M < 0) return Q4_ERR_INVALID_ARG;
+  if (M > Q4MM_M_MAX) return Q4_ERR_SHAPE;
+  if (M == 0) return Q4_OK;
+  if (!aligned16(x) || (y && !aligned16(y)) || (idx && !aligned16(idx)) ||
+      (maxval && !aligned16(maxval)))
+    return Q4_ERR_ALIGN;
+  const Weight* W = &Wh->w;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (dev != W->device) return Q4_ERR_INVALID_ARG;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  const int path = choose_path(ds, M, flags);
+  if (path < 0) return -path;
+  if (path == Q4MM_PATH_TC) {
+    const TcPlan plan = tc_plan(W, M, ds.num_sms, (flags & Q4MM_BATCH_INVARIANT) != 0);
+    Workspace ws;
+    st = workspace_get(dev, tc_partial_bytes(W, plan, M), tc_xop_bytes(W, plan, M), &ws);
+    if (st) return st;
+    return launch_tc(W, x, M, y, idx, maxval, plan, ws, s);
+  }
+  const SimtPlan plan = simt_plan(W, ds.num_sms);
+  Workspace ws;
+  if (path == Q4MM_PATH_ROW_BY_ROW) {
+    st = workspace_get(dev, simt_partial_bytes(W, plan, 1), 0, &ws);
+    if (st) return st;
+    for (int64_t m = 0; m < M; ++m) {
+      st = launch_simt(W, x + m * W->K, 1, y ? y + m * W->N : nullptr, idx ? idx + m : nullptr,
+                       (idx && maxval) ? maxval + m : nullptr, plan, ws, s);
+      if (st) return st;
+    }
+    return Q4_OK;
+  }
+  st = workspace_get(dev, simt_partial_bytes(W, plan, M), 0, &ws);
+  if (st) return st;
+  return launch_simt(W, x, M, y, idx, maxval, plan, ws, s);
+}
+
+}  // namespace
+
+// Caller holds g_dev[device].mu.
+int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* out) {
+  DeviceScratch& ds = g_dev[device];
+  if (partial_bytes > ds.ws.partial_bytes) {
+    size_t want = partial_bytes + partial_bytes / 2;
+    if (ds.ws.partial) cudaFree(ds.ws.partial);  // cudaFree waits for work in flight
+    ds.ws.partial = nullptr;
+    ds.ws.partial_bytes = 0;
+    if (cudaMalloc(&ds.ws.partial, want) != cudaSuccess) {
+      cudaGetLastError();
+      return Q4_ERR_NOMEM;
+    }
+    ds.ws.partial_bytes = want;
+  }
+  if (xop_bytes > ds.ws.xop_bytes) {
+    size_t want = xop_bytes + xop_bytes / 2;
+    if (ds.ws.xop) cudaFree(ds.ws.xop);
+    ds.ws.xop = nullptr;
+    ds.ws.xop_bytes = 0;
+    if (cudaMalloc(&ds.ws.xop, want) != cudaSuccess) {
+      cudaGetLastError();
+      return Q4_ERR_NOMEM;
+    }
+    ds.ws.xop_bytes = want;
+  }
+  *out = ds.ws;
+  return Q4_OK;
+}
+
+int device_num_sms(int device) { return g_dev[device].num_sms; }
+
+}  // namespace q4
+
+using namespace q4;
+
+extern "C" {
+
+int q4_quantize(const float* w, int64_t N, int64_t K, q4_weight** out, cudaStream_t stream) {
+  if (!w || !out) return Q4_ERR_INVALID_ARG;
+  int st = check_shape(N, K);
+  if (st) return st;
+  if (!aligned16(w)) return Q4_ERR_ALIGN;
+  int dev;
+  st = current_device(&dev);
+  if (st) return st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  q4_weight* h = new (std::nothrow) q4_weight;
+  if (!h) return Q4_ERR_NOMEM;
+  st = alloc_weight(N, K, dev, &h->w);
+  if (st) {
+    delete h;
+    return st;
+  }
+  unsigned flag = 0;
+  st = Q4_OK;
+  if (cudaMemsetAsync(ds.format_flag, 0, sizeof(unsigned), stream) != cudaSuccess) st = Q4_ERR_CUDA;
+  if (!st) st = launch_quantize(w, N, K, &h->w, ds.format_flag, stream);
+  if (!st && cudaMemcpyAsync(&flag, ds.format_flag, sizeof(unsigned), cudaMemcpyDeviceToHost,
+                             stream) != cudaSuccess)
+    st = Q4_ERR_CUDA;
+  if (!st && cudaStreamSynchronize(stream) != cudaSuccess) st = Q4_ERR_CUDA;
+  if (!st) st = quantize_flag_status(flag);
+  if (st) {
+    cudaFree(h->w.alloc);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return Q4_OK;
+}
+
+int q4_import_blocks(const void* host_blocks, int64_t N, int64_t K, q4_weight** out,
+                     cudaStream_t stream) {
+  if (!host_blocks || !out) return Q4_ERR_INVALID_ARG;
+  int st = check_shape(N, K);
+  if (st) return st;
+  int dev;
+  st = current_device(&dev);
+  if (st) return st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  q4_weight* h = new (std::nothrow) q4_weight;
+  if (!h) return Q4_ERR_NOMEM;
+  st = alloc_weight(N, K, dev, &h->w);
+  if (st) {
+    delete h;
+    return st;
+  }
+  const size_t bytes = (size_t)N * (size_t)(K / BLOCK_K) * CANON_BLOCK_BYTES;
+  uint8_t* staging = nullptr;
+  if (cudaMalloc(&staging, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->w.alloc);
+    delete h;
+    return Q4_ERR_NOMEM;
+  }
+  unsigned flag = 0;
+  if (cudaMemsetAsync(ds.format_flag, 0, sizeof(unsigned), stream) != cudaSuccess ||
+      cudaMemcpyAsync(staging, host_blocks, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    st = Q4_ERR_CUDA;
+  if (!st) st = launch_import(staging, &h->w, ds.format_flag, stream);
+  if (!st && cudaMemcpyAsync(&flag, ds.format_flag, sizeof(unsigned), cudaMemcpyDeviceToHost,
+                             stream) != cudaSuccess)
+    st = Q4_ERR_CUDA;
+  if (!st && cudaStreamSynchronize(stream) != cudaSuccess) st = Q4_ERR_CUDA;
+  cudaFree(staging);
+  if (!st) st = quantize_flag_status(flag);
+  if (st) {
+    cudaFree(h->w.alloc);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return Q4_OK;
+}
+
+int q4_export_blocks(const q4_weight* W, void* host_blocks, size_t bytes) {
+  if (!W || !host_blocks) return Q4_ERR_INVALID_ARG;
+  const size_t need = (size_t)W->w.N * (size_t)W->w.KB * CANON_BLOCK_BYTES;
+  if (bytes < need) return Q4_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (dev != W->w.device) return Q4_ERR_INVALID_ARG;
+  uint8_t* staging = nullptr;
+  if (cudaMalloc(&staging, need) != cudaSuccess) {
+    cudaGetLastError();
+    return Q4_ERR_NOMEM;
+  }
+  st = launch_export(&W->w, staging, 0);
+  if (!st && cudaMemcpy(host_blocks, staging, need, cudaMemcpyDeviceToHost) != cudaSuccess)
+    st = Q4_ERR_CUDA;
+  cudaFree(staging);
+  return st;
+}
+
+int q4_weight_free(q4_weight* W) {
+  if (!W) return Q4_ERR_INVALID_ARG;
+  const cudaError_t e = cudaFree(W->w.alloc);
+  delete W;
+  return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+int q4_weight_shape(const q4_weight* W, int64_t* N, int64_t* K) {
+  if (!W || !N || !K) return Q4_ERR_INVALID_ARG;
+  *N = W->w.N;
+  *K = W->w.K;
+  return Q4_OK;
+}
+
+int q4_weight_device_bytes(const q4_weight* W, size_t* bytes) {
+  if (!W || !bytes) return Q4_ERR_INVALID_ARG;
+  *bytes = W->w.alloc_bytes;
+  return Q4_OK;
+}
+
+int q4mm_forward(const q4_weight* W, const float* x, float* y, int64_t M, cudaStream_t stream) {
+  if (!y) return Q4_ERR_INVALID_ARG;
+  return run(W, x, y, nullptr, nullptr, M, 0u, stream);
+}
+
+int q4mm_forward_ex(const q4_weight* W, const float* x, float* y, int64_t M, uint32_t flags,
+                    cudaStream_t stream) {
+  if (!y) return Q4_ERR_INVALID_ARG;
+  return run(W, x, y, nullptr, nullptr, M, flags, stream);
+}
+
+int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
+                cudaStream_t stream) {
+  if (!idx) return Q4_ERR_INVALID_ARG;
+  return run(W, x, nullptr, idx, maxval, M, 0u, stream);
+}
+
+int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
+                   uint32_t flags, cudaStream_t stream) {
+  if (!idx) return Q4_ERR_INVALID_ARG;
+  return run(W, x, nullptr, idx, maxval, M, flags, stream);
+}
+
+int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags) {
+  if (!W || M < 0 || (flags & ~KNOWN_FLAGS)) return -Q4_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return -st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return -st;
+  return choose_path(ds, M, flags);
+}
+
+int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int* launches,
+                   int* splits) {
+  if (!W || M < 0 || M > Q4MM_M_MAX || (flags & ~KNOWN_FLAGS)) return Q4_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  const int p = choose_path(ds, M, flags);
+  if (p < 0) return -p;
+  int l = 0, sp = 1;
+  if (p == Q4MM_PATH_TC) {
+    const TcPlan plan = tc_plan(&W->w, M, ds.num_sms, (flags & Q4MM_BATCH_INVARIANT) != 0);
+    l = tc_launch_count(plan, M);
+    sp = plan.splits;
+  } else {
+    const SimtPlan plan = simt_plan(&W->w, ds.num_sms);
+    l = p == Q4MM_PATH_ROW_BY_ROW ? (int)M : simt_launch_count(M);
+    sp = plan.splits;
+  }
+  if (M == 0) l = 0;
+  if (path) *path = p;
+  if (launches) *launches = l;
+  if (splits) *splits = sp;
+  return Q4_OK;
+}
+
+int q4mm_set_m_threshold(int64_t m) {
+  if (m < 1 || m > Q4MM_M_MAX + 1) return Q4_ERR_INVALID_ARG;
+  g_m_threshold.store(m);
+  return Q4_OK;
+}
+
+int64_t q4mm_get_m_threshold(void) { return g_m_threshold.load(); }
+
+int q4_device_status(void) {
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  if (!ds.init) return Q4_OK;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, ds.ws.status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return Q4_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(ds.ws.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
+      return Q4_ERR_CUDA;
+    return Q4_ERR_TIMEOUT;
+  }
+  return Q4_OK;
+}
+
+const char* q4_status_string(int status) {
+  switch (status) {
+    case Q4_OK: return "ok";
+    case Q4_ERR_INVALID_ARG: return "invalid argument";
+    case Q4_ERR_SHAPE: return "unsupported shape";
+    case Q4_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case Q4_ERR_NONFINITE: return "non-finite weight or scale";
+    case Q4_ERR_RANGE: return "block scale out of binary16 range";
+    case Q4_ERR_CUDA: return "CUDA runtime error";
+    case Q4_ERR_TIMEOUT: return "device-side wait timed out";
+    case Q4_ERR_NOMEM: return "device allocation failed";
+    case Q4_ERR_UNSUPPORTED: return "unsupported device or path";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

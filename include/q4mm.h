@@ -1,0 +1,181 @@
+/*
+ * q4mm.h — C ABI of the GB300 (sm_103a) Q4_0 block-quantized matmul library.
+ *
+ * The operation is the linear layer of LLM decode and continuous batching:
+ * M activation rows (token rows: decode, prefill and verify rows merged into
+ * one batch) times a weight matrix stored in 4-bit blocks and dequantized on
+ * the fly,
+ *
+ *     y[m, n] = sum_k x[m, k] * w[n, k],   w[n, k] = (q[n, k] - 8) * d[n, k/32]
+ *
+ * ("Why Continuous Batching Slowed Down My LLM Inference Engine: A Metal
+ * Kernel Investigation", §"Two Rows of Input, Two Different Kernels": the
+ * quantized matmul whose one-row (GEMV) and many-row (GEMM) kernels the
+ * investigation compares; "Why LLM Decoding Is Slow, and Why Batching Is
+ * (Almost) Free", §3 "Two Ceilings" and §4 "Share the Weights Across Users":
+ * every token row that shares one pass over the weights is nearly free while
+ * the step stays memory-bound).
+ *
+ * Q4_0 block format (the pages say only "4-bit"; this library fixes it):
+ * 32 consecutive weights along K share one fp16 scale d = m / -8, where m is
+ * the first element of largest magnitude, and q = clamp(round(w/d) + 8, 0, 15)
+ * with IEEE fp32 division and round-half-away-from-zero; an all-zero block has
+ * d = 0 and q = 8.  The canonical serialized block is 18 bytes: d as binary16
+ * little-endian, then 16 bytes where byte j holds q_j in its low nibble and
+ * q_{j+16} in its high nibble.  Blocks of row n follow in ascending K; rows in
+ * ascending n.  Inside the library the weights live in a private device layout
+ * (tiled for coalesced, 16-byte-aligned streaming); only the canonical form is
+ * exchanged across this boundary.
+ *
+ * Conventions for every entry point:
+ *  - All functions return an int status (Q4_OK on success), never throw and
+ *    never trap the device.  Invalid arguments are rejected on the host before
+ *    any launch.
+ *  - "device" pointers are CUDA global-memory pointers on the current device;
+ *    "host" pointers are ordinary CPU memory.  The caller owns x, y, idx,
+ *    maxval and all host buffers.  A q4_weight is owned by the library from
+ *    its creation (q4_quantize / q4_import_blocks) until q4_weight_free.
+ *  - Compute calls are asynchronous on `stream` (0 = the legacy default
+ *    stream) and do not synchronize the host.  A kernel fault from an earlier
+ *    call surfaces as Q4_ERR_CUDA on a later call.
+ *  - Compute calls use a per-device scratch area owned by the library (split-K
+ *    partial sums, the activation operand of the tensor-core path, argmax
+ *    keys).  It is allocated (or grown) on the first call that needs it, so
+ *    make one call of each shape before capturing a CUDA graph.  Calls that
+ *    share that scratch must be ordered on one stream; calls on different
+ *    streams that overlap on the GPU race on it.
+ *  - Every device-side wait in the kernels is bounded; a wait that runs out
+ *    records Q4_ERR_TIMEOUT in a device status word that q4_device_status()
+ *    returns.
+ */
+#ifndef Q4MM_H
+#define Q4MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define Q4_API __attribute__((visibility("default")))
+#else
+#define Q4_API
+#endif
+
+/* ---- status codes ---- */
+#define Q4_OK 0
+#define Q4_ERR_INVALID_ARG 1  /* null pointer, negative size, wrong device, bad flag */
+#define Q4_ERR_SHAPE 2        /* K not a positive multiple of 32 or above 32*65535, N < 1, M above Q4MM_M_MAX */
+#define Q4_ERR_ALIGN 3        /* a device pointer not 16-byte aligned */
+#define Q4_ERR_NONFINITE 4    /* a weight is NaN or infinite (quantize), or a stored scale is */
+#define Q4_ERR_RANGE 5        /* a block scale does not fit binary16 (|d| >= 65520) */
+#define Q4_ERR_CUDA 6         /* a CUDA runtime error (launch failure, sticky fault) */
+#define Q4_ERR_TIMEOUT 7      /* a bounded device-side wait ran out */
+#define Q4_ERR_NOMEM 8        /* device allocation failed */
+#define Q4_ERR_UNSUPPORTED 9  /* the device is not sm_103 / requested path unavailable */
+
+/* ---- flags for the _ex entry points ---- */
+/* Bit-identical output rows: row r of y depends only on x[r,:] and W, never on
+ * M, on r's position in the batch or on the other rows' values.  The kernel
+ * family and the K partition are then fixed per weight shape, independent of M
+ * (§"The Other Request Already Finished": a 120-prefill + 4-verify batch
+ * crossed the kernel-switch threshold and changed the cached numbers). */
+#define Q4MM_BATCH_INVARIANT 0x1u
+/* Force the CUDA-core streaming kernel (the measured small-M path). */
+#define Q4MM_FORCE_SIMT 0x2u
+/* Force the tensor-core (tcgen05/TMEM) kernel. */
+#define Q4MM_FORCE_TC 0x4u
+/* Ablation: one launch per activation row with the small-M kernel, the
+ * row-by-row fallback of §"Row-by-Row GEMV to the Rescue". */
+#define Q4MM_ROW_BY_ROW 0x8u
+
+/* Largest M accepted by one call. */
+#define Q4MM_M_MAX 4096
+
+/* Kernel paths reported by q4mm_select_path. */
+#define Q4MM_PATH_SIMT 1
+#define Q4MM_PATH_TC 2
+#define Q4MM_PATH_ROW_BY_ROW 3
+
+typedef struct q4_weight q4_weight;
+
+/* Quantize an fp32 weight matrix already on the device.
+ *   w      device, fp32 [N, K] row-major, 16-byte aligned; read only.
+ *   N, K   N >= 1 output rows; K >= 32 and a multiple of 32.
+ *   out    receives a new handle (library-owned) on Q4_OK; untouched otherwise.
+ * Synchronizes `stream` to report Q4_ERR_NONFINITE / Q4_ERR_RANGE (this is an
+ * off-step operation).  The blocks are byte-identical to the canonical rule in
+ * the file header. */
+Q4_API int q4_quantize(const float* w, int64_t N, int64_t K, q4_weight** out, cudaStream_t stream);
+
+/* Create a handle from canonical blocks in host memory (N*K/32*18 bytes).
+ * Rejects blocks whose scale is not finite (Q4_ERR_NONFINITE).  Synchronous. */
+Q4_API int q4_import_blocks(const void* host_blocks, int64_t N, int64_t K, q4_weight** out,
+                     cudaStream_t stream);
+
+/* Write the canonical blocks (N*K/32*18 bytes) of W to host memory.
+ * bytes must be at least that size.  Synchronous. */
+Q4_API int q4_export_blocks(const q4_weight* W, void* host_blocks, size_t bytes);
+
+/* Release a handle and its device memory (after the work that uses it). */
+Q4_API int q4_weight_free(q4_weight* W);
+
+/* Shape and device footprint of a handle. */
+Q4_API int q4_weight_shape(const q4_weight* W, int64_t* N, int64_t* K);
+Q4_API int q4_weight_device_bytes(const q4_weight* W, size_t* bytes);
+
+/* y = x @ W^T.
+ *   x   device, fp32 [M, K] row-major, 16-byte aligned.
+ *   y   device, fp32 [M, N] row-major, 16-byte aligned; fully overwritten.
+ *   M   0 <= M <= Q4MM_M_MAX; M = 0 is a no-op returning Q4_OK.
+ * Picks the kernel from the measured M threshold (q4mm_get_m_threshold).
+ * Result per element within 1e-5 * sum_k |w x| + 1e-6 of the exact value. */
+Q4_API int q4mm_forward(const q4_weight* W, const float* x, float* y, int64_t M, cudaStream_t stream);
+
+/* q4mm_forward with Q4MM_* flags (batch-invariant mode, forced path, ablation). */
+Q4_API int q4mm_forward_ex(const q4_weight* W, const float* x, float* y, int64_t M, uint32_t flags,
+                    cudaStream_t stream);
+
+/* Greedy pick per row (the LM-head use, §"Same Prompt, Different Story"):
+ * idx[m] = argmax_n y[m, n] with the lowest index on exact ties and NaN never
+ * winning, without writing y.
+ *   idx     device, int32 [M].
+ *   maxval  device, fp32 [M] receiving y[m, idx[m]], or NULL. */
+Q4_API int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
+                cudaStream_t stream);
+Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
+                   uint32_t flags, cudaStream_t stream);
+
+/* The kernel path (Q4MM_PATH_*) a call with these arguments would take, or a
+ * negative status. */
+Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
+
+/* Plan of a call with these arguments, without running it: *path receives
+ * the Q4MM_PATH_* value, *launches the number of kernel launches the call
+ * makes, *splits the K partition count.  Any output pointer may be NULL. */
+Q4_API int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int* launches,
+                          int* splits);
+
+/* The M threshold: calls with M >= threshold take the tensor-core path, smaller
+ * M the CUDA-core streaming path (the kernel-switch threshold that
+ * §"Row-by-Row GEMV to the Rescue" says must be measured, not assumed).
+ * The default is the value measured on GB300; set_m_threshold overrides it for
+ * the process (1 = always tensor cores; Q4MM_M_MAX + 1 = never). */
+Q4_API int q4mm_set_m_threshold(int64_t m);
+Q4_API int64_t q4mm_get_m_threshold(void);
+
+/* Synchronize the current device and return (then clear) the device status
+ * word: Q4_OK, or Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out, or
+ * Q4_ERR_CUDA if the device reports an error. */
+Q4_API int q4_device_status(void);
+
+/* Human-readable name of a status code (static storage). */
+Q4_API const char* q4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4MM_H */

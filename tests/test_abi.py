@@ -1,0 +1,64 @@
+"""Host-side checks of the C ABI that need no GPU: the shared library builds
+and loads, exports every symbol ``include/q4mm.h`` declares, and rejects bad
+arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def q4():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import bit_quantized_matmul_gb300 as q4
+
+    return q4
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "q4mm.h")).read()
+    return sorted(set(re.findall(r"^Q4_API\s+[\w\s\*]+?\b(q4\w*)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("q4_quantize", "q4mm_forward", "q4mm_argmax", "q4_import_blocks", "q4_export_blocks"):
+        assert want in names
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(q4):
+    lib = ctypes.CDLL(q4.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert sorted(q4.EXPORTS) == _declared()
+
+
+def test_status_strings_and_threshold(q4):
+    assert q4.q4_status_string(q4.Q4_OK) == "ok"
+    assert "aligned" in q4.q4_status_string(q4.Q4_ERR_ALIGN)
+    assert q4.q4_status_string(12345) == "unknown status"
+    old = q4.q4mm_get_m_threshold()
+    assert old >= 1
+    q4.q4mm_set_m_threshold(7)
+    assert q4.q4mm_get_m_threshold() == 7
+    q4.q4mm_set_m_threshold(old)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.q4mm_set_m_threshold(0)
+    assert e.value.status == q4.Q4_ERR_INVALID_ARG
+
+
+def test_null_arguments_rejected_on_host(q4):
+    lib = q4.raw_library()
+    assert lib.q4mm_forward(None, None, None, 4, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_forward_ex(None, None, None, 4, 0, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_argmax(None, None, None, None, 4, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4_quantize(None, 4, 32, None, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4_weight_free(None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4_export_blocks(None, None, 0) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_select_path(None, 1, 0) == -q4.Q4_ERR_INVALID_ARG
