@@ -38,6 +38,20 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _foreign_binary(path: str) -> bool:
+    """True if `path` is an ELF file built for another CPU architecture."""
+    import platform
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF" or want is None:
+        return False
+    return int.from_bytes(head[18:20], "little") != want
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(OBJDIR, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
@@ -61,7 +75,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(OUT, objs):
+    if force or jobs or _stale(OUT, objs) or _foreign_binary(OUT):
         tmp = OUT + ".%d.tmp" % os.getpid()
         run([cc] + ARCH + ["-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-o", tmp] + objs)
         os.replace(tmp, OUT)

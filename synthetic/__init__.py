@@ -33,8 +33,22 @@ LM_HEAD = (152064, 3584)
 WEIGHT_SIGMA = 0.02
 
 
+def _foreign_binary(path: str) -> bool:
+    """True if `path` is an ELF file built for another CPU architecture."""
+    import platform
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF" or want is None:
+        return False
+    return int.from_bytes(head[18:20], "little") != want
+
+
 def build(force: bool = False) -> str:
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC) or _foreign_binary(_LIB):
         tmp = _LIB + ".%d.tmp" % os.getpid()
         subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fopenmp",
                                "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
