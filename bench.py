@@ -416,6 +416,68 @@ def run_gpu(args):
     return 0
 
 
+def run_path_sweep(args):
+    """Measure both kernel paths (CUDA-core streaming vs tensor-core) per M on
+    the 7B shapes; the crossover is the library's M threshold."""
+    import torch
+
+    import bit_quantized_matmul_gb300 as q4
+    import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    layers = args.layers
+    stack = build_stack(q4, torch, dev, layers)
+    stream = torch.cuda.Stream(dev)
+    sweep = (1, 2, 3, 4, 5, 6, 8, 16, 32, 64, 128, 256)
+    paths = {"simt": q4.Q4MM_FORCE_SIMT, "tc": q4.Q4MM_FORCE_TC}
+    out = {}
+    for M in sweep:
+        xs = {K: torch.from_numpy(synthetic.normal(synthetic.act_seed(5, M) + K, (M, K))).to(dev)
+              for K in (3584, 18944)}
+        for name in ("q_proj", "k_proj", "gate_proj", "down_proj"):
+            N, K = synthetic.QWEN7B_LINEARS[name]
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            for pname, flags in paths.items():
+                def issue():
+                    for W in stack[name]:
+                        q4.q4mm_forward_ex(W, xs[K], flags, y=y, stream=stream)
+                with torch.cuda.stream(stream):
+                    issue()
+                torch.cuda.synchronize(dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    issue()
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        g.replay()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(5):
+                        g.replay()
+                    b.record(stream)
+                torch.cuda.synchronize(dev)
+                us = a.elapsed_time(b) * 1e3 / (5 * layers)
+                wb = N * K * BLOCK_BYTES_PER_WEIGHT
+                out.setdefault(name, {}).setdefault(str(M), {})[pname] = {
+                    "us": us, "weight_gbs": wb / us / 1e3, "rows_per_s": M / us * 1e6}
+                del g
+    # threshold: smallest M from which the tensor-core path is at least as fast
+    # on the large shapes (gate, down) for every larger M of the sweep
+    thr = None
+    for i, M in enumerate(sweep):
+        if all(out[n][str(m)]["tc"]["us"] <= out[n][str(m)]["simt"]["us"]
+               for n in ("gate_proj", "down_proj") for m in sweep[i:]):
+            thr = M
+            break
+    print(json.dumps({"path_sweep": out, "measured_threshold": thr, "layers": layers,
+                      "sweep": list(sweep)}), flush=True)
+    for name in TYPES:
+        for W in stack[name]:
+            W.free()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,7 +486,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path-sweep", action="store_true",
+                    help="time both kernel paths per M and print the measured M threshold")
     args = ap.parse_args()
+    if args.path_sweep:
+        return run_path_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
