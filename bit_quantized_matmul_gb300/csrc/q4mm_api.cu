@@ -96,7 +96,8 @@ int alloc_weight(int64_t N, int64_t K, int dev, Weight* W) {
 
 int check_shape(int64_t N, int64_t K) {
   if (N < 1 || K < BLOCK_K || (K % BLOCK_K) != 0) return Q4_ERR_SHAPE;
-  if (N > (int64_t)1 << 31 || K / BLOCK_K > 65535) return Q4_ERR_SHAPE;  // grid.y = K/32
+  // grid limits: K/32 blocks and N/128 tiles are grid dimensions of 65535 max
+  if (pad_n(N) / TILE_N > 65535 || K / BLOCK_K > 65535) return Q4_ERR_SHAPE;
   return Q4_OK;
 }
 

@@ -1,34 +1,43 @@
 // q4mm_tc.cu — tensor-core (tcgen05 / TMEM) path of the Q4_0 matmul.
 //
-// For M token rows this is the "GEMM" side of the kernel split described in
+// For several token rows this is the "GEMM" side of the kernel split in
 // "Why Continuous Batching Slowed Down My LLM Inference Engine"
-// (§"Two Rows of Input, Two Different Kernels"): many rows processed together
-// so each weight read serves all of them ("Why LLM Decoding Is Slow, and Why
-// Batching Is (Almost) Free", §4).  Dequantization happens on the fly in the
-// kernel; the weights are streamed from HBM exactly once per CTA pass.
+// (§"Two Rows of Input, Two Different Kernels"): all rows of the call share
+// one pass over the weights ("Why LLM Decoding Is Slow, and Why Batching Is
+// (Almost) Free", §4 "Share the Weights Across Users"), and the 4-bit
+// weights are dequantized on the fly inside the kernel.
 //
-// Exactness.  The contraction must match the fp64 reference to about fp32
-// accuracy, so operands are exact:
-//   A (weights)   = (q - 8), small integers, exact in bf16, written by the
-//                   CUDA cores straight into tensor memory (no smem round
-//                   trip): bf16(128 + q) is 0x4300 | q, minus 136 is exact;
-//   B (activations) = x split into three bf16 terms x0 + x1 + x2 == x
-//                   exactly (a pre-pass kernel), accumulated by three MMAs
-//                   into the same fp32 accumulator;
-//   the per-block scale d is applied on the CUDA cores: for each 32-weight
-//   block the 128 x M_TILE accumulator D_b = sum_{k in b} (q-8) x is read
-//   from TMEM and folded as acc = fma(d, D_b, acc).
+// Exactness.  The result must match the fp64 reference to about fp32
+// accuracy, so the tensor-core operands are exact:
+//   A (weights)     (q - 8), small integers, exact in bf16, written by the
+//                   CUDA cores straight into tensor memory: bf16(128 + q) is
+//                   0x4300 | q, and subtracting 136 is exact;
+//   B (activations) x split into three bf16 terms x0 + x1 + x2 == x exactly
+//                   (pre-pass kernel), stacked along the MMA's N dimension
+//                   (term t of token row m is B row t*MTR + m), so one
+//                   128 x NB x 16 MMA covers every term and row of a tile;
+//   per-block scale the fp16 scale d of each 32-weight block is applied on
+//                   the CUDA cores: the block's accumulator
+//                   D_b[n, t*MTR + m] = sum_{k in b} (q-8) x_t[m, k] is read
+//                   back from TMEM and folded as acc = fma(d, (D0+D1)+D2, acc).
 //
-// Per CTA: one 128-row weight tile (one TMEM lane per row), one K range (a
-// fixed split that depends on N and K only), one tile of M_TILE token rows.
-// Warp roles (320 threads):
-//   warps 0-7  convert + epilogue.  Warp w serves TMEM lane quarter w % 4;
-//              warps 0-3 take even blocks, warps 4-7 odd blocks.
-//   warp 8     TMA producer: 1-D bulk copies of nibbles, scales and the
-//              activation operand of one block per smem stage.
-//   warp 9     TMEM allocator and the single MMA-issuing thread.
-// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
-// Q4_ERR_TIMEOUT in the device status word, drains what it issued and exits.
+// Work decomposition.  CTA = one 128-row weight tile (a TMEM lane per row) x
+// one K range (a split that depends on N and K only) x one tile of MTR token
+// rows (MTR = NB/3).  The K range is processed in units of U = 4 blocks; every
+// barrier, bulk copy and commit is per unit, because each such operation
+// costs tens of cycles of issue latency in the thread that executes it.
+// Roles (704 threads):
+//   warps  0- 7  converters: nibbles -> bf16 (q-8) in the TMEM A ring; two
+//                groups of four (one per TMEM lane quarter) take alternate units
+//   warps  8-15  epilogue: TMEM D ring -> scale -> fp32 accumulators; two
+//                groups take alternate units; their sums are added in a fixed
+//                order (even units + odd units) at the end
+//   warps 16-17  bulk-copy producers (alternate units): nibbles, scales and
+//                the activation operand of a unit into one smem stage
+//   warps 18-21  MMA issuers (every fourth unit each); warp 18 also owns the
+//                TMEM allocation
+// Every mbarrier wait is bounded; on expiry the CTA records Q4_ERR_TIMEOUT in
+// the device status word, drains what it issued, frees TMEM and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,40 +46,56 @@
 namespace q4 {
 namespace {
 
-constexpr int TC_THREADS = 320;
-constexpr int MATH_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int U = 4;                    // blocks per unit
+constexpr int CONV_WARP0 = 0;           // 8 warps
+constexpr int EPI_WARP0 = 8;            // 8 warps
+constexpr int PROD_WARP0 = 16;          // 2 warps
+constexpr int MMA_WARP0 = 18;           // 4 warps
+constexpr int NPROD = 2;
+constexpr int NISS = 4;
+constexpr int TC_THREADS = 22 * 32;
 constexpr int TMEM_COLS = 512;
-constexpr int MAX_STAGES = 32;
+constexpr int MAX_STAGES = 16;
+// Barriers are per unit, in a ring of NBR units: unit u uses index u % NBR at
+// phase parity (u / NBR) & 1.  Every role handles its units in order and NBR is
+// a multiple of the role strides (2 and 4), so a waiter has always observed the
+// previous phase of the same barrier before it waits for the next one; a
+// parity wait can never run two phases ahead, however the four MMA issuers and
+// the independently progressing warps interleave.
+constexpr int NBR = 64;
 constexpr int SMEM_BUDGET = 200 * 1024;
-constexpr int LAG = 2;  // iterations between converting a block and reading its accumulator
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s bound on any wait
 
-template <int MT>
+template <int NB>
 struct Cfg {
-  static constexpr int NIB_BYTES = TILE_N * 16;            // 2048
-  static constexpr int SCL_BYTES = TILE_N * 2;             // 256
-  static constexpr int BOP_BYTES = 192 * MT;               // 3 terms x 2 k-steps x MT rows x 16 k x 2 B
-  static constexpr int STAGE_BYTES = NIB_BYTES + SCL_BYTES + BOP_BYTES;
-  static constexpr int SLOT_COLS = 16 + MT;                // A: 16 columns, D: MT columns
-  static constexpr int NSLOT = ((TMEM_COLS / SLOT_COLS) / 2) * 2;
-  static constexpr int DSL_BYTES = NSLOT * TILE_N * 4;
-  static constexpr int BAR_BYTES = (2 * MAX_STAGES + 2 * 16 + 4) * 8;
-  static constexpr int NST_RAW = (SMEM_BUDGET - DSL_BYTES - BAR_BYTES - 64) / STAGE_BYTES;
+  static constexpr int MTR = NB / 3;                   // token rows per CTA
+  static constexpr int NIB_BYTES = U * TILE_N * 16;    // 8 KB
+  static constexpr int SCL_OFF = NIB_BYTES;
+  static constexpr int SCL_BYTES = U * TILE_N * 2;     // 1 KB
+  static constexpr int BOP_OFF = SCL_OFF + SCL_BYTES;
+  static constexpr int BOP_BLOCK = 64 * NB;            // 2 k-steps x NB rows x 16 k x 2 B
+  static constexpr int STAGE_BYTES = BOP_OFF + U * BOP_BLOCK;
+  static constexpr int A_UNIT_COLS = U * 16;           // 64
+  static constexpr int D_UNIT_COLS = U * NB;
+  static constexpr int NA = NB == 16 ? 3 : 2;
+  static constexpr int ND = (TMEM_COLS - NA * A_UNIT_COLS) / D_UNIT_COLS;
+  static constexpr int NSC = NA + ND;                  // scale ring (units)
+  static constexpr int DSL_BYTES = NSC * U * TILE_N * 4;
+  static constexpr int BAR_BYTES = 6 * NBR * 8 + 16;
+  static constexpr int NST_RAW = (SMEM_BUDGET - DSL_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_RAW > MAX_STAGES ? MAX_STAGES : NST_RAW;
-  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + DSL_BYTES + BAR_BYTES + 64;
-  static_assert(NSLOT >= 2 * (LAG + 1), "TMEM slots must cover the conversion lag");
-  static_assert(NSLOT <= 16, "barrier area sized for 16 slots");
-  static_assert(NST >= 4, "pipeline too shallow");
-  static_assert(MT % 16 == 0 && MT <= 64, "M tile");
-  static_assert(MT * TILE_N * 4 <= NST * STAGE_BYTES, "group-combine buffer");
+  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + DSL_BYTES + BAR_BYTES;
+  static_assert(NA * A_UNIT_COLS + ND * D_UNIT_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(ND >= 3 && NA >= 2 && NST >= 6, "pipeline too shallow");
+  static_assert(NBR % 4 == 0 && NBR > 2 * (NST + NA + ND), "barrier ring depth");
+  static_assert(MTR * TILE_N * 4 <= NST * STAGE_BYTES, "group-combine buffer");
+  static_assert(NB == 16 || NB == 32, "MMA N");
 };
 
 struct TcArgs {
   const uint8_t* nib;
   const uint16_t* d;
-  const uint8_t* xop;  // activation operand, [mtiles][KB][192*MT] bytes
+  const uint8_t* xop;  // activation operand, [mtiles][KB][64*NB] bytes
   int64_t KB, K, N, N_pad;
   int64_t M;           // rows in this launch
   float* y;
@@ -127,17 +152,53 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait: returns false (and raises the CTA error flag) if the phase
 // does not complete within WAIT_NS, or if another role already gave up.
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// parked (it stops competing for issue slots) until the phase completes or
+// the hint elapses.
+constexpr uint32_t SUSPEND_NS = 1000000u;  // 1 ms per try
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(SUSPEND_NS)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false (and the CTA error flag raised) if the phase does not
+// complete within WAIT_NS, or if another role already gave up.  The timer is
+// read only after a try has expired, off the common path.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u) {
-      if (*err) return false;
-      if (globaltimer() - t0 > WAIT_NS) {
-        *err = 1;
-        return false;
-      }
+  unsigned long long t0 = 0;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*err) return false;
+    const unsigned long long now = globaltimer();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > WAIT_NS) {
+      *err = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded wait used only while draining (no error flag to consult).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  unsigned long long t0 = 0;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return;
+    const unsigned long long now = globaltimer();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > WAIT_NS) {
+      return;
     }
   }
 }
@@ -187,14 +248,20 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -234,12 +301,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-// (q - 8) for the nibble pair at bits (4p, 16 + 4p) of w, as exact bf16x2.
+// (q - 8) for the nibble pair at bits (4p, 16 + 4p) of w, as exact bf16x2:
+// (w >> 4p) & 0x000F000F | 0x43004300 is the pair bf16(128 + q), and one
+// bf16x2 FMA, x * 1.0 + (-136.0), gives q - 8 exactly.
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
-  const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16 (128 + q) pair
-  __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&t);
-  h = __hsub2(h, __floats2bfloat162_rn(136.0f, 136.0f));
-  return *reinterpret_cast<const uint32_t*>(&h);
+  const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
+  return r;
 }
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t n) {
@@ -257,24 +326,26 @@ __device__ __forceinline__ float key_value(unsigned long long k) {
 }
 
 // ----------------------------------------------------------------------------
-// Pre-pass: x[M, K] fp32 -> activation operand, three exact bf16 terms, laid
-// out per (m tile, block) as the MMA reads it:
-//   [k-step s (2)][term t (3)][k group g (2)][row group rg (MT/8)][row (8)][8 k]
-// One thread per (m tile, block, row, s, g): 8 consecutive k of one row.
+// Pre-pass: x[M, K] fp32 -> activation operand: three exact bf16 terms per
+// value, laid out per (m tile, block) exactly as the MMA reads it from smem,
+//   [k-step s (2)][k group g (2)][B row (NB)][8 k]   (16-byte rows)
+// with B row t*MTR + m holding term t of token row m, and rows >= 3*MTR zero.
+// One thread per (m tile, block, s, g, token row in tile).
 // ----------------------------------------------------------------------------
-template <int MT>
+template <int NB>
 __global__ void __launch_bounds__(256) xop_kernel(const float* __restrict__ x, int64_t M, int64_t K,
                                                   int64_t KB, int mtiles, uint8_t* __restrict__ xop) {
+  constexpr int MTR = NB / 3;
   asm volatile("griddepcontrol.launch_dependents;");
-  const int64_t total = (int64_t)mtiles * KB * MT * 4;
+  const int64_t total = (int64_t)mtiles * KB * 4 * MTR;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
-    const int sg = (int)(t & 3);
-    const int rr = (int)((t >> 2) % MT);
-    const int64_t b = (t >> 2) / MT % KB;
-    const int64_t mt = (t >> 2) / MT / KB;
+    const int mm = (int)(t % MTR);
+    const int sg = (int)((t / MTR) & 3);
+    const int64_t b = (t / MTR / 4) % KB;
+    const int64_t mt = t / MTR / 4 / KB;
     const int s = sg >> 1, g = sg & 1;
-    const int64_t m = mt * MT + rr;
+    const int64_t m = mt * MTR + mm;
     float v[8];
     if (m < M) {
       const float4* src = reinterpret_cast<const float4*>(x + m * K + b * BLOCK_K + s * 16 + g * 8);
@@ -300,13 +371,14 @@ __global__ void __launch_bounds__(256) xop_kernel(const float* __restrict__ x, i
       out[1][e / 2] = *reinterpret_cast<uint32_t*>(&p1);
       out[2][e / 2] = *reinterpret_cast<uint32_t*>(&p2);
     }
-    uint8_t* base = xop + (mt * KB + b) * (int64_t)(192 * MT);
-    const int rg = rr >> 3, r8 = rr & 7;
+    uint8_t* chunk = xop + (mt * KB + b) * (int64_t)(64 * NB) + (int64_t)(s * 2 + g) * NB * 16;
 #pragma unroll
-    for (int term = 0; term < 3; ++term) {
-      const int64_t off = ((((int64_t)(s * 3 + term) * 2 + g) * (MT / 8) + rg) * 8 + r8) * 16;
-      *reinterpret_cast<uint4*>(base + off) =
+    for (int term = 0; term < 3; ++term)
+      *reinterpret_cast<uint4*>(chunk + (term * MTR + mm) * 16) =
           make_uint4(out[term][0], out[term][1], out[term][2], out[term][3]);
+    if (mm == 0) {
+      for (int r = 3 * MTR; r < NB; ++r)
+        *reinterpret_cast<uint4*>(chunk + r * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 }
@@ -314,193 +386,245 @@ __global__ void __launch_bounds__(256) xop_kernel(const float* __restrict__ x, i
 // ----------------------------------------------------------------------------
 // Main kernel
 // ----------------------------------------------------------------------------
-template <int MT>
+template <int NB>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
-  using C = Cfg<MT>;
+  using C = Cfg<NB>;
+  constexpr int MTR = C::MTR;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float* dsl = reinterpret_cast<float*>(smem + C::NST * C::STAGE_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE_BYTES + C::DSL_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + MAX_STAGES;
-  uint64_t* afull = bars + 2 * MAX_STAGES;
-  uint64_t* dfull = bars + 2 * MAX_STAGES + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 32);
+  uint64_t* full = bars;           // unit data landed in its smem stage (tx count)
+  uint64_t* empty = full + NBR;    // stage consumed: 4 converter warps + MMA commit
+  uint64_t* afull = empty + NBR;   // A operand written to TMEM: 4 converter warps
+  uint64_t* afree = afull + NBR;   // MMAs of the unit done (A slot reusable): commit
+  uint64_t* dfull = afree + NBR;   // accumulators of the unit ready: commit
+  uint64_t* dfree = dfull + NBR;   // accumulators read back: 4 epilogue warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfree + NBR);
   volatile int* err = reinterpret_cast<volatile int*>(tmem_slot + 2);
   __shared__ int s_last;
+  __shared__ unsigned long long red[4][MTR];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, split = blockIdx.y, mt = blockIdx.z;
+  const int mt = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
   const int64_t kb0 = (int64_t)split * a.kb_per_split;
   const int64_t kb1 = min(a.KB, kb0 + a.kb_per_split);
   const int nblk = (int)(kb1 - kb0);
+  const int nunits = (nblk + U - 1) / U;
+  const int64_t m0 = (int64_t)mt * MTR;
+  const int mcount = (int)min((int64_t)MTR, a.M - m0);
 
   if (tid == 0) {
-    for (int i = 0; i < C::NST; ++i) {
+    for (int i = 0; i < NBR; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 4 + 1);
-    }
-    for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(smem_u32(&afull[i]), 4);
+      mbar_init(smem_u32(&afree[i]), 1);
       mbar_init(smem_u32(&dfull[i]), 1);
+      mbar_init(smem_u32(&dfree[i]), 4);
     }
     *err = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == MMA_WARP) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == MMA_WARP0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t a_base = tmem;                                    // A ring columns
+  const uint32_t d_base = tmem + (uint32_t)(C::NA * C::A_UNIT_COLS);  // D ring columns
 
-  float acc[MT];
+  float acc[MTR];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+  for (int m = 0; m < MTR; ++m) acc[m] = 0.0f;
 
-  if (warp == PRODUCER_WARP) {
+  if (warp >= PROD_WARP0 && warp < PROD_WARP0 + NPROD) {
+    // ---------------- producers ----------------
     if (lane == 0) {
+      const int p = warp - PROD_WARP0;
       asm volatile("griddepcontrol.wait;" ::: "memory");
       const uint8_t* nib_base = a.nib + ((int64_t)tile * a.KB + kb0) * TILE_N * 16;
       const uint8_t* scl_base =
           reinterpret_cast<const uint8_t*>(a.d + ((int64_t)tile * a.KB + kb0) * TILE_N);
-      const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB + kb0) * (int64_t)C::BOP_BYTES;
-      int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % C::NST;
-        if (!mbar_wait(smem_u32(&empty[st]), ((j / C::NST) & 1) ^ 1, err)) break;
-        const uint32_t sb = smem_u32(stages + st * C::STAGE_BYTES);
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_expect_tx(fb, C::STAGE_BYTES);
-        bulk_g2s(sb, nib_base + (int64_t)j * C::NIB_BYTES, C::NIB_BYTES, fb);
-        bulk_g2s(sb + C::NIB_BYTES, scl_base + (int64_t)j * C::SCL_BYTES, C::SCL_BYTES, fb);
-        bulk_g2s(sb + C::NIB_BYTES + C::SCL_BYTES, bop_base + (int64_t)j * C::BOP_BYTES,
-                 C::BOP_BYTES, fb);
-        issued = j + 1;
-      }
-      // drain: every issued copy has landed before the CTA may exit
-      for (int j = max(0, issued - C::NST); j < issued; ++j) {
-        const uint32_t fb = smem_u32(&full[j % C::NST]);
-        const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(fb, (j / C::NST) & 1) && globaltimer() - t0 < WAIT_NS) {
+      const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB + kb0) * (int64_t)C::BOP_BLOCK;
+      int last = -1;
+      for (int u = p; u < nunits; u += NPROD) {
+        const int st = u % C::NST;
+        const int ub = min(U, nblk - u * U);
+        if (u >= C::NST) {  // stage reuse: unit u - NST must be consumed
+          const int v = u - C::NST;
+          if (!mbar_wait(smem_u32(&empty[v % NBR]), (v / NBR) & 1, err)) break;
         }
+        const uint32_t sb = smem_u32(stages + st * C::STAGE_BYTES);
+        const uint32_t fb = smem_u32(&full[u % NBR]);
+        mbar_expect_tx(fb, (uint32_t)(ub * (TILE_N * 16 + TILE_N * 2 + C::BOP_BLOCK)));
+        bulk_g2s(sb, nib_base + (int64_t)u * U * TILE_N * 16, ub * TILE_N * 16, fb);
+        bulk_g2s(sb + C::SCL_OFF, scl_base + (int64_t)u * U * TILE_N * 2, ub * TILE_N * 2, fb);
+        bulk_g2s(sb + C::BOP_OFF, bop_base + (int64_t)u * U * C::BOP_BLOCK, ub * C::BOP_BLOCK, fb);
+        last = u;
       }
+      // drain: every copy this producer issued has landed before the CTA exits
+      for (int u = last; u >= 0 && u > last - C::NST; u -= NPROD)
+        mbar_drain(smem_u32(&full[u % NBR]), (u / NBR) & 1);
     }
-  } else if (warp == MMA_WARP) {
+  } else if (warp >= MMA_WARP0) {
+    // ---------------- MMA issuers ----------------
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16(MT);
-      int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % C::NST, sl = j % C::NSLOT;
-        if (!mbar_wait(smem_u32(&full[st]), (j / C::NST) & 1, err)) break;
-        if (!mbar_wait(smem_u32(&afull[sl]), (j / C::NSLOT) & 1, err)) break;
+      constexpr uint32_t IDESC = idesc_bf16(NB);
+      const int iss = warp - MMA_WARP0;
+      int last = -1;
+      for (int u = iss; u < nunits; u += NISS) {
+        const int st = u % C::NST, sa = u % C::NA, sd = u % C::ND;
+        const int ub = min(U, nblk - u * U);
+        const int bi = u % NBR;
+        const uint32_t par = (u / NBR) & 1;
+        if (!mbar_wait(smem_u32(&full[bi]), par, err)) break;
+        if (!mbar_wait(smem_u32(&afull[bi]), par, err)) break;
+        if (u >= C::ND) {  // D slot reuse: unit u - ND must be read back
+          const int v = u - C::ND;
+          if (!mbar_wait(smem_u32(&dfree[v % NBR]), (v / NBR) & 1, err)) break;
+        }
         tc_fence_after();
-        const uint32_t bop = smem_u32(stages + st * C::STAGE_BYTES + C::NIB_BYTES + C::SCL_BYTES);
-        const uint32_t a_col = tmem + (uint32_t)(sl * C::SLOT_COLS);
-        const uint32_t d_col = a_col + 16u;
+        const uint32_t bop = smem_u32(stages + st * C::STAGE_BYTES + C::BOP_OFF);
+        const uint32_t acol = a_base + (uint32_t)(sa * C::A_UNIT_COLS);
+        const uint32_t dcol = d_base + (uint32_t)(sd * C::D_UNIT_COLS);
+        for (int b = 0; b < ub; ++b) {
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-#pragma unroll
-          for (int t = 0; t < 3; ++t) {
-            const uint64_t bd = smem_desc(bop + (uint32_t)((s * 3 + t) * 32 * MT), 16u * MT, 128u);
-            mma_ts(d_col, a_col + 8u * s, bd, IDESC, (s | t) != 0);
+          for (int s = 0; s < 2; ++s) {
+            const uint64_t bd = smem_desc(bop + (uint32_t)(b * C::BOP_BLOCK + s * 32 * NB), 16u * NB, 128u);
+            mma_ts(dcol + (uint32_t)(b * NB), acol + (uint32_t)(b * 16 + 8 * s), bd, IDESC, s != 0);
           }
         }
-        mma_commit(smem_u32(&dfull[sl]));
-        mma_commit(smem_u32(&empty[st]));
-        issued = j + 1;
+        mma_commit(smem_u32(&afree[bi]));
+        mma_commit(smem_u32(&dfull[bi]));
+        mma_commit(smem_u32(&empty[bi]));
+        last = u;
       }
-      if (issued > 0) {  // drain: the last commit covers every MMA issued
-        const int j = issued - 1;
-        const uint32_t db = smem_u32(&dfull[j % C::NSLOT]);
-        const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(db, (j / C::NSLOT) & 1) && globaltimer() - t0 < WAIT_NS) {
-        }
-      }
+      if (last >= 0)  // drain: the last commit covers every MMA this thread issued
+        mbar_drain(smem_u32(&dfull[last % NBR]), (last / NBR) & 1);
     }
     __syncwarp();
-  } else {
-    // ---- convert + epilogue warps ----
-    const int q = warp & 3, g = warp >> 2;
+  } else if (warp < EPI_WARP0) {
+    // ---------------- converters ----------------
+    const int q = warp & 3, g = (warp - CONV_WARP0) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const int n_g = nblk > g ? (nblk - g + 1) / 2 : 0;
-    for (int i = 0; i < n_g + LAG; ++i) {
-      if (i < n_g) {
-        const int j = g + 2 * i;
-        const int st = j % C::NST, sl = j % C::NSLOT;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[st]), (j / C::NST) & 1, err))) break;
-        const uint8_t* sp = stages + st * C::STAGE_BYTES;
-        const uint4 v = *reinterpret_cast<const uint4*>(sp + row * 16);
-        const uint16_t dh = *reinterpret_cast<const uint16_t*>(sp + C::NIB_BYTES + row * 2);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-        dsl[sl * TILE_N + row] = __half2float(__ushort_as_half(dh));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        uint32_t av[16];
+    for (int u = g; u < nunits; u += 2) {
+      const int st = u % C::NST, sa = u % C::NA;
+      const int ub = min(U, nblk - u * U);
+      const int bi = u % NBR;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[bi]), (u / NBR) & 1, err))) break;
+      const uint8_t* sp = stages + st * C::STAGE_BYTES;
+      uint4 v[U];
+      float dsc[U];
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-#pragma unroll
-          for (int p = 0; p < 4; ++p) av[4 * w + p] = nib_pair_bf16(wv[w], p);
-        tmem_st16(tmem + lane_off + (uint32_t)(sl * C::SLOT_COLS), av);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[sl]));
-      }
-      if (i >= LAG) {
-        const int j = g + 2 * (i - LAG);
-        const int sl = j % C::NSLOT;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&dfull[sl]), (j / C::NSLOT) & 1, err)))
-          break;
-        tc_fence_after();
-        const float dsc = dsl[sl * TILE_N + row];
-        const uint32_t dcol = tmem + lane_off + (uint32_t)(sl * C::SLOT_COLS + 16);
-#pragma unroll
-        for (int c = 0; c < MT; c += 16) {
-          float dv[16];
-          tmem_ld16(dcol + (uint32_t)c, dv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc[c + e] = fmaf(dsc, dv[e], acc[c + e]);
+      for (int b = 0; b < U; ++b) {
+        if (b < ub) {
+          v[b] = *reinterpret_cast<const uint4*>(sp + b * TILE_N * 16 + row * 16);
+          const uint16_t dh = *reinterpret_cast<const uint16_t*>(sp + C::SCL_OFF + b * TILE_N * 2 + row * 2);
+          dsc[b] = __half2float(__ushort_as_half(dh));
+        } else {
+          v[b] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+          dsc[b] = 0.0f;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[bi]));
+      if (u >= C::NA) {  // A slot reuse: the MMAs of unit u - NA must be done
+        const int w = u - C::NA;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&afree[w % NBR]), (w / NBR) & 1, err))) break;
+      }
+      // The scale slot u % NSC was last read by the epilogue of unit u - NSC;
+      // the wait above orders it: MMA(u - NA) waited for the read-back of unit
+      // u - NA - ND = u - NSC.
+      float* dslu = dsl + (u % C::NSC) * (U * TILE_N);
+#pragma unroll
+      for (int b = 0; b < U; ++b) dslu[b * TILE_N + row] = dsc[b];
+      const uint32_t acol = a_base + lane_off + (uint32_t)(sa * C::A_UNIT_COLS);
+#pragma unroll
+      for (int h = 0; h < U / 2; ++h) {
+        uint32_t av[32];
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const uint32_t wv[4] = {v[2 * h + bb].x, v[2 * h + bb].y, v[2 * h + bb].z, v[2 * h + bb].w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) av[16 * bb + 4 * w + pp] = nib_pair_bf16(wv[w], pp);
+        }
+        tmem_st32(acol + (uint32_t)(32 * h), av);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&afull[bi]));
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3, g = (warp - EPI_WARP0) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    for (int u = g; u < nunits; u += 2) {
+      const int sd = u % C::ND;
+      const int ub = min(U, nblk - u * U);
+      const int bi = u % NBR;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&dfull[bi]), (u / NBR) & 1, err))) break;
+      tc_fence_after();
+      const float* dslu = dsl + (u % C::NSC) * (U * TILE_N);
+      const uint32_t dcol = d_base + lane_off + (uint32_t)(sd * C::D_UNIT_COLS);
+      for (int b = 0; b < ub; ++b) {
+        float dv[NB];
+#pragma unroll
+        for (int c = 0; c < NB; c += 16) {
+          float t16[16];
+          tmem_ld16(dcol + (uint32_t)(b * NB + c), t16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dv[c + e] = t16[e];
+        }
+        tmem_wait_ld();
+        const float dsc = dslu[b * TILE_N + row];
+#pragma unroll
+        for (int m = 0; m < MTR; ++m)
+          if (m < mcount) acc[m] = fmaf(dsc, (dv[m] + dv[MTR + m]) + dv[2 * MTR + m], acc[m]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&dfree[bi]));
     }
   }
 
-  // ---- combine the two block groups (fixed order: even + odd) ----
+  // ---- combine the two epilogue groups (fixed order: even units + odd units) ----
   tc_fence_before();
   __syncthreads();
   float* comb = reinterpret_cast<float*>(stages);
-  if (warp >= 4 && warp < MATH_WARPS) {
+  if (warp >= EPI_WARP0 + 4 && warp < EPI_WARP0 + 8) {
     const int row = (warp & 3) * 32 + lane;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) comb[m * TILE_N + row] = acc[m];
+    for (int m = 0; m < MTR; ++m) comb[m * TILE_N + row] = acc[m];
   }
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == MMA_WARP0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  const bool timed_out = *err != 0;
-  if (timed_out) {
+  if (*err != 0) {
     if (tid == 0) atomicOr(a.status, (unsigned)Q4_ERR_TIMEOUT);
     return;
   }
-  if (warp >= 4) return;  // warps 0-3 own the 128 rows from here on
+  if (warp < EPI_WARP0 || warp >= EPI_WARP0 + 4) return;  // warps 8-11 own the rows now
 
-  const int row = warp * 32 + lane;
+  const int row = (warp & 3) * 32 + lane;
   const int64_t n = (int64_t)tile * TILE_N + row;
-  const int64_t m0 = (int64_t)mt * MT;
-  const int mcount = (int)min((int64_t)MT, a.M - m0);
 #pragma unroll
-  for (int m = 0; m < MT; ++m) acc[m] += comb[m * TILE_N + row];
+  for (int m = 0; m < MTR; ++m) acc[m] += comb[m * TILE_N + row];
 
-  // named barrier over warps 0-3 only (128 threads)
+  // named barrier over the 128 threads of warps 8-11
   auto sync128 = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
 
   if (a.splits > 1) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int m = 0; m < MTR; ++m)
       if (m < mcount) a.partial[((int64_t)split * a.M + m0 + m) * a.N_pad + n] = acc[m];
     __threadfence();
     sync128();
@@ -512,7 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     if (!s_last) return;
     __threadfence();
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
+    for (int m = 0; m < MTR; ++m) {
       if (m < mcount) {
         float v = 0.0f;
         for (int s = 0; s < a.splits; ++s)
@@ -526,23 +650,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   if (a.idx == nullptr) {
     if (n < a.N) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
+      for (int m = 0; m < MTR; ++m)
         if (m < mcount) a.y[(m0 + m) * a.N + n] = acc[m];
     }
     return;
   }
 
   // ---- fused greedy pick ----
-  __shared__ unsigned long long red[4][MT];
+  const int w4 = warp & 3;
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
+  for (int m = 0; m < MTR; ++m) {
     unsigned long long k = (m < mcount && n < a.N) ? argmax_key(acc[m], (uint32_t)n) : 0ull;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, k, off);
       k = o > k ? o : k;
     }
-    if (lane == 0) red[warp][m] = k;
+    if (lane == 0) red[w4][m] = k;
   }
   sync128();
   if (row < mcount) {
@@ -570,28 +694,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
 
 constexpr int64_t TC_M_LAUNCH = 256;  // rows per launch pair (pre-pass + main)
 
-int mt_for(int64_t M, bool batch_invariant) {
-  if (batch_invariant) return 16;
-  return M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+// MMA N for a launch of ml rows.  Batch-invariant mode always uses NB = 32 so
+// that neither the instruction shape nor the token tile depends on M.
+int nb_for(int64_t ml, bool batch_invariant) {
+  if (batch_invariant) return 32;
+  return ml <= Cfg<16>::MTR ? 16 : 32;
 }
 
-template <int MT>
-int launch_mt(const Weight* W, const float* x, int64_t ml, float* y, int32_t* idx, float* maxval,
+template <int NB>
+int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* idx, float* maxval,
               const TcPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
-  using C = Cfg<MT>;
-  const int mtiles = (int)((ml + MT - 1) / MT);
+  using C = Cfg<NB>;
+  const int mtiles = (int)((ml + C::MTR - 1) / C::MTR);
   if (plan.splits > 1 && W->tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
-  // pre-pass
   {
-    const int64_t total = (int64_t)mtiles * W->KB * MT * 4;
+    const int64_t total = (int64_t)mtiles * W->KB * 4 * C::MTR;
     const int64_t want = (total + 255) / 256;
     const int blocks = (int)(want < 4096 ? want : 4096);
-    xop_kernel<MT><<<blocks, 256, 0, s>>>(x, ml, W->K, W->KB, mtiles, static_cast<uint8_t*>(ws.xop));
+    xop_kernel<NB><<<blocks, 256, 0, s>>>(x, ml, W->K, W->KB, mtiles, static_cast<uint8_t*>(ws.xop));
     if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
   }
   static bool attr_set[64] = {};
   if (!attr_set[W->device & 63]) {
-    if (cudaFuncSetAttribute(tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W->device & 63] = true;
@@ -619,7 +744,7 @@ int launch_mt(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.status = ws.status;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)W->tiles, (unsigned)plan.splits, (unsigned)mtiles);
+  cfg.gridDim = dim3((unsigned)mtiles, (unsigned)W->tiles, (unsigned)plan.splits);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
@@ -628,7 +753,7 @@ int launch_mt(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc_kernel<MT>, a) != cudaSuccess) return Q4_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_kernel<NB>, a) != cudaSuccess) return Q4_ERR_CUDA;
   return Q4_OK;
 }
 
@@ -638,16 +763,16 @@ bool tc_kernel_built() { return true; }
 
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   TcPlan p;
-  p.m_tile = mt_for(M < TC_M_LAUNCH ? M : TC_M_LAUNCH, batch_invariant);
+  p.m_tile = nb_for(M < TC_M_LAUNCH ? M : TC_M_LAUNCH, batch_invariant);
   // K partition from N and K only: fill the SMs with one CTA each, balancing
-  // waves against blocks per CTA.
+  // waves against units per CTA (+ a fixed per-CTA cost in unit terms).
   const int64_t tiles = W->tiles;
   int64_t best_s = 1, best_cost = -1;
-  const int64_t smax = W->KB < 32 ? W->KB : 32;
+  const int64_t smax = W->KB < 64 ? W->KB : 64;
   for (int64_t s = 1; s <= smax; ++s) {
     const int64_t kbps = (W->KB + s - 1) / s;
     const int64_t waves = (tiles * s + num_sms - 1) / num_sms;
-    const int64_t cost = waves * (kbps + 8);  // + per-CTA fixed cost in block units
+    const int64_t cost = waves * ((kbps + U - 1) / U + 6);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_s = s;
@@ -666,8 +791,9 @@ size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M) {
 
 size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) {
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
-  const int64_t mtiles = (ml + p.m_tile - 1) / p.m_tile;
-  return (size_t)mtiles * (size_t)W->KB * 192u * (size_t)p.m_tile;
+  const int64_t mtr = p.m_tile / 3;
+  const int64_t mtiles = (ml + mtr - 1) / mtr;
+  return (size_t)mtiles * (size_t)W->KB * 64u * (size_t)p.m_tile;
 }
 
 int tc_launch_count(const TcPlan&, int64_t M) {
@@ -678,12 +804,9 @@ int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx
               const TcPlan& plan, const Workspace& ws, cudaStream_t s) {
   for (int64_t mb = 0; mb < M; mb += TC_M_LAUNCH) {
     const int64_t ml = (M - mb) < TC_M_LAUNCH ? (M - mb) : TC_M_LAUNCH;
-    int st;
-    switch (plan.m_tile) {
-      case 16: st = launch_mt<16>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      case 32: st = launch_mt<32>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      default: st = launch_mt<64>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-    }
+    const int st = plan.m_tile == 16
+                       ? launch_nb<16>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s)
+                       : launch_nb<32>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s);
     if (st) return st;
   }
   return Q4_OK;

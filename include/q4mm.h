@@ -68,7 +68,7 @@ extern "C" {
 /* ---- status codes ---- */
 #define Q4_OK 0
 #define Q4_ERR_INVALID_ARG 1  /* null pointer, negative size, wrong device, bad flag */
-#define Q4_ERR_SHAPE 2        /* K not a positive multiple of 32 or above 32*65535, N < 1, M above Q4MM_M_MAX */
+#define Q4_ERR_SHAPE 2        /* K not a multiple of 32 in [32, 32*65535], N not in [1, 128*65535], M above Q4MM_M_MAX */
 #define Q4_ERR_ALIGN 3        /* a device pointer not 16-byte aligned */
 #define Q4_ERR_NONFINITE 4    /* a weight is NaN or infinite (quantize), or a stored scale is */
 #define Q4_ERR_RANGE 5        /* a block scale does not fit binary16 (|d| >= 65520) */
