@@ -430,7 +430,7 @@ def run_path_sweep(args):
     stack = build_stack(q4, torch, dev, layers)
     stream = torch.cuda.Stream(dev)
     sweep = (1, 2, 3, 4, 5, 6, 8, 16, 32, 64, 128, 256)
-    paths = {"simt": q4.Q4MM_FORCE_SIMT, "tc": q4.Q4MM_FORCE_TC}
+    paths = {"simt": q4.Q4MM_FORCE_SIMT, "mma": q4.Q4MM_FORCE_MMA, "tc": q4.Q4MM_FORCE_TC}
     out = {}
     for M in sweep:
         xs = {K: torch.from_numpy(synthetic.normal(synthetic.act_seed(5, M) + K, (M, K))).to(dev)
@@ -462,11 +462,12 @@ def run_path_sweep(args):
                 out.setdefault(name, {}).setdefault(str(M), {})[pname] = {
                     "us": us, "weight_gbs": wb / us / 1e3, "rows_per_s": M / us * 1e6}
                 del g
-    # threshold: smallest M from which the tensor-core path is at least as fast
-    # on the large shapes (gate, down) for every larger M of the sweep
+    # threshold: smallest M from which the tcgen05 path is at least as fast as
+    # the streaming mma.sync path on the large shapes (gate, down) for every
+    # larger M of the sweep
     thr = None
     for i, M in enumerate(sweep):
-        if all(out[n][str(m)]["tc"]["us"] <= out[n][str(m)]["simt"]["us"]
+        if all(out[n][str(m)]["tc"]["us"] <= out[n][str(m)]["mma"]["us"]
                for n in ("gate_proj", "down_proj") for m in sweep[i:]):
             thr = M
             break

@@ -30,10 +30,12 @@ Q4MM_BATCH_INVARIANT = 0x1
 Q4MM_FORCE_SIMT = 0x2
 Q4MM_FORCE_TC = 0x4
 Q4MM_ROW_BY_ROW = 0x8
+Q4MM_FORCE_MMA = 0x10
 Q4MM_M_MAX = 4096
 Q4MM_PATH_SIMT = 1
 Q4MM_PATH_TC = 2
 Q4MM_PATH_ROW_BY_ROW = 3
+Q4MM_PATH_MMA = 4
 
 BLOCK = 32
 BLOCK_BYTES = 18

@@ -36,9 +36,9 @@ struct DeviceScratch {
 };
 DeviceScratch g_dev[MAX_DEVICES];
 
-// Measured on GB300: below this M the CUDA-core streaming kernel is used,
-// at or above it the tensor-core kernel.
-constexpr int64_t DEFAULT_M_THRESHOLD = 2;
+// Measured on GB300: below this M the streaming mma.sync kernel is used, at
+// or above it the tcgen05 kernel.
+constexpr int64_t DEFAULT_M_THRESHOLD = 17;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -79,10 +79,11 @@ int alloc_weight(int64_t N, int64_t K, int dev, Weight* W) {
   W->K = K;
   W->N_pad = pad_n(N);
   W->KB = K / BLOCK_K;
+  W->KBP = (W->KB + 1) / 2;
   W->tiles = W->N_pad / TILE_N;
   W->device = dev;
-  const size_t nib_bytes = (size_t)W->tiles * W->KB * TILE_N * 16;
-  const size_t d_bytes = (size_t)W->tiles * W->KB * TILE_N * 2;
+  const size_t nib_bytes = (size_t)W->tiles * W->KBP * PAIR_NIB_BYTES;
+  const size_t d_bytes = (size_t)W->tiles * W->KBP * PAIR_SCL_BYTES;
   const size_t off = (nib_bytes + 255) / 256 * 256;
   W->alloc_bytes = off + d_bytes;
   if (cudaMalloc(&W->alloc, W->alloc_bytes) != cudaSuccess) {
@@ -102,24 +103,27 @@ int check_shape(int64_t N, int64_t K) {
 }
 
 // Path choice.  Deterministic in (flags, M, device); in batch-invariant mode
-// it ignores M entirely.
+// it ignores M entirely (always the streaming MMA kernel with one token row
+// per column group).
 int choose_path(const DeviceScratch& ds, int64_t M, uint32_t flags) {
   const bool tc = tc_supported(ds);
   if (flags & Q4MM_ROW_BY_ROW) return Q4MM_PATH_ROW_BY_ROW;
   if (flags & Q4MM_FORCE_SIMT) return Q4MM_PATH_SIMT;
+  if (flags & Q4MM_FORCE_MMA) return Q4MM_PATH_MMA;
   if (flags & Q4MM_FORCE_TC) return tc ? Q4MM_PATH_TC : -Q4_ERR_UNSUPPORTED;
-  if (flags & Q4MM_BATCH_INVARIANT) return tc ? Q4MM_PATH_TC : Q4MM_PATH_SIMT;
-  return (tc && M >= g_m_threshold.load()) ? Q4MM_PATH_TC : Q4MM_PATH_SIMT;
+  if (flags & Q4MM_BATCH_INVARIANT) return Q4MM_PATH_MMA;
+  return (tc && M >= g_m_threshold.load()) ? Q4MM_PATH_TC : Q4MM_PATH_MMA;
 }
 
-constexpr uint32_t KNOWN_FLAGS =
-    Q4MM_BATCH_INVARIANT | Q4MM_FORCE_SIMT | Q4MM_FORCE_TC | Q4MM_ROW_BY_ROW;
+constexpr uint32_t KNOWN_FLAGS = Q4MM_BATCH_INVARIANT | Q4MM_FORCE_SIMT | Q4MM_FORCE_TC |
+                                 Q4MM_ROW_BY_ROW | Q4MM_FORCE_MMA;
 
 int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxval, int64_t M,
         uint32_t flags, cudaStream_t s) {
   if (!Wh || !x || (!y && !idx)) return Q4_ERR_INVALID_ARG;
   if (flags & ~KNOWN_FLAGS) return Q4_ERR_INVALID_ARG;
-  const int forced = !!(flags & Q4MM_FORCE_SIMT) + !!(flags & Q4MM_FORCE_TC) + !!(flags & Q4MM_ROW_BY_ROW);
+  const int forced = !!(flags & Q4MM_FORCE_SIMT) + !!(flags & Q4MM_FORCE_TC) +
+                     !!(flags & Q4MM_ROW_BY_ROW) + !!(flags & Q4MM_FORCE_MMA);
   if (forced > 1) return Q4_ERR_INVALID_ARG;
   if (M < 0) return Q4_ERR_INVALID_ARG;
   if (M > Q4MM_M_MAX) return Q4_ERR_SHAPE;
@@ -138,14 +142,22 @@ int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxv
   if (st) return st;
   const int path = choose_path(ds, M, flags);
   if (path < 0) return -path;
+  const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
   if (path == Q4MM_PATH_TC) {
-    const TcPlan plan = tc_plan(W, M, ds.num_sms, (flags & Q4MM_BATCH_INVARIANT) != 0);
+    const TcPlan plan = tc_plan(W, M, ds.num_sms, inv);
     Workspace ws;
     st = workspace_get(dev, tc_partial_bytes(W, plan, M), tc_xop_bytes(W, plan, M), &ws);
     if (st) return st;
     return launch_tc(W, x, M, y, idx, maxval, plan, ws, s);
   }
-  const SimtPlan plan = simt_plan(W, ds.num_sms);
+  if (path == Q4MM_PATH_MMA) {
+    const MmaPlan plan = mma_plan(W, ds.num_sms);
+    Workspace ws;
+    st = workspace_get(dev, mma_partial_bytes(W, plan, M, inv), 0, &ws);
+    if (st) return st;
+    return launch_mma(W, x, M, y, idx, maxval, plan, inv, ws, s);
+  }
+  const MmaPlan plan = simt_plan(W, ds.num_sms);
   Workspace ws;
   if (path == Q4MM_PATH_ROW_BY_ROW) {
     st = workspace_get(dev, simt_partial_bytes(W, plan, 1), 0, &ws);
@@ -220,14 +232,22 @@ int q4_quantize(const float* w, int64_t N, int64_t K, q4_weight** out, cudaStrea
     delete h;
     return st;
   }
+  uint8_t* canon = nullptr;  // canonical blocks, repacked into the device layout
+  if (cudaMalloc(&canon, (size_t)N * (size_t)(K / BLOCK_K) * CANON_BLOCK_BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->w.alloc);
+    delete h;
+    return Q4_ERR_NOMEM;
+  }
   unsigned flag = 0;
   st = Q4_OK;
   if (cudaMemsetAsync(ds.format_flag, 0, sizeof(unsigned), stream) != cudaSuccess) st = Q4_ERR_CUDA;
-  if (!st) st = launch_quantize(w, N, K, &h->w, ds.format_flag, stream);
+  if (!st) st = launch_quantize(w, N, K, canon, &h->w, ds.format_flag, stream);
   if (!st && cudaMemcpyAsync(&flag, ds.format_flag, sizeof(unsigned), cudaMemcpyDeviceToHost,
                              stream) != cudaSuccess)
     st = Q4_ERR_CUDA;
   if (!st && cudaStreamSynchronize(stream) != cudaSuccess) st = Q4_ERR_CUDA;
+  cudaFree(canon);
   if (!st) st = quantize_flag_status(flag);
   if (st) {
     cudaFree(h->w.alloc);
@@ -377,8 +397,12 @@ int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int
     const TcPlan plan = tc_plan(&W->w, M, ds.num_sms, (flags & Q4MM_BATCH_INVARIANT) != 0);
     l = tc_launch_count(plan, M);
     sp = plan.splits;
+  } else if (p == Q4MM_PATH_MMA) {
+    const MmaPlan plan = mma_plan(&W->w, ds.num_sms);
+    l = mma_launch_count(M, (flags & Q4MM_BATCH_INVARIANT) != 0);
+    sp = plan.splits;
   } else {
-    const SimtPlan plan = simt_plan(&W->w, ds.num_sms);
+    const MmaPlan plan = simt_plan(&W->w, ds.num_sms);
     l = p == Q4MM_PATH_ROW_BY_ROW ? (int)M : simt_launch_count(M);
     sp = plan.splits;
   }

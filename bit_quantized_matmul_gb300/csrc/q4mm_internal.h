@@ -11,34 +11,52 @@
 namespace q4 {
 
 // ---------------------------------------------------------------------------
-// Device weight layout ("tiled Q4").
+// Device weight layout ("fragment layout").
 //
-// Rows are grouped in tiles of TILE_N = 128 (one row per TMEM lane / thread);
-// N is padded to a multiple of 128 with zero-scale rows.  For tile t, block b
-// (32 weights along K) and row r of the tile:
-//   nibbles: 16 bytes at  ((t * KB + b) * 128 + r) * 16
-//   scale:   binary16 at   (t * KB + b) * 128 + r
-// so one block column of a tile is 2 KB of nibbles plus 256 B of scales, both
-// contiguous: a warp's 32 rows read 512 consecutive bytes, and a bulk copy of
-// B consecutive blocks of one tile is one contiguous range.
+// Rows are grouped in tiles of TILE_N = 128 (N is padded to a multiple of 128
+// with zero-scale rows); blocks of 32 weights along K are grouped in pairs
+// (KB is padded to an even count with zero blocks).  A tile is 8 row groups
+// of 16 rows.  For tile t, block pair bp, row group rg and lane L = 4g + tq
+// (g = 0..7, tq = 0..3) there are 16 bytes: four 32-bit words, word 2h + s for
+// block b = 2bp + h and k-step s (16 weights of the block).  Lane L holds the
+// weights of rows R0 = 16rg + g and R1 = R0 + 8 at k0 = 16s + 2tq, k0 + 1,
+// k0 + 8, k0 + 9 of the block.  In each word, nibble pair p (bits 4p..4p+3 and
+// 16+4p..19+4p) holds row (p & 1 ? R1 : R0) at k = k0 + 8(p >> 1) and k + 1.
+// So (w >> 4p) & 0x000F000F is pair p, and pairs 0..3 are exactly the A
+// fragment registers a0..a3 of an m16n8k16 MMA over that k-step.  The 16-byte
+// groups of a (tile, block pair) are contiguous (4 KB), so a warp's 32 lanes
+// read 512 consecutive bytes and consecutive block pairs of a tile are one
+// contiguous range.
 //
-// Nibble order inside the 16 bytes (four little-endian 32-bit words w_i, word
-// i covering k = 8i .. 8i+7): the nibble at bit 4p (p = 0..3) holds
-// k = 8i + 2p and the nibble at bit 16 + 4p holds k = 8i + 2p + 1.  Then
-// (w_i >> 4p) & 0x000F000F puts the pair (k = 8i+2p, 8i+2p+1) in the low and
-// high 16-bit halves, which is what both kernels unpack.
+// Scales: for tile t, block pair bp, row group rg and g, four binary16 values
+// (8 bytes): d(R0, 2bp), d(R0, 2bp+1), d(R1, 2bp), d(R1, 2bp+1); 512 bytes per
+// (tile, block pair).
 // ---------------------------------------------------------------------------
 constexpr int TILE_N = 128;
 constexpr int BLOCK_K = 32;
 constexpr int CANON_BLOCK_BYTES = 18;
+constexpr int PAIR_NIB_BYTES = 4096;   // nibbles of one (tile, block pair)
+constexpr int PAIR_SCL_BYTES = 512;    // scales of one (tile, block pair)
 
 inline int64_t pad_n(int64_t N) { return (N + TILE_N - 1) / TILE_N * TILE_N; }
 
+// 32-bit word index of (tile t, block pair bp, row group rg, lane, half h, k-step s).
+__host__ __device__ inline int64_t nib_word_index(int64_t KBP, int64_t t, int64_t bp, int rg, int lane,
+                                                  int h, int s) {
+  return ((((t * KBP + bp) * 8 + rg) * 32 + lane) * 4) + h * 2 + s;
+}
+
+// binary16 index of the scale of (tile t, block pair bp, row group rg, g, upper, h).
+__host__ __device__ inline int64_t scale_index(int64_t KBP, int64_t t, int64_t bp, int rg, int g,
+                                               int upper, int h) {
+  return ((((t * KBP + bp) * 8 + rg) * 8 + g) * 4) + upper * 2 + h;
+}
+
 struct Weight {
-  int64_t N = 0, K = 0, N_pad = 0, KB = 0, tiles = 0;
+  int64_t N = 0, K = 0, N_pad = 0, KB = 0, KBP = 0, tiles = 0;
   int device = 0;
-  uint8_t* nib = nullptr;   // [tiles][KB][128][16]
-  uint16_t* d = nullptr;    // [tiles][KB][128] binary16 bits
+  uint8_t* nib = nullptr;   // tiles * KBP * 4096 bytes (fragment layout)
+  uint16_t* d = nullptr;    // tiles * KBP * 256 binary16 scales
   void* alloc = nullptr;    // single allocation backing nib and d
   size_t alloc_bytes = 0;
 };
@@ -60,28 +78,38 @@ constexpr int MAX_COUNTERS = 1 << 16;
 int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws);
 
 // ---- launchers (return a Q4 status; launch errors map to Q4_ERR_CUDA) ----
-int launch_quantize(const float* w, int64_t N, int64_t K, Weight* W, unsigned int* flag,
-                    cudaStream_t s);
+// Quantize fp32 W (device) into canonical blocks in canon_dev, then repack.
+int launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* canon_dev, Weight* W,
+                    unsigned int* flag, cudaStream_t s);
 int launch_import(const uint8_t* canon_dev, Weight* W, unsigned int* flag, cudaStream_t s);
 int launch_export(const Weight* W, uint8_t* canon_dev, cudaStream_t s);
 int quantize_flag_status(unsigned flag);
 
-struct SimtPlan {
-  int splits;          // K partition count (depends on N and K only)
-  int64_t kb_per_split;
+// K partition of the streaming kernels (from N and K only, never from M).
+struct MmaPlan {
+  int splits;
+  int64_t kbp_per_split;  // block pairs per split
 };
-SimtPlan simt_plan(const Weight* W, int num_sms);
-size_t simt_partial_bytes(const Weight* W, const SimtPlan& p, int64_t M);
+
+// mma.sync streaming kernel (small and medium M).
+MmaPlan mma_plan(const Weight* W, int num_sms);
+size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant);
+int mma_launch_count(int64_t M, bool batch_invariant);
+int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
+               const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
+
+// CUDA-core streaming kernel.
+MmaPlan simt_plan(const Weight* W, int num_sms);
+size_t simt_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M);
 int simt_launch_count(int64_t M);
-
-// Mode: y output, or argmax (idx/maxval).
 int launch_simt(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx,
-                float* maxval, const SimtPlan& plan, const Workspace& ws, cudaStream_t s);
+                float* maxval, const MmaPlan& plan, const Workspace& ws, cudaStream_t s);
 
+// tcgen05 kernel (large M).
 struct TcPlan {
   int splits;
-  int64_t kb_per_split;
-  int m_tile;          // token rows per CTA pass (MMA N), multiple of 16
+  int64_t kbp_per_split;  // block pairs per split
+  int m_tile;             // MMA N (16 or 32)
 };
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant);
 size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M);

@@ -41,12 +41,13 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "q4mm_epilogue.cuh"
 #include "q4mm_internal.h"
 
 namespace q4 {
 namespace {
 
-constexpr int U = 4;                    // blocks per unit
+constexpr int U = 4;                    // blocks per unit (two block pairs)
 constexpr int CONV_WARP0 = 0;           // 8 warps
 constexpr int EPI_WARP0 = 8;            // 8 warps
 constexpr int PROD_WARP0 = 16;          // 2 warps
@@ -93,23 +94,14 @@ struct Cfg {
 };
 
 struct TcArgs {
-  const uint8_t* nib;
-  const uint16_t* d;
-  const uint8_t* xop;  // activation operand, [mtiles][KB][64*NB] bytes
-  int64_t KB, K, N, N_pad;
-  int64_t M;           // rows in this launch
-  float* y;
-  int32_t* idx;
-  float* maxval;
-  int splits;
-  int64_t kb_per_split;
+  const uint8_t* nib;  // fragment layout
+  const uint8_t* scl;
+  const uint8_t* xop;  // activation operand, [mtiles][KB2][64*NB] bytes
+  int64_t KBP, KB2;    // block pairs, padded blocks (2 * KBP)
+  int64_t kbp_per_split;
   int mtiles;
-  int tiles;
-  float* partial;
-  unsigned int* counters;
-  unsigned long long* keys;
-  unsigned int* argmax_done;
   unsigned int* status;
+  EpiArgs e;
 };
 
 // ----------------------------------------------------------------------------
@@ -311,20 +303,6 @@ __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
   return r;
 }
 
-__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t n) {
-  if (v != v) return 0ull;
-  if (v == 0.0f) v = 0.0f;
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - n);
-}
-
-__device__ __forceinline__ float key_value(unsigned long long k) {
-  const uint32_t u = (uint32_t)(k >> 32);
-  if (u == 0u) return __uint_as_float(0x7FC00000u);
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-}
-
 // ----------------------------------------------------------------------------
 // Pre-pass: x[M, K] fp32 -> activation operand: three exact bf16 terms per
 // value, laid out per (m tile, block) exactly as the MMA reads it from smem,
@@ -335,6 +313,7 @@ __device__ __forceinline__ float key_value(unsigned long long k) {
 template <int NB>
 __global__ void __launch_bounds__(256) xop_kernel(const float* __restrict__ x, int64_t M, int64_t K,
                                                   int64_t KB, int mtiles, uint8_t* __restrict__ xop) {
+  // KB here is the padded block count; blocks past the real K read as zero
   constexpr int MTR = NB / 3;
   asm volatile("griddepcontrol.launch_dependents;");
   const int64_t total = (int64_t)mtiles * KB * 4 * MTR;
@@ -347,7 +326,7 @@ __global__ void __launch_bounds__(256) xop_kernel(const float* __restrict__ x, i
     const int s = sg >> 1, g = sg & 1;
     const int64_t m = mt * MTR + mm;
     float v[8];
-    if (m < M) {
+    if (m < M && b * BLOCK_K < K) {
       const float4* src = reinterpret_cast<const float4*>(x + m * K + b * BLOCK_K + s * 16 + g * 8);
       const float4 a = src[0], c = src[1];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -403,17 +382,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfree + NBR);
   volatile int* err = reinterpret_cast<volatile int*>(tmem_slot + 2);
   __shared__ int s_last;
-  __shared__ unsigned long long red[4][MTR];
+  __shared__ unsigned long long red[4][MTR];  // greedy-pick scratch of the epilogue
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
-  const int64_t kb0 = (int64_t)split * a.kb_per_split;
-  const int64_t kb1 = min(a.KB, kb0 + a.kb_per_split);
-  const int nblk = (int)(kb1 - kb0);
+  const int64_t bp0 = (int64_t)split * a.kbp_per_split;
+  const int64_t bp1 = min(a.KBP, bp0 + a.kbp_per_split);
+  const int nblk = (int)(2 * (bp1 - bp0));  // includes the zero pad block of an odd count
   const int nunits = (nblk + U - 1) / U;
   const int64_t m0 = (int64_t)mt * MTR;
-  const int mcount = (int)min((int64_t)MTR, a.M - m0);
+  const int mcount = (int)min((int64_t)MTR, a.e.M - m0);
 
   if (tid == 0) {
     for (int i = 0; i < NBR; ++i) {
@@ -444,10 +423,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     if (lane == 0) {
       const int p = warp - PROD_WARP0;
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      const uint8_t* nib_base = a.nib + ((int64_t)tile * a.KB + kb0) * TILE_N * 16;
-      const uint8_t* scl_base =
-          reinterpret_cast<const uint8_t*>(a.d + ((int64_t)tile * a.KB + kb0) * TILE_N);
-      const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB + kb0) * (int64_t)C::BOP_BLOCK;
+      const uint8_t* nib_base = a.nib + ((int64_t)tile * a.KBP + bp0) * PAIR_NIB_BYTES;
+      const uint8_t* scl_base = a.scl + ((int64_t)tile * a.KBP + bp0) * PAIR_SCL_BYTES;
+      const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB2 + 2 * bp0) * (int64_t)C::BOP_BLOCK;
       int last = -1;
       for (int u = p; u < nunits; u += NPROD) {
         const int st = u % C::NST;
@@ -510,22 +488,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     const int q = warp & 3, g = (warp - CONV_WARP0) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    // this row's place in the fragment layout
+    const int frg = row >> 4, fup = (row >> 3) & 1, fg = row & 7;
     for (int u = g; u < nunits; u += 2) {
       const int st = u % C::NST, sa = u % C::NA;
       const int ub = min(U, nblk - u * U);
       const int bi = u % NBR;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[bi]), (u / NBR) & 1, err))) break;
       const uint8_t* sp = stages + st * C::STAGE_BYTES;
-      uint4 v[U];
+      // Block b of the unit (pair b / 2, half b % 2): the row's 32 weights sit
+      // in the words of lanes 4fg + tq (tq = 0..3), two k-steps each.
+      uint2 v[U][4];
       float dsc[U];
 #pragma unroll
       for (int b = 0; b < U; ++b) {
+        const int bpl = b >> 1, h = b & 1;
         if (b < ub) {
-          v[b] = *reinterpret_cast<const uint4*>(sp + b * TILE_N * 16 + row * 16);
-          const uint16_t dh = *reinterpret_cast<const uint16_t*>(sp + C::SCL_OFF + b * TILE_N * 2 + row * 2);
+#pragma unroll
+          for (int tq = 0; tq < 4; ++tq)
+            v[b][tq] = *reinterpret_cast<const uint2*>(
+                sp + (((bpl * 8 + frg) * 32 + 4 * fg + tq) * 16) + h * 8);
+          const uint16_t dh = *reinterpret_cast<const uint16_t*>(
+              sp + C::SCL_OFF + ((bpl * 8 + frg) * 8 + fg) * 8 + (fup * 2 + h) * 2);
           dsc[b] = __half2float(__ushort_as_half(dh));
         } else {
-          v[b] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+#pragma unroll
+          for (int tq = 0; tq < 4; ++tq) v[b][tq] = make_uint2(0x88888888u, 0x88888888u);
           dsc[b] = 0.0f;
         }
       }
@@ -544,15 +532,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
       const uint32_t acol = a_base + lane_off + (uint32_t)(sa * C::A_UNIT_COLS);
 #pragma unroll
       for (int h = 0; h < U / 2; ++h) {
+        // TMEM column c of a block holds k = 2c, 2c + 1: the pair at
+        // k0 = 16s + 2tq is column 8s + tq, the pair at k0 + 8 is 8s + 4 + tq
         uint32_t av[32];
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const uint32_t wv[4] = {v[2 * h + bb].x, v[2 * h + bb].y, v[2 * h + bb].z, v[2 * h + bb].w};
+        for (int bb = 0; bb < 2; ++bb)
 #pragma unroll
-          for (int w = 0; w < 4; ++w)
+          for (int tq = 0; tq < 4; ++tq) {
+            const uint32_t ws[2] = {v[2 * h + bb][tq].x, v[2 * h + bb][tq].y};
 #pragma unroll
-            for (int pp = 0; pp < 4; ++pp) av[16 * bb + 4 * w + pp] = nib_pair_bf16(wv[w], pp);
-        }
+            for (int st2 = 0; st2 < 2; ++st2) {
+              av[16 * bb + 8 * st2 + tq] = nib_pair_bf16(ws[st2], fup);
+              av[16 * bb + 8 * st2 + 4 + tq] = nib_pair_bf16(ws[st2], fup + 2);
+            }
+          }
         tmem_st32(acol + (uint32_t)(32 * h), av);
       }
       tmem_wait_st();
@@ -615,81 +608,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   if (warp < EPI_WARP0 || warp >= EPI_WARP0 + 4) return;  // warps 8-11 own the rows now
 
   const int row = (warp & 3) * 32 + lane;
-  const int64_t n = (int64_t)tile * TILE_N + row;
 #pragma unroll
   for (int m = 0; m < MTR; ++m) acc[m] += comb[m * TILE_N + row];
-
   // named barrier over the 128 threads of warps 8-11
-  auto sync128 = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-
-  if (a.splits > 1) {
-#pragma unroll
-    for (int m = 0; m < MTR; ++m)
-      if (m < mcount) a.partial[((int64_t)split * a.M + m0 + m) * a.N_pad + n] = acc[m];
-    __threadfence();
-    sync128();
-    if (row == 0) {
-      const unsigned prev = atomicAdd(&a.counters[tile * a.mtiles + mt], 1u);
-      s_last = (prev == (unsigned)(a.splits - 1));
-    }
-    sync128();
-    if (!s_last) return;
-    __threadfence();
-#pragma unroll
-    for (int m = 0; m < MTR; ++m) {
-      if (m < mcount) {
-        float v = 0.0f;
-        for (int s = 0; s < a.splits; ++s)
-          v += __ldcg(&a.partial[((int64_t)s * a.M + m0 + m) * a.N_pad + n]);
-        acc[m] = v;
-      }
-    }
-    if (row == 0) a.counters[tile * a.mtiles + mt] = 0u;
-  }
-
-  if (a.idx == nullptr) {
-    if (n < a.N) {
-#pragma unroll
-      for (int m = 0; m < MTR; ++m)
-        if (m < mcount) a.y[(m0 + m) * a.N + n] = acc[m];
-    }
-    return;
-  }
-
-  // ---- fused greedy pick ----
-  const int w4 = warp & 3;
-#pragma unroll
-  for (int m = 0; m < MTR; ++m) {
-    unsigned long long k = (m < mcount && n < a.N) ? argmax_key(acc[m], (uint32_t)n) : 0ull;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, k, off);
-      k = o > k ? o : k;
-    }
-    if (lane == 0) red[w4][m] = k;
-  }
-  sync128();
-  if (row < mcount) {
-    unsigned long long k = red[0][row];
-#pragma unroll
-    for (int w = 1; w < 4; ++w) k = red[w][row] > k ? red[w][row] : k;
-    atomicMax(&a.keys[m0 + row], k);
-  }
-  __threadfence();
-  sync128();
-  if (row == 0) {
-    const unsigned prev = atomicAdd(a.argmax_done, 1u);
-    s_last = (prev == (unsigned)(a.tiles * a.mtiles - 1));
-  }
-  sync128();
-  if (!s_last) return;
-  __threadfence();
-  for (int64_t m = row; m < a.M; m += TILE_N) {
-    const unsigned long long k = atomicExch(&a.keys[m], 0ull);
-    a.idx[m] = k == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
-    if (a.maxval) a.maxval[m] = key_value(k);
-  }
-  if (row == 0) *a.argmax_done = 0u;
+  finish_tile<MTR>(a.e, acc, row, tile, m0, mcount, split, tile * a.mtiles + mt, &s_last, red,
+                   []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
 }
 
 constexpr int64_t TC_M_LAUNCH = 256;  // rows per launch pair (pre-pass + main)
@@ -706,12 +629,13 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
               const TcPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
   using C = Cfg<NB>;
   const int mtiles = (int)((ml + C::MTR - 1) / C::MTR);
+  const int64_t KB2 = 2 * W->KBP;
   if (plan.splits > 1 && W->tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   {
-    const int64_t total = (int64_t)mtiles * W->KB * 4 * C::MTR;
+    const int64_t total = (int64_t)mtiles * KB2 * 4 * C::MTR;
     const int64_t want = (total + 255) / 256;
     const int blocks = (int)(want < 4096 ? want : 4096);
-    xop_kernel<NB><<<blocks, 256, 0, s>>>(x, ml, W->K, W->KB, mtiles, static_cast<uint8_t*>(ws.xop));
+    xop_kernel<NB><<<blocks, 256, 0, s>>>(x, ml, W->K, KB2, mtiles, static_cast<uint8_t*>(ws.xop));
     if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
   }
   static bool attr_set[64] = {};
@@ -723,25 +647,25 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   }
   TcArgs a;
   a.nib = W->nib;
-  a.d = W->d;
+  a.scl = reinterpret_cast<const uint8_t*>(W->d);
   a.xop = static_cast<const uint8_t*>(ws.xop);
-  a.KB = W->KB;
-  a.K = W->K;
-  a.N = W->N;
-  a.N_pad = W->N_pad;
-  a.M = ml;
-  a.y = y ? y + mb * W->N : nullptr;
-  a.idx = idx ? idx + mb : nullptr;
-  a.maxval = (idx && maxval) ? maxval + mb : nullptr;
-  a.splits = plan.splits;
-  a.kb_per_split = plan.kb_per_split;
+  a.KBP = W->KBP;
+  a.KB2 = KB2;
+  a.kbp_per_split = plan.kbp_per_split;
   a.mtiles = mtiles;
-  a.tiles = (int)W->tiles;
-  a.partial = ws.partial;
-  a.counters = ws.counters;
-  a.keys = ws.keys + mb;
-  a.argmax_done = ws.argmax_done;
   a.status = ws.status;
+  a.e.N = W->N;
+  a.e.N_pad = W->N_pad;
+  a.e.M = ml;
+  a.e.y = y ? y + mb * W->N : nullptr;
+  a.e.idx = idx ? idx + mb : nullptr;
+  a.e.maxval = (idx && maxval) ? maxval + mb : nullptr;
+  a.e.splits = plan.splits;
+  a.e.partial = ws.partial;
+  a.e.counters = ws.counters;
+  a.e.keys = ws.keys + mb;
+  a.e.argmax_done = ws.argmax_done;
+  a.e.tiles = (int)(W->tiles * mtiles);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)mtiles, (unsigned)W->tiles, (unsigned)plan.splits);
@@ -768,18 +692,18 @@ TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   // waves against units per CTA (+ a fixed per-CTA cost in unit terms).
   const int64_t tiles = W->tiles;
   int64_t best_s = 1, best_cost = -1;
-  const int64_t smax = W->KB < 64 ? W->KB : 64;
+  const int64_t smax = W->KBP < 64 ? W->KBP : 64;
   for (int64_t s = 1; s <= smax; ++s) {
-    const int64_t kbps = (W->KB + s - 1) / s;
+    const int64_t kbps = (W->KBP + s - 1) / s;  // block pairs per split
     const int64_t waves = (tiles * s + num_sms - 1) / num_sms;
-    const int64_t cost = waves * ((kbps + U - 1) / U + 6);
+    const int64_t cost = waves * ((2 * kbps + U - 1) / U + 6);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_s = s;
     }
   }
-  p.kb_per_split = (W->KB + best_s - 1) / best_s;
-  p.splits = (int)((W->KB + p.kb_per_split - 1) / p.kb_per_split);
+  p.kbp_per_split = (W->KBP + best_s - 1) / best_s;
+  p.splits = (int)((W->KBP + p.kbp_per_split - 1) / p.kbp_per_split);
   return p;
 }
 
@@ -793,7 +717,7 @@ size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) {
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
   const int64_t mtr = p.m_tile / 3;
   const int64_t mtiles = (ml + mtr - 1) / mtr;
-  return (size_t)mtiles * (size_t)W->KB * 64u * (size_t)p.m_tile;
+  return (size_t)mtiles * (size_t)(2 * W->KBP) * 64u * (size_t)p.m_tile;
 }
 
 int tc_launch_count(const TcPlan&, int64_t M) {

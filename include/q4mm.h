@@ -80,17 +80,20 @@ extern "C" {
 /* ---- flags for the _ex entry points ---- */
 /* Bit-identical output rows: row r of y depends only on x[r,:] and W, never on
  * M, on r's position in the batch or on the other rows' values.  The kernel
- * family and the K partition are then fixed per weight shape, independent of M
- * (§"The Other Request Already Finished": a 120-prefill + 4-verify batch
- * crossed the kernel-switch threshold and changed the cached numbers). */
+ * family, the K partition and each row's MMA column positions are then fixed
+ * per weight shape, independent of M (§"The Other Request Already Finished":
+ * a 120-prefill + 4-verify batch crossed the kernel-switch threshold and
+ * changed the cached numbers). */
 #define Q4MM_BATCH_INVARIANT 0x1u
-/* Force the CUDA-core streaming kernel (the measured small-M path). */
+/* Force the CUDA-core streaming kernel (no tensor cores). */
 #define Q4MM_FORCE_SIMT 0x2u
-/* Force the tensor-core (tcgen05/TMEM) kernel. */
+/* Force the tcgen05/TMEM tensor-core kernel (the large-M path). */
 #define Q4MM_FORCE_TC 0x4u
-/* Ablation: one launch per activation row with the small-M kernel, the
+/* Ablation: one launch per activation row with the CUDA-core kernel, the
  * row-by-row fallback of §"Row-by-Row GEMV to the Rescue". */
 #define Q4MM_ROW_BY_ROW 0x8u
+/* Force the streaming mma.sync kernel (the measured small/medium-M path). */
+#define Q4MM_FORCE_MMA 0x10u
 
 /* Largest M accepted by one call. */
 #define Q4MM_M_MAX 4096
@@ -99,6 +102,7 @@ extern "C" {
 #define Q4MM_PATH_SIMT 1
 #define Q4MM_PATH_TC 2
 #define Q4MM_PATH_ROW_BY_ROW 3
+#define Q4MM_PATH_MMA 4
 
 typedef struct q4_weight q4_weight;
 
@@ -159,8 +163,8 @@ Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
 Q4_API int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int* launches,
                           int* splits);
 
-/* The M threshold: calls with M >= threshold take the tensor-core path, smaller
- * M the CUDA-core streaming path (the kernel-switch threshold that
+/* The M threshold: calls with M >= threshold take the tcgen05 path, smaller M
+ * the streaming mma.sync path (the kernel-switch threshold that
  * §"Row-by-Row GEMV to the Rescue" says must be measured, not assumed).
  * The default is the value measured on GB300; set_m_threshold overrides it for
  * the process (1 = always tensor cores; Q4MM_M_MAX + 1 = never). */

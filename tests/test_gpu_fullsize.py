@@ -63,7 +63,7 @@ def test_qwen7b_linear_decode_parity(q4, name):
         x = acts(2, M, W.K)
         _sampled_check(q4, W, blocks, x, 0, rng, what="%s M=%d" % (name, M))
     x = acts(2, 8, W.K, salt=1)
-    for flags in (q4.Q4MM_FORCE_SIMT, q4.Q4MM_BATCH_INVARIANT):
+    for flags in (q4.Q4MM_FORCE_SIMT, q4.Q4MM_FORCE_TC, q4.Q4MM_BATCH_INVARIANT):
         _sampled_check(q4, W, blocks, x, flags, rng, n_per_row=512, what="%s flags=%d" % (name, flags))
     assert q4.q4_device_status() == q4.Q4_OK
 
@@ -118,9 +118,10 @@ def test_mixed_step_m124_parity_and_invariance(q4, name):
 def test_gate_m_sweep_parity(q4):
     W, blocks = _weight(q4, 4, "gate_proj")
     rng = np.random.default_rng(77)
-    for M in (6, 16, 32, 64, 128, 256):
+    for M in (6, 16, 17, 32, 64, 128, 256):
         x = acts(4, M, W.K)
         _sampled_check(q4, W, blocks, x, 0, rng, n_per_row=64, what="gate M=%d" % M)
+        _sampled_check(q4, W, blocks, x, q4.Q4MM_FORCE_MMA, rng, n_per_row=32, what="gate mma M=%d" % M)
 
 
 def test_lm_head_argmax_planted_near_ties(q4):

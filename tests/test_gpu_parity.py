@@ -25,7 +25,8 @@ def q4():
 
 
 def _flags(q4):
-    return {"auto": 0, "simt": q4.Q4MM_FORCE_SIMT, "invariant": q4.Q4MM_BATCH_INVARIANT,
+    return {"auto": 0, "simt": q4.Q4MM_FORCE_SIMT, "mma": q4.Q4MM_FORCE_MMA,
+            "tc": q4.Q4MM_FORCE_TC, "invariant": q4.Q4MM_BATCH_INVARIANT,
             "row_by_row": q4.Q4MM_ROW_BY_ROW}
 
 
@@ -98,6 +99,8 @@ def test_status_codes(q4):
     assert lib.q4mm_forward_ex(W.handle, buf.data_ptr(), y.data_ptr(), 2, 0x100, None) == q4.Q4_ERR_INVALID_ARG
     assert lib.q4mm_forward_ex(W.handle, buf.data_ptr(), y.data_ptr(), 2,
                                q4.Q4MM_FORCE_SIMT | q4.Q4MM_FORCE_TC, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_forward_ex(W.handle, buf.data_ptr(), y.data_ptr(), 2,
+                               q4.Q4MM_FORCE_MMA | q4.Q4MM_ROW_BY_ROW, None) == q4.Q4_ERR_INVALID_ARG
     y.fill_(7.0)
     assert lib.q4mm_forward(W.handle, buf.data_ptr(), y.data_ptr(), 0, None) == q4.Q4_OK  # no-op
     torch.cuda.synchronize()
@@ -117,7 +120,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("N,K,Ms", CASES)
-@pytest.mark.parametrize("mode", ["auto", "simt", "invariant", "row_by_row"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "mma", "tc", "invariant", "row_by_row"])
 def test_forward_matches_oracle(q4, N, K, Ms, mode):
     w = weights(51, N % 16, N, K)
     blocks = oracle.quantize(w)
@@ -159,7 +162,7 @@ def test_special_inputs(q4):
     xs.append(acts(53, 3, K) * np.float32(1e30))
     xs.append(acts(53, 3, K) * np.float32(1e-30))
     for x in xs:
-        for mode in ("auto", "simt", "invariant"):
+        for mode in ("auto", "simt", "mma", "tc", "invariant"):
             y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), _flags(q4)[mode]).cpu().numpy()
             _, y64, bound = oracle.matmul(blocks, x)
             assert_within_bound(y, y64, bound, mode)
@@ -191,7 +194,7 @@ def test_batch_invariant_rows_bit_identical(q4, N, K):
 
 # ------------------------------------------------------------------ argmax
 
-@pytest.mark.parametrize("mode", ["auto", "simt", "invariant"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "mma", "tc", "invariant"])
 def test_argmax_matches_oracle(q4, mode):
     N, K = 1000, 512
     w = weights(55, 0, N, K)
