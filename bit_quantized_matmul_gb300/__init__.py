@@ -32,6 +32,7 @@ Q4MM_FORCE_TC = 0x4
 Q4MM_ROW_BY_ROW = 0x8
 Q4MM_FORCE_MMA = 0x10
 Q4MM_M_MAX = 4096
+Q4MM_NOALLOC_PARTIAL_BYTES = 1179648
 Q4MM_PATH_SIMT = 1
 Q4MM_PATH_TC = 2
 Q4MM_PATH_ROW_BY_ROW = 3
@@ -44,7 +45,7 @@ BLOCK_BYTES = 18
 EXPORTS = (
     "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
-    "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
+    "q4mm_forward_noalloc", "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
     "q4_status_string",
 )
 
@@ -67,6 +68,7 @@ _sig = {
     "q4mm_forward_ex": [_p, _p, _p, _i64, _u32, _p],
     "q4mm_argmax": [_p, _p, _p, _p, _i64, _p],
     "q4mm_argmax_ex": [_p, _p, _p, _p, _i64, _u32, _p],
+    "q4mm_forward_noalloc": [_p, _p, _p, _i64, _p],
     "q4mm_select_path": [_p, _i64, _u32],
     "q4mm_plan_info": [_p, _i64, _u32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                        ctypes.POINTER(ctypes.c_int)],
@@ -219,6 +221,28 @@ def q4mm_forward(W: Q4Weight, x: torch.Tensor, y: torch.Tensor | None = None, st
         raise ValueError("y must be [M, %d]" % W.N)
     with torch.cuda.device(x.device):
         _check(_lib.q4mm_forward(W.handle, x.data_ptr(), y.data_ptr(), M, _stream(stream)), "q4mm_forward")
+    return y
+
+
+def q4mm_forward_noalloc(W: Q4Weight, x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ W^T into the caller's y, allocating no device memory.
+
+    For callers that must not allocate mid-step (their memory is all in their
+    own pool, or a device-wide wait is unacceptable).  The first call on a
+    device sets up the fixed scratch and synchronizes once; calls whose kernels
+    overlap on the GPU race on that scratch.  Raises Q4Error(Q4_ERR_SHAPE) when
+    the split-K partial sums exceed Q4MM_NOALLOC_PARTIAL_BYTES.
+    """
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [M, %d]" % W.K)
+    _dev_f32(y, "y")
+    if tuple(y.shape) != (M, W.N):
+        raise ValueError("y must be [M, %d]" % W.N)
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_forward_noalloc(W.handle, x.data_ptr(), y.data_ptr(), M, _stream(stream)),
+               "q4mm_forward_noalloc")
     return y
 
 

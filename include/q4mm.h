@@ -153,6 +153,40 @@ Q4_API int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* 
 Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                    uint32_t flags, cudaStream_t stream);
 
+/* Capacity of the split-K partial sums of q4mm_forward_noalloc (1152 KiB). */
+#define Q4MM_NOALLOC_PARTIAL_BYTES 1179648
+
+/* y = x @ W^T without allocating any device memory.  (The pages have no
+ * counterpart: this is a library concern.)
+ *
+ * The other compute calls create and grow their scratch with cudaMalloc and
+ * cudaFree on the first call that needs more.  Callers that cannot allocate
+ * at that moment use this call instead: a serving process that gave all free
+ * device memory to its own pool (the allocation would fail), or a step that
+ * must not wait for the whole device, as cudaFree does.  Its scratch is one
+ * fixed device array in the library (about 1.2 MB per device, created when the
+ * library's device code is loaded), so this call allocates nothing.  (As for
+ * any CUDA library, the runtime may still load kernel code on first use.)
+ *
+ *   x, y, M   as q4mm_forward; y is fully overwritten.
+ * Always runs the streaming mma.sync kernel with its usual K partition: the
+ * results are bit-identical to q4mm_forward_ex(W, x, y, M, Q4MM_FORCE_MMA).
+ * Returns Q4_ERR_SHAPE, before any launch, if the call's split-K partial
+ * sums (splits x min(M, 16) x N rounded up to 128 x 4 bytes) exceed
+ * Q4MM_NOALLOC_PARTIAL_BYTES.  On a 152-SM GB300 every linear layer of a
+ * 7B decoder (N, K up to 18944) fits at any M; q4mm_forward has no such limit.
+ *
+ * The first call on each device sets up: it looks up the array's address,
+ * clears the counters that must start at zero and synchronizes the device
+ * once.  Make that first call before any stream capture begins.
+ * All calls on one device share the one array: calls whose kernels overlap on
+ * the GPU (other streams, other host threads) race on it and give wrong
+ * results.  Order them on one stream.  A bounded device-side wait that runs
+ * out is recorded in this array's own status word, which q4_device_status
+ * does not read; y is then unspecified. */
+Q4_API int q4mm_forward_noalloc(const q4_weight* W, const float* x, float* y, int64_t M,
+                                cudaStream_t stream);
+
 /* The kernel path (Q4MM_PATH_*) a call with these arguments would take, or a
  * negative status. */
 Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
