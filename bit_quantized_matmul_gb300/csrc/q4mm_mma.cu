@@ -1,29 +1,37 @@
-// q4mm_mma.cu — streaming tensor-core kernel for small and medium M.
+// q4mm_mma.cu — streaming tensor-core kernel for small M (the decode path).
 //
-// This is the decode path of the linear layer: M token rows (1 to 16 per
-// launch) times a Q4_0 weight matrix read from HBM exactly once per call
-// ("Why LLM Decoding Is Slow, and Why Batching Is (Almost) Free", §2-§4: decode
-// streams every weight once per step, and the extra token rows of a batch ride
-// along almost for free while the step stays memory-bound).  It replaces the
-// two kernels of "Why Continuous Batching Slowed Down My LLM Inference Engine"
+// This is the linear layer of a decode step: M token rows (1 to 8 per launch)
+// times a Q4_0 weight matrix read from HBM exactly once per call ("Why LLM
+// Decoding Is Slow, and Why Batching Is (Almost) Free", §3-§4: decode streams
+// every weight once per step, and the extra token rows of a batch ride along
+// almost for free while the step stays memory-bound).  It replaces the two
+// kernels of "Why Continuous Batching Slowed Down My LLM Inference Engine"
 // (§"Two Rows of Input, Two Different Kernels") — a one-row GEMV and a tiled
 // GEMM — with one kernel whose cost per weight hardly changes between 1 and
-// 16 rows, so no row count needs a different kernel or a per-row relaunch.
+// 8 rows, so no row count needs a different kernel or a per-row relaunch.
 //
-// Per warp: one 16-row group of a 128-row tile over the CTA's K range.  Each
-// lane loads 16 bytes per block pair (coalesced: a warp reads 512 contiguous
-// bytes) that are exactly its A fragments of two m16n8k16 MMAs per block.
-// The nibbles are unpacked in registers to exact bf16 (q - 8); the
-// activations enter as B fragments holding three exact bf16 terms
-// x = x0 + x1 + x2 per token row (term t of row m is MMA column 3m + t, or
-// column t of the row's own column group in batch-invariant mode), split
-// inside the kernel one pipeline stage ahead of their use.  The two
-// MMAs of a block accumulate D_b = sum_{k in b} (q-8) x_t in fresh fp32
-// registers; the block's fp16 scale is applied on the CUDA cores,
-// acc = fma(d, D_b, acc), in ascending block order.  At the end the three
-// terms of each token row are added in a fixed order (t = 0, 1, 2) and the
-// K splits, if any, are added in ascending split order.
-#include <cuda_bf16.h>
+// CTA = one 128-row tile over a K range (block pairs [bp0, bp1)); 640 threads:
+//
+//   16 compute warps  warp w takes row groups 2(w&3), 2(w&3)+1 (32 rows) and
+//                     K slice w>>2: block pairs bp0 + slice + 4i.  Its lanes
+//                     load their 16-byte weight fragments straight from HBM
+//                     into registers (coalesced, 1 KB per warp and pair, four
+//                     pairs in flight) — in the fragment layout they are
+//                     exactly the A registers of m16n8k16 MMAs once unpacked
+//                     to exact bf16 (q - 8).  No CTA barrier in the loop.
+//   4 converter warps stage, per chunk of 8 block pairs, the activations as
+//                     exact three-term bf16 B fragments (x = x0 + x1 + x2,
+//                     term t of row m in MMA column 3m + t, or column t of the
+//                     row's own column group in batch-invariant mode) and copy
+//                     the chunk's fp16 scales, into a 4-slot shared-memory
+//                     ring with full/empty mbarriers (every wait bounded).
+//
+// Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
+// fp32 registers; the block's fp16 scale is applied on the CUDA cores,
+// acc = fma(d, D_b, acc), in ascending block order.  At the end the four K
+// slices and the three terms of each row are added in a fixed order, then the
+// K splits in ascending split order (q4mm_epilogue.cuh).  Nothing in that
+// order depends on M.
 #include <cuda_fp16.h>
 
 #include "q4mm_epilogue.cuh"
@@ -32,26 +40,48 @@
 namespace q4 {
 namespace {
 
-constexpr int MAX_CG = 6;         // column groups per launch (48 MMA columns)
+constexpr int MAX_CG = 3;          // column groups per launch (24 MMA columns)
+constexpr int SLICES = 4;          // K slices per CTA
+constexpr int COMPUTE_WARPS = 16;  // 4 row-group pairs x 4 slices
+constexpr int CONV_WARPS = 4;
+constexpr int COMPUTE_THREADS = COMPUTE_WARPS * 32;
+constexpr int CONV_THREADS = CONV_WARPS * 32;
+constexpr int KERNEL_THREADS = COMPUTE_THREADS + CONV_THREADS;
+constexpr int CHUNK_PAIRS = 8;              // block pairs per ring slot (512 k)
+constexpr int CHUNK_K = CHUNK_PAIRS * 64;
+constexpr int NSLOT = 4;                    // ring depth (a power of two)
 
 struct MmaArgs {
   const uint4* nib;     // fragment layout, 16 bytes per (tile, pair, rg, lane)
-  const uint2* scl;     // 8 bytes per (tile, pair, rg, g)
+  const uint8_t* scl;   // scale plane, 512 bytes per (tile, pair)
   const float* x;       // [mrows, K] activations of this launch
   int64_t K, KBP;       // K, block pairs
   int mrows;            // token rows in this launch
-  int dense;            // 1: column 3m + t; 0: column 8m + t (one row per group)
   int64_t kbp_per_split;
   unsigned int* status; // device status word (bounded-wait expiry)
   EpiArgs e;
 };
 
+template <int C>
+struct MmaCfg {
+  static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
+  static constexpr int BF_PAIR = C * 1024;  // B fragments of a pair: [cg][h][32 slots] x 16 B
+  static constexpr int SCL_OFF = CHUNK_PAIRS * BF_PAIR;
+  static constexpr int SLOT = SCL_OFF + CHUNK_PAIRS * PAIR_SCL_BYTES;
+  static constexpr int RING = NSLOT * SLOT;
+  static constexpr int RED = SLICES * C * 8 * (TILE_N + 1) * 4;  // per-slice sums for the gather
+  static constexpr int BAR_OFF = RING > RED ? RING : RED;
+  static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
+  static constexpr int PREFETCH = 2;  // weight pairs in flight per warp (registers)
+};
+
 // bf16 pair (q - 8) for nibble pair p of word w: 0x4300 | q is bf16(128 + q),
-// and one bf16x2 FMA x * 1 + (-136) is exact.
+// and one bf16x2 subtraction of 136 is exact.
 __device__ __forceinline__ uint32_t nib_pair(uint32_t w, int p) {
-  const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-  uint32_t r;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
+  uint32_t t, r;
+  // (w >> 4p) & 0x000F000F | 0x43004300 as one three-input logic op
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(w >> (4 * p)));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
   return r;
 }
 
@@ -71,45 +101,13 @@ __device__ __forceinline__ void mma_bf16_acc(float (&d)[4], const uint32_t (&a)[
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// ----------------------------------------------------------------------------
-// Main kernel.  Grid (tiles, splits), one CTA per SM: 16 compute warps (warp w
-// takes row group w % 8 of the 128-row tile and block pair w / 8 of each
-// stage) + 1 producer warp.
-//
-// A ring of STAGES shared-memory stages holds two block pairs (128 k) of the
-// tile each: 8 KB of weight fragments and 1 KB of scales, brought in by the
-// producer with two bulk copies completing on the stage's mbarrier (the
-// tile's block pairs are contiguous in the fragment layout).  The activations
-// of a stage are read from global memory (tiny and shared by every CTA, so
-// they stay in L2) two stages ahead into registers, split into exact bf16 B
-// fragments one stage ahead and stored in the stage's fragment area.  One
-// __syncthreads per iteration publishes the fragments and retires the slot
-// the producer refills next.  The two warps of a row group add their sums in
-// a fixed order at the end.
-// ----------------------------------------------------------------------------
-constexpr int COMPUTE_WARPS = 16;
-constexpr int COMPUTE_THREADS = COMPUTE_WARPS * 32;
-constexpr int KERNEL_THREADS = COMPUTE_THREADS + 32;
-constexpr int PAIRS_PER_STAGE = 2;
-constexpr int SMEM_LIMIT = 220 * 1024;
-
-template <int C>
-struct MmaCfg {
-  static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
-  static constexpr int NIB = PAIRS_PER_STAGE * PAIR_NIB_BYTES;     // [pair][rg][lane] 16 B
-  static constexpr int SCL = PAIRS_PER_STAGE * PAIR_SCL_BYTES;     // [pair][rg][g] 8 B
-  static constexpr int XF = PAIRS_PER_STAGE * C * 2 * 32 * 16;     // [pair][cg][h][lane] 16 B
-  static constexpr int SCL_OFF = NIB;
-  static constexpr int XF_OFF = NIB + SCL;
-  static constexpr int STAGE = XF_OFF + XF;
-  static constexpr int RED = C * 8 * (TILE_N + 1) * 4 * 2;  // two partial sums per row
-  static constexpr int STAGES_RAW = (SMEM_LIMIT - 256) / STAGE;
-  static constexpr int STAGES = STAGES_RAW >= 16 ? 16 : 8;  // a power of two
-  static constexpr int RING = STAGE * STAGES;
-  static constexpr int BAR_OFF = RING > RED ? RING : RED;
-  static constexpr int BYTES = BAR_OFF + STAGES * 8;
-  static_assert(STAGES >= 4, "pipeline too shallow");
-};
+__device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -117,9 +115,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -137,214 +134,292 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait (1 s); returns false on expiry.  The timer is read only after
-// many polls, off the common path.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Bounded wait (1 s, or until another thread of the CTA reported an expiry);
+// returns false on expiry.  The timer is read only after many polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0u) {
+      if (*err) return false;
       const unsigned long long now = globaltimer();
       if (t0 == 0) t0 = now;
       else if (now - t0 > 1000000000ull) return false;
     }
   }
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// The mbarrier receives one arrival when all earlier cp.async of this thread
+// have landed (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-template <int C>
+// Exact three-term bf16 split of two consecutive activations: term 0 is the
+// top 16 bits of x (truncation), term 1 the top 16 bits of the exact
+// remainder, term 2 the rest (at most 8 significant bits, exact in bf16).
+// Each term packs (k, k + 1) as a bf16x2 word, k in the low half.
+__device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_t& t1,
+                                       uint32_t& t2) {
+  uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+  t0 = __byte_perm(u0, u1, 0x7632);
+  float r0 = x0 - __uint_as_float(u0 & 0xFFFF0000u);
+  float r1 = x1 - __uint_as_float(u1 & 0xFFFF0000u);
+  u0 = __float_as_uint(r0);
+  u1 = __float_as_uint(r1);
+  t1 = __byte_perm(u0, u1, 0x7632);
+  r0 -= __uint_as_float(u0 & 0xFFFF0000u);
+  r1 -= __uint_as_float(u1 & 0xFFFF0000u);
+  t2 = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+}
+
+// ----------------------------------------------------------------------------
+// Shared-memory B fragments of one block pair: [cg][h][32 slots] x 16 bytes,
+// slot of lane L = 4g + tq at L ^ sw with sw = 4 (pair & 1) + h, so that the
+// converters' scattered 4-byte stores hit 32 distinct banks (a compute warp
+// reads its 512 contiguous bytes conflict-free in any slot order).  The slot
+// holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
+// ----------------------------------------------------------------------------
+template <int C, bool DENSE>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
   using S = MmaCfg<C>;
   constexpr int MAXM = S::MAXM;
-  constexpr int STAGES = S::STAGES;
-  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int PREFETCH = S::PREFETCH;
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ unsigned long long kred[4][MAXM];
   __shared__ int s_flag;
-  __shared__ int s_err;
+  __shared__ volatile int s_err;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const bool producer = warp == COMPUTE_WARPS;
-  const int g = lane >> 2, tq = lane & 3;
-  const int rg = warp & 7, pis = (warp >> 3) & 1;  // row group, pair within a stage
   const int64_t tile = blockIdx.x;
   const int split = blockIdx.y;
   const int64_t bp0 = (int64_t)split * a.kbp_per_split;
   const int64_t bp1 = min(a.KBP, bp0 + a.kbp_per_split);
   const int npairs = (int)(bp1 - bp0);
-  const int nst = (npairs + PAIRS_PER_STAGE - 1) / PAIRS_PER_STAGE;  // stages of this CTA
+  const int nchunks = (npairs + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
   const int mrows = a.mrows;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  uint64_t* bfull = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  uint64_t* bempty = bfull + NSLOT;
+  const bool compute = warp < COMPUTE_WARPS;
 
-  // conversion work items: pair (k, k + 1) of row m in a stage (128 k = 64 pairs)
-  const int items = 64 * mrows;
-  const int conv_passes = producer ? 0 : (tid < items) + (tid + COMPUTE_THREADS < items);
-  const float* conv_src[2];
-  int64_t conv_k_end[2];
-  uint32_t conv_dst[2][3];
+  // compute warps: first weight loads before anything else (weights never
+  // depend on an earlier kernel)
+  const int rgp = warp & 3, sl = (warp >> 2) & 3;
+  const int n_i = (compute && npairs > sl) ? (npairs - sl + SLICES - 1) / SLICES : 0;
+  const uint4* wp = a.nib + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
+  constexpr int64_t WSTEP = SLICES * 8 * 32;  // uint4 between a slice's consecutive pairs
+  uint4 wb[PREFETCH][2];
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int jj = tid + r * COMPUTE_THREADS;
-    const int m = r < conv_passes ? (jj >> 6) : 0, pp = jj & 63;
-    const int kk = 2 * pp;                      // 0..126 within the stage
-    const int pr = kk >> 6;                     // pair of the stage
-    const int h = (kk >> 5) & 1, kb = kk & 31;  // block of the pair, k within block
-    const int sks = kb >> 4, ks = kb & 15, half = ks >> 3, tql = (ks & 7) >> 1;
-    conv_src[r] = a.x + (int64_t)m * a.K + bp0 * 64 + kk;
-    conv_k_end[r] = a.K - bp0 * 64 - kk;  // the pair of stage i is real iff 128 i < this
-#pragma unroll
-    for (int t = 0; t < 3; ++t) {
-      const int c = a.dense ? 3 * m + t : 8 * m + t;
-      const int cg = c >> 3, gl = c & 7;
-      conv_dst[r][t] = (uint32_t)(S::XF_OFF + (((pr * C + cg) * 2 + h) * 32 + 4 * gl + tql) * 16 +
-                                  (2 * sks + half) * 4);
+  for (int u = 0; u < PREFETCH; ++u) {
+    wb[u][0] = wb[u][1] = make_uint4(0u, 0u, 0u, 0u);
+    if (u < n_i) {
+      wb[u][0] = ld_stream16(wp + u * WSTEP);
+      wb[u][1] = ld_stream16(wp + u * WSTEP + 32);
     }
   }
-  auto load_raw = [&](int i, float2 (&v)[2]) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      v[r] = make_float2(0.0f, 0.0f);
-      if (r < conv_passes && i < nst && (int64_t)i * 128 < conv_k_end[r])
-        v[r] = __ldg(reinterpret_cast<const float2*>(conv_src[r] + (int64_t)i * 128));
-    }
-  };
-  auto convert = [&](int i, const float2 (&v)[2]) {
-    if (i >= nst || conv_passes == 0) return;
-    uint8_t* st = smem + (i & (STAGES - 1)) * S::STAGE;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (r < conv_passes) {
-        float v0 = v[r].x, v1 = v[r].y;
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {  // exact split x = x0 + x1 + x2, each bf16
-          const __nv_bfloat162 p = __floats2bfloat162_rn(v0, v1);
-          v0 -= __low2float(p);
-          v1 -= __high2float(p);
-          *reinterpret_cast<__nv_bfloat162*>(st + conv_dst[r][t]) = p;
+
+  // zero the B-fragment columns no converter writes: the last column group
+  // (dense packing with 3 * mrows < 8C) or every group (one row per group)
+  {
+    const bool part = DENSE ? (3 * mrows < 8 * C) : true;
+    if (part) {
+      constexpr int PER_SLOT = DENSE ? CHUNK_PAIRS * 2 * 32 : CHUNK_PAIRS * C * 2 * 32;  // uint4
+      for (int j = tid; j < NSLOT * PER_SLOT; j += KERNEL_THREADS) {
+        const int slot = j / PER_SLOT, r = j % PER_SLOT;
+        int off;
+        if (DENSE) {
+          const int pc = r >> 6, h = (r >> 5) & 1, q = r & 31;
+          off = ((pc * C + (C - 1)) * 2 + h) * 512 + q * 16;
+        } else {
+          off = r * 16;
         }
+        *reinterpret_cast<uint4*>(smem + slot * S::SLOT + off) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-  };
-
-  // producer: block pairs [bp0 + 2i, bp0 + 2i + 2) of the tile into stage i
-  const uint8_t* nib_g = reinterpret_cast<const uint8_t*>(a.nib) + (tile * a.KBP + bp0) * PAIR_NIB_BYTES;
-  const uint8_t* scl_g = reinterpret_cast<const uint8_t*>(a.scl) + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
-  int produced = 0;
-  auto produce = [&](int i) {
-    if (i < nst) {
-      produced = i + 1;
-      const int np = min(PAIRS_PER_STAGE, npairs - i * PAIRS_PER_STAGE);
-      const uint32_t st = smem_u32(smem + (i & (STAGES - 1)) * S::STAGE);
-      const uint32_t bar = smem_u32(&full[i & (STAGES - 1)]);
-      mbar_expect_tx(bar, (uint32_t)(np * (PAIR_NIB_BYTES + PAIR_SCL_BYTES)));
-      bulk_g2s(st, nib_g + (int64_t)i * S::NIB, np * PAIR_NIB_BYTES, bar);
-      bulk_g2s(st + S::SCL_OFF, scl_g + (int64_t)i * S::SCL, np * PAIR_SCL_BYTES, bar);
-    }
-  };
-
-  // zero every fragment slot once: padding columns are never written again
-  for (int j = tid; j < STAGES * (S::XF / 16); j += KERNEL_THREADS) {
-    const int stg = j / (S::XF / 16), w = j % (S::XF / 16);
-    *reinterpret_cast<uint4*>(smem + stg * S::STAGE + S::XF_OFF + w * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   if (tid == 0) {
-    for (int b = 0; b < STAGES; ++b) mbar_init(smem_u32(&full[b]), 1);
+    for (int b = 0; b < NSLOT; ++b) {
+      mbar_init(smem_u32(&bfull[b]), 2 * CONV_THREADS);  // converter stores + their scale copies
+      mbar_init(smem_u32(&bempty[b]), COMPUTE_WARPS);
+    }
     s_err = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (producer && lane == 0) {
-    for (int i = 0; i < STAGES - 1; ++i) produce(i);  // weights do not depend on earlier kernels
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // activations may come from the previous kernel
 
-  float acc[C][4];
+  float acc[2][C][4];
 #pragma unroll
-  for (int cg = 0; cg < C; ++cg)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[cg][e] = 0.0f;
-
-  float2 raw_a[2], raw_b[2];  // activations of stages i + 1 and i + 2
-  load_raw(0, raw_a);
-  convert(0, raw_a);
-  load_raw(1, raw_a);
-  load_raw(2, raw_b);
-
-  for (int i = 0; i < nst; ++i) {
-    __syncthreads();  // stage i's fragments visible; slot of stage i - 1 retired
-    if (s_err) break;  // uniform: read after the barrier by every thread
-    if (producer) {
-      if (lane == 0) produce(i + STAGES - 1);
-      continue;
-    }
-    convert(i + 1, raw_a);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) raw_a[r] = raw_b[r];
-    load_raw(i + 3, raw_b);
-    const int slot = i & (STAGES - 1);
-    if (!mbar_wait_bounded(smem_u32(&full[slot]), (uint32_t)((i / STAGES) & 1))) {
-      s_err = 1;  // skip this stage; every thread leaves at the next barrier
-      continue;
-    }
-    if (i * PAIRS_PER_STAGE + pis >= npairs) continue;  // odd pair count: no second pair
-    const uint8_t* st = smem + slot * S::STAGE;
-    const uint4 wv = *reinterpret_cast<const uint4*>(st + ((pis * 8 + rg) * 32 + lane) * 16);
-    const uint2 sv = *reinterpret_cast<const uint2*>(st + S::SCL_OFF + ((pis * 8 + rg) * 8 + g) * 8);
-    const float2 dr0 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));  // d(R0, b0/b1)
-    const float2 dr1 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));  // d(R1, b0/b1)
-    const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-    const uint4* xf = reinterpret_cast<const uint4*>(st + S::XF_OFF) + pis * (C * 64) + lane;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t a0[4], a1[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        a0[p] = nib_pair(w4[2 * h], p);      // k-step 0 of block h of the pair
-        a1[p] = nib_pair(w4[2 * h + 1], p);  // k-step 1
-      }
-      const float d0 = h ? dr0.y : dr0.x, d1 = h ? dr1.y : dr1.x;
-#pragma unroll
-      for (int cg = 0; cg < C; ++cg) {
-        const uint4 bf = xf[(cg * 2 + h) * 32];
-        float d[4];
-        mma_bf16_first(d, a0, bf.x, bf.y);
-        mma_bf16_acc(d, a1, bf.z, bf.w);
-        acc[cg][0] = fmaf(d0, d[0], acc[cg][0]);
-        acc[cg][1] = fmaf(d0, d[1], acc[cg][1]);
-        acc[cg][2] = fmaf(d1, d[2], acc[cg][2]);
-        acc[cg][3] = fmaf(d1, d[3], acc[cg][3]);
-      }
-    }
-  }
-  // On the normal path every issued stage was waited for.  After a timeout
-  // the producer waits (bounded) for the copies it issued before the CTA exits.
-  __syncthreads();
-  if (s_err) {
-    if (producer && lane == 0) {
-      for (int i = (produced > STAGES ? produced - STAGES : 0); i < produced; ++i)
-        mbar_wait_bounded(smem_u32(&full[i & (STAGES - 1)]), (uint32_t)((i / STAGES) & 1));
-      atomicOr(a.status, (unsigned)Q4_ERR_TIMEOUT);
-    }
-    return;
-  }
-
-  // ---- gather: per tile row and MMA column, the two pair-in-stage halves ----
-  float* red = reinterpret_cast<float*>(smem);  // [2][C*8][TILE_N + 1]
-  constexpr int RS = C * 8 * (TILE_N + 1);
-  if (!producer) {
+  for (int r = 0; r < 2; ++r)
 #pragma unroll
     for (int cg = 0; cg < C; ++cg)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        red[pis * RS + (cg * 8 + 2 * tq + (e & 1)) * (TILE_N + 1) + rg * 16 + g + 8 * (e >> 1)] =
-            acc[cg][e];
+      for (int e = 0; e < 4; ++e) acc[r][cg][e] = 0.0f;
+
+  if (compute) {
+    const int g = lane >> 2;
+    const int lsw0 = (lane ^ ((sl & 1) * 4)) * 16;        // slot of this lane, h = 0
+    const int lsw1 = (lane ^ ((sl & 1) * 4 + 1)) * 16;    // h = 1
+    for (int i0 = 0; i0 < n_i; i0 += PREFETCH) {
+#pragma unroll
+      for (int u = 0; u < PREFETCH; ++u) {
+        const int i = i0 + u;
+        if (i >= n_i) break;
+        const int c = i >> 1;
+        const int slot = c & (NSLOT - 1);
+        if ((i & 1) == 0 &&
+            !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
+          s_err = 1;
+          goto compute_done;
+        }
+        const uint4 w0 = wb[u][0], w1 = wb[u][1];
+        const int pc = sl + 4 * (i & 1);  // pair within the chunk
+        const uint8_t* sb = smem + slot * S::SLOT;
+        const uint2 sv0 = *reinterpret_cast<const uint2*>(sb + S::SCL_OFF + pc * PAIR_SCL_BYTES +
+                                                          ((2 * rgp) * 8 + g) * 8);
+        const uint2 sv1 = *reinterpret_cast<const uint2*>(sb + S::SCL_OFF + pc * PAIR_SCL_BYTES +
+                                                          ((2 * rgp + 1) * 8 + g) * 8);
+        // sv.x = d(R0, b0), d(R0, b1); sv.y = d(R1, b0), d(R1, b1) of each row group
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a00[4], a01[4], a10[4], a11[4];  // [rg][k-step]
+          const uint32_t x0 = h ? w0.z : w0.x, x1 = h ? w0.w : w0.y;
+          const uint32_t y0 = h ? w1.z : w1.x, y1 = h ? w1.w : w1.y;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            a00[p] = nib_pair(x0, p);
+            a01[p] = nib_pair(x1, p);
+            a10[p] = nib_pair(y0, p);
+            a11[p] = nib_pair(y1, p);
+          }
+          if (h == 1 && i + PREFETCH < n_i) {  // refill once the pair's words are unpacked
+            wb[u][0] = ld_stream16(wp + (int64_t)(i + PREFETCH) * WSTEP);
+            wb[u][1] = ld_stream16(wp + (int64_t)(i + PREFETCH) * WSTEP + 32);
+          }
+          const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
+          const __half2* q1 = reinterpret_cast<const __half2*>(&sv1);
+          const float s00 = h ? __high2float(q0[0]) : __low2float(q0[0]);
+          const float s01 = h ? __high2float(q0[1]) : __low2float(q0[1]);
+          const float s10 = h ? __high2float(q1[0]) : __low2float(q1[0]);
+          const float s11 = h ? __high2float(q1[1]) : __low2float(q1[1]);
+          const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
+#pragma unroll
+          for (int cg = 0; cg < C; ++cg) {
+            const uint4 bf = *reinterpret_cast<const uint4*>(bb + cg * 1024);
+            float d[4];
+            mma_bf16_first(d, a00, bf.x, bf.y);
+            mma_bf16_acc(d, a01, bf.z, bf.w);
+            acc[0][cg][0] = fmaf(s00, d[0], acc[0][cg][0]);
+            acc[0][cg][1] = fmaf(s00, d[1], acc[0][cg][1]);
+            acc[0][cg][2] = fmaf(s01, d[2], acc[0][cg][2]);
+            acc[0][cg][3] = fmaf(s01, d[3], acc[0][cg][3]);
+            float e[4];
+            mma_bf16_first(e, a10, bf.x, bf.y);
+            mma_bf16_acc(e, a11, bf.z, bf.w);
+            acc[1][cg][0] = fmaf(s10, e[0], acc[1][cg][0]);
+            acc[1][cg][1] = fmaf(s10, e[1], acc[1][cg][1]);
+            acc[1][cg][2] = fmaf(s11, e[2], acc[1][cg][2]);
+            acc[1][cg][3] = fmaf(s11, e[3], acc[1][cg][3]);
+          }
+        }
+        if ((i & 1) && c + NSLOT < nchunks) {  // this warp is done with the slot
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bempty[slot]));
+        }
+      }
+    }
+  compute_done:;
+  } else {
+    // ---- converter warps ----
+    const int ct = tid - COMPUTE_THREADS;  // k = 4ct .. 4ct + 3 of each chunk
+    const int pc = ct >> 4, h = (ct >> 3) & 1, j = (ct >> 1) & 3, tql = 2 * (ct & 1);
+    // byte offset of column (cg, gl) for the k pairs 4ct (.x/.y) and 4ct + 2 (.z/.w)
+    const int kbase = (pc * C * 2 + h) * 512 + j * 4;
+    const int s2 = pc & 1;
+    const int oa = ((tql) ^ h) * 16, ob = ((tql + 1) ^ h) * 16;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+    const float* xr = a.x + bp0 * 64 + 4 * ct;
+    const uint8_t* sg = a.scl + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
+    for (int c = 0; c < nchunks; ++c) {
+      const int slot = c & (NSLOT - 1);
+      uint8_t* sb = smem + slot * S::SLOT;
+      const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
+      const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
+      if (c >= NSLOT &&
+          !mbar_wait_bounded(smem_u32(&bempty[slot]), (uint32_t)(((c / NSLOT) + 1) & 1), &s_err)) {
+        s_err = 1;
+        break;
+      }
+      const int scl_bytes = min(CHUNK_PAIRS, npairs - c * CHUNK_PAIRS) * PAIR_SCL_BYTES;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int q = ct + r * CONV_THREADS;
+        if (q * 16 < scl_bytes)
+          cp_async16(smem_u32(sb + S::SCL_OFF + q * 16),
+                     sg + (int64_t)c * CHUNK_PAIRS * PAIR_SCL_BYTES + q * 16);
+      }
+      cp_async_arrive(smem_u32(&bfull[slot]));
+      if (pair_ok) {
+        constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows loaded together
+#pragma unroll
+        for (int m0 = 0; m0 < MAXM; m0 += MG) {
+          float4 v[MG];
+#pragma unroll
+          for (int mm = 0; mm < MG; ++mm) {
+            v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (m0 + mm < mrows && k_ok)
+              v[mm] = __ldg(reinterpret_cast<const float4*>(xr + (int64_t)(m0 + mm) * a.K +
+                                                            (int64_t)c * CHUNK_K));
+          }
+#pragma unroll
+          for (int mm = 0; mm < MG; ++mm) {
+            const int m = m0 + mm;
+            if (m < mrows) {
+              uint32_t ta[3], tb[3];
+              split3(v[mm].x, v[mm].y, ta[0], ta[1], ta[2]);
+              split3(v[mm].z, v[mm].w, tb[0], tb[1], tb[2]);
+#pragma unroll
+              for (int t = 0; t < 3; ++t) {
+                const int col = DENSE ? 3 * m + t : 8 * m + t;
+                const int cg = col >> 3, gl = col & 7;
+                uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
+                *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
+                *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
+              }
+            }
+          }
+        }
+      }
+      mbar_arrive(smem_u32(&bfull[slot]));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after the previous kernel
+  __syncthreads();
+  if (s_err) {
+    if (tid == 0) atomicOr(a.status, (unsigned)Q4_ERR_TIMEOUT);
+    return;
+  }
+
+  // ---- gather: per tile row and MMA column, the four K slices ----
+  float* red = reinterpret_cast<float*>(smem);  // [SLICES][C*8][TILE_N + 1]
+  constexpr int RS = C * 8 * (TILE_N + 1);
+  if (compute) {
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int cg = 0; cg < C; ++cg)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * (TILE_N + 1) + (2 * rgp + r) * 16 + g +
+              8 * (e >> 1)] = acc[r][cg][e];
   }
   __syncthreads();
 
@@ -356,11 +431,12 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
       if (m < mrows) {
-        const int c0 = a.dense ? 3 * m : 8 * m;
+        const int c0 = DENSE ? 3 * m : 8 * m;
         float v = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each the even + odd pair sums
-          v += red[(c0 + t) * (TILE_N + 1) + row] + red[RS + (c0 + t) * (TILE_N + 1) + row];
+        for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each slice 0..3
+#pragma unroll
+          for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * (TILE_N + 1) + row];
         val[m] = v;
       }
     }
@@ -369,18 +445,17 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
                     []() { __syncthreads(); });
 }
 
-template <int C>
-int launch_c(const Weight* W, const float* x, int mrows, int dense, float* y, int32_t* idx,
-             float* maxval, const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
+template <int C, bool DENSE>
+int launch_c(const Weight* W, const float* x, int mrows, float* y, int32_t* idx, float* maxval,
+             const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
   using S = MmaCfg<C>;
   MmaArgs a;
   a.nib = reinterpret_cast<const uint4*>(W->nib);
-  a.scl = reinterpret_cast<const uint2*>(W->d);
+  a.scl = reinterpret_cast<const uint8_t*>(W->d);
   a.x = x;
   a.K = W->K;
   a.KBP = W->KBP;
   a.mrows = mrows;
-  a.dense = dense;
   a.kbp_per_split = plan.kbp_per_split;
   a.status = ws.status;
   a.e.N = W->N;
@@ -397,7 +472,7 @@ int launch_c(const Weight* W, const float* x, int mrows, int dense, float* y, in
   a.e.tiles = (int)W->tiles;
   static bool attr_set[64] = {};
   if (!attr_set[W->device & 63]) {
-    if (cudaFuncSetAttribute(mma_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W->device & 63] = true;
@@ -412,11 +487,11 @@ int launch_c(const Weight* W, const float* x, int mrows, int dense, float* y, in
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
-// Rows per launch: 16 with dense packing (6 column groups), 6 with one row
-// per column group (batch-invariant mode).
+// Rows per launch: 8 with dense packing (3 column groups), 3 with one row per
+// column group (batch-invariant mode).
 int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (MAX_CG * 8) / 3; }
 
 }  // namespace
@@ -424,12 +499,11 @@ int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (M
 MmaPlan mma_plan(const Weight* W, int num_sms) {
   // K partition from N and K only (never from M).  One CTA per SM: splits =
   // floor(SMs / tiles) for a single wave, at least one, and small enough that
-  // each CTA keeps at least four stages (eight block pairs).
+  // each CTA keeps at least two block pairs.
   MmaPlan p;
   int64_t sp = (int64_t)num_sms / W->tiles;
-  int64_t cap = W->KBP / (4 * PAIRS_PER_STAGE);
+  int64_t cap = W->KBP / 2;
   if (cap < 1) cap = 1;
-  if (cap > 64) cap = 64;
   if (sp < 1) sp = 1;
   if (sp > cap) sp = cap;
   p.kbp_per_split = (W->KBP + sp - 1) / sp;
@@ -452,21 +526,23 @@ int mma_launch_count(int64_t M, bool batch_invariant) {
 int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
                const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s) {
   const int64_t rpl = rows_per_launch(batch_invariant);
-  const int dense = batch_invariant ? 0 : 1;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     if (plan.splits > 1 && W->tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
-    // column groups needed for this launch
-    const int ncg = dense ? (3 * mrows + 7) / 8 : mrows;
     const float* xs = x + mb * W->K;
     int st;
-    switch (ncg) {
-      case 1: st = launch_c<1>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
-      case 2: st = launch_c<2>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
-      case 3: st = launch_c<3>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
-      case 4: st = launch_c<4>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
-      case 5: st = launch_c<5>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
-      default: st = launch_c<6>(W, xs, mrows, dense, y, idx, maxval, plan, ws, mb, s); break;
+    if (batch_invariant) {
+      switch (mrows) {
+        case 1: st = launch_c<1, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        case 2: st = launch_c<2, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        default: st = launch_c<3, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+      }
+    } else {
+      switch ((3 * mrows + 7) / 8) {  // column groups of this launch
+        case 1: st = launch_c<1, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        case 2: st = launch_c<2, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        default: st = launch_c<3, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+      }
     }
     if (st) return st;
   }

@@ -153,8 +153,8 @@ Q4_API int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* 
 Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                    uint32_t flags, cudaStream_t stream);
 
-/* Capacity of the split-K partial sums of q4mm_forward_noalloc (1152 KiB). */
-#define Q4MM_NOALLOC_PARTIAL_BYTES 1179648
+/* Capacity of the split-K partial sums of q4mm_forward_noalloc (600 KiB). */
+#define Q4MM_NOALLOC_PARTIAL_BYTES 614400
 
 /* y = x @ W^T without allocating any device memory.  (The pages have no
  * counterpart: this is a library concern.)
@@ -164,7 +164,7 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
  * at that moment use this call instead: a serving process that gave all free
  * device memory to its own pool (the allocation would fail), or a step that
  * must not wait for the whole device, as cudaFree does.  Its scratch is one
- * fixed device array in the library (about 1.2 MB per device, created when the
+ * fixed device array in the library (about 0.65 MB per device, created when the
  * library's device code is loaded), so this call allocates nothing.  (As for
  * any CUDA library, the runtime may still load kernel code on first use.)
  *
@@ -172,7 +172,7 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
  * Always runs the streaming mma.sync kernel with its usual K partition: the
  * results are bit-identical to q4mm_forward_ex(W, x, y, M, Q4MM_FORCE_MMA).
  * Returns Q4_ERR_SHAPE, before any launch, if the call's split-K partial
- * sums (splits x min(M, 16) x N rounded up to 128 x 4 bytes) exceed
+ * sums (splits x min(M, 8) x N rounded up to 128 x 4 bytes) exceed
  * Q4MM_NOALLOC_PARTIAL_BYTES.  On a 152-SM GB300 every linear layer of a
  * 7B decoder (N, K up to 18944) fits at any M; q4mm_forward has no such limit.
  *

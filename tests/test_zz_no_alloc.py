@@ -42,12 +42,12 @@ def _setup(N, K, c, m):
 def _partial_need(W, M):
     _, _, splits = q4.q4mm_plan_info(W, M, q4.Q4MM_FORCE_MMA)
     n_pad = (W.N + 127) // 128 * 128
-    return 0 if splits <= 1 else splits * min(M, 16) * n_pad * 4
+    return 0 if splits <= 1 else splits * min(M, 8) * n_pad * 4
 
 
-# (N, K, token-row counts): ragged tiles, a 7-way K split with launches of
-# 16 + 16 + 8 rows, the largest scratch of a 7B layer (q_proj at M = 16), and
-# a one-split shape.
+# (N, K, token-row counts): ragged tiles, a many-way K split with launches
+# of 8 + ... rows, the largest scratch of a 7B layer (q_proj at M >= 8), and a
+# one-split shape.
 CASES = [
     (300, 1024, (1, 5, 17)),
     (512, 3584, (1, 4, 16, 40)),
@@ -101,12 +101,12 @@ def test_noalloc_allocates_no_device_memory():
 
 
 def test_noalloc_rejects_oversized_calls_before_launch():
-    # 1024 x 18944: 8 tiles, so a 152-SM device splits K 19 ways and 16 rows
-    # need 19 * 16 * 1024 * 4 bytes of partial sums, more than the capacity.
+    # 1024 x 18944: 8 tiles, so a 152-SM device splits K 19 ways and 8 rows
+    # need 19 * 8 * 1024 * 4 bytes of partial sums, more than the capacity.
     N, K = 1024, 18944
     W, blocks = _setup(N, K, 92, 0)
     checked_reject = False
-    for M in (14, 15, 16, 33):
+    for M in (6, 7, 8, 33):
         x_np = acts(92, M, K)
         x = torch.from_numpy(x_np).cuda()
         y = torch.full((M, N), float("nan"), device="cuda")
@@ -124,10 +124,10 @@ def test_noalloc_rejects_oversized_calls_before_launch():
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
         assert checked_reject
     # the ordinary entry point has no such limit
-    x = torch.from_numpy(acts(92, 16, K)).cuda()
+    x = torch.from_numpy(acts(92, 8, K)).cuda()
     y = q4.q4mm_forward(W, x)
-    _, y64, bound = oracle.matmul(blocks, acts(92, 16, K))
-    assert_within_bound(y.cpu().numpy(), y64, bound, "q4mm_forward M=16")
+    _, y64, bound = oracle.matmul(blocks, acts(92, 8, K))
+    assert_within_bound(y.cpu().numpy(), y64, bound, "q4mm_forward M=8")
     W.free()
 
 
