@@ -77,14 +77,27 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MAXM]
     if (!*s_flag) return;
     __threadfence();
     if (row >= 0) {
+      // ascending split order per output; the loads of a batch of splits for
+      // every token row are issued before any of them is added
+      constexpr int SB = 4;
+      const int64_t sstride = e.M * e.N_pad;
+      const float* pp = e.partial + (m0 * e.N_pad + n);
 #pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        if (m < mcount) {
-          float v = 0.0f;
-          for (int s = 0; s < e.splits; ++s)
-            v += __ldcg(&e.partial[((int64_t)s * e.M + m0 + m) * e.N_pad + n]);
-          val[m] = v;
-        }
+      for (int m = 0; m < MAXM; ++m) val[m] = 0.0f;
+      for (int s0 = 0; s0 < e.splits; s0 += SB) {
+        float t[MAXM][SB];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+#pragma unroll
+          for (int j = 0; j < SB; ++j)
+            t[m][j] = (m < mcount && s0 + j < e.splits)
+                          ? __ldcg(pp + (int64_t)(s0 + j) * sstride + (int64_t)m * e.N_pad)
+                          : 0.0f;
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+#pragma unroll
+          for (int j = 0; j < SB; ++j)
+            if (s0 + j < e.splits) val[m] += t[m][j];
       }
     }
     if (row == 0) e.counters[counter_slot] = 0u;  // ready for the next launch
