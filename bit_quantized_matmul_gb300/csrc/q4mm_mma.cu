@@ -22,9 +22,10 @@
 //   4 converter warps stage, per chunk of 8 block pairs, the activations as
 //                     exact three-term bf16 B fragments (x = x0 + x1 + x2,
 //                     term t of row m in MMA column 3m + t, or column t of the
-//                     row's own column group in batch-invariant mode) and copy
-//                     the chunk's fp16 scales, into a 4-slot shared-memory
-//                     ring with full/empty mbarriers (every wait bounded).
+//                     row's own column group in batch-invariant mode) and the
+//                     chunk's fp16 scales, into a 4-slot shared-memory ring
+//                     with full/empty mbarriers (every wait bounded).  Their
+//                     inputs arrive by cp.async two chunks ahead.
 //
 // Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
 // fp32 registers; the block's fp16 scale is applied on the CUDA cores,
@@ -50,6 +51,7 @@ constexpr int KERNEL_THREADS = COMPUTE_THREADS + CONV_THREADS;
 constexpr int CHUNK_PAIRS = 8;              // block pairs per ring slot (512 k)
 constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 constexpr int NSLOT = 4;                    // ring depth (a power of two)
+constexpr int XSTAGES = 3;                  // converter staging slots (chunks in flight)
 
 struct MmaArgs {
   const uint4* nib;     // fragment layout, 16 bytes per (tile, pair, rg, lane)
@@ -69,8 +71,11 @@ struct MmaCfg {
   static constexpr int SCL_OFF = CHUNK_PAIRS * BF_PAIR;
   static constexpr int SLOT = SCL_OFF + CHUNK_PAIRS * PAIR_SCL_BYTES;
   static constexpr int RING = NSLOT * SLOT;
+  // converter staging: per slot the chunk's raw fp32 x rows and its scales
+  static constexpr int XSLOT = MAXM * CHUNK_K * 4 + CHUNK_PAIRS * PAIR_SCL_BYTES;
+  static constexpr int XRAW_OFF = RING;
   static constexpr int RED = SLICES * C * 8 * (TILE_N + 1) * 4;  // per-slice sums for the gather
-  static constexpr int BAR_OFF = RING > RED ? RING : RED;
+  static constexpr int BAR_OFF = RING + XSTAGES * XSLOT > RED ? RING + XSTAGES * XSLOT : RED;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static constexpr int PREFETCH = 2;  // weight pairs in flight per warp (registers)
 };
@@ -153,12 +158,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// The mbarrier receives one arrival when all earlier cp.async of this thread
-// have landed (counted in the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // Exact three-term bf16 split of two consecutive activations: term 0 is the
 // top 16 bits of x (truncation), term 1 the top 16 bits of the exact
 // remainder, term 2 the rest (at most 8 significant bits, exact in bf16).
@@ -244,7 +243,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   }
   if (tid == 0) {
     for (int b = 0; b < NSLOT; ++b) {
-      mbar_init(smem_u32(&bfull[b]), 2 * CONV_THREADS);  // converter stores + their scale copies
+      mbar_init(smem_u32(&bfull[b]), CONV_THREADS);
       mbar_init(smem_u32(&bempty[b]), COMPUTE_WARPS);
     }
     s_err = 0;
@@ -344,11 +343,42 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
     const float* xr = a.x + bp0 * 64 + 4 * ct;
     const uint8_t* sg = a.scl + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
+    // Stage chunk c: this thread's 16 bytes of every token row (k = 4ct..4ct+3)
+    // and its two 16-byte pieces of the chunk's scales.  Each thread reads back
+    // only what it copied, so completion needs no barrier.
+    auto stage = [&](int c) {
+      if (c < nchunks) {
+        uint8_t* xs = smem + S::XRAW_OFF + (c % XSTAGES) * S::XSLOT;
+        const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
+        const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
+        if (k_ok) {
+#pragma unroll
+          for (int m = 0; m < MAXM; ++m)
+            if (m < mrows)
+              cp_async16(smem_u32(xs + m * (CHUNK_K * 4) + ct * 16),
+                         xr + (int64_t)m * a.K + (int64_t)c * CHUNK_K);
+        }
+        const int scl_bytes = min(CHUNK_PAIRS, npairs - c * CHUNK_PAIRS) * PAIR_SCL_BYTES;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int q = ct + r * CONV_THREADS;
+          if (q * 16 < scl_bytes)
+            cp_async16(smem_u32(xs + MAXM * CHUNK_K * 4 + q * 16),
+                       sg + (int64_t)c * CHUNK_PAIRS * PAIR_SCL_BYTES + q * 16);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    stage(0);
+    stage(1);
     for (int c = 0; c < nchunks; ++c) {
       const int slot = c & (NSLOT - 1);
       uint8_t* sb = smem + slot * S::SLOT;
+      const uint8_t* xs = smem + S::XRAW_OFF + (c % XSTAGES) * S::XSLOT;
       const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
       const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // chunk c staged (c + 1 may be in flight)
+      stage(c + 2);  // refills the slot read in the previous iteration
       if (c >= NSLOT &&
           !mbar_wait_bounded(smem_u32(&bempty[slot]), (uint32_t)(((c / NSLOT) + 1) & 1), &s_err)) {
         s_err = 1;
@@ -359,12 +389,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       for (int r = 0; r < 2; ++r) {
         const int q = ct + r * CONV_THREADS;
         if (q * 16 < scl_bytes)
-          cp_async16(smem_u32(sb + S::SCL_OFF + q * 16),
-                     sg + (int64_t)c * CHUNK_PAIRS * PAIR_SCL_BYTES + q * 16);
+          *reinterpret_cast<uint4*>(sb + S::SCL_OFF + q * 16) =
+              *reinterpret_cast<const uint4*>(xs + MAXM * CHUNK_K * 4 + q * 16);
       }
-      cp_async_arrive(smem_u32(&bfull[slot]));
       if (pair_ok) {
-        constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows loaded together
+        constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows read back together
 #pragma unroll
         for (int m0 = 0; m0 < MAXM; m0 += MG) {
           float4 v[MG];
@@ -372,8 +401,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           for (int mm = 0; mm < MG; ++mm) {
             v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             if (m0 + mm < mrows && k_ok)
-              v[mm] = __ldg(reinterpret_cast<const float4*>(xr + (int64_t)(m0 + mm) * a.K +
-                                                            (int64_t)c * CHUNK_K));
+              v[mm] = *reinterpret_cast<const float4*>(xs + (m0 + mm) * (CHUNK_K * 4) + ct * 16);
           }
 #pragma unroll
           for (int mm = 0; mm < MG; ++mm) {
