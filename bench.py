@@ -33,14 +33,23 @@ sys.path.insert(0, ROOT)
 
 M_SWEEP = (1, 2, 3, 4, 5, 8)
 TYPES = ("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
-DOMINANT = ("gate_proj", "up_proj", "down_proj")
+# calls per layer: the projections that share their input go in one grouped call
+GROUPS = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
+          ("gate_up", ("gate_proj", "up_proj")), ("down", ("down_proj",)))
 METRIC = "Q4 matmul effective weight GB/s and token-rows/s vs M (1-256); % of HBM peak"
 WORKLOAD = "qwen2.5-7b decode linears, Q4_0, 28-layer stack (q,k,v,o,gate,up,down), M sweep 1,2,3,4,5,8"
 BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
 
 # DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
 # hash of the kernel source it was taken on (null once the kernel changes).
-TRAFFIC = {}
+TRAFFIC = {
+    "source_hash": "07d52c2b615d8d08",
+    "grouped": True,
+    "bytes_per_launch": 32935861,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
+    "capture": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
+               "--clock-control none -k regex:mma_kernel -s 96 -c 96 python bench.py --layers 4 "
+               "--steps 2 --warmup 3 --no-cpu-baseline (one step: 4 layers x 4 calls x 6 M)",
+}
 
 
 def _env_int(name, default):
@@ -237,59 +246,68 @@ def run_gpu(args):
         for name in TYPES:
             N, _ = synthetic.QWEN7B_LINEARS[name]
             ys[(M, name)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+    groups = tuple((n, (n,)) for n in TYPES) if args.separate else GROUPS
 
-    def issue(M, name):
-        K = synthetic.QWEN7B_LINEARS[name][1]
+    def issue(M, gname):
+        names = dict(groups)[gname]
+        K = synthetic.QWEN7B_LINEARS[names[0]][1]
         x = xs[(M, K)]
-        y = ys[(M, name)]
-        for W in stack[name]:
-            q4.q4mm_forward(W, x, y=y, stream=stream)
+        for layer in range(layers):
+            if len(names) == 1:
+                q4.q4mm_forward(stack[names[0]][layer], x, y=ys[(M, names[0])], stream=stream)
+            else:
+                q4.q4mm_forward_group([stack[n][layer] for n in names], x,
+                                      ys=[ys[(M, n)] for n in names], stream=stream)
 
     # warm the library (scratch allocation) before capture
     with torch.cuda.stream(stream):
         for M in M_SWEEP:
-            for name in TYPES:
-                issue(M, name)
+            for gname, _ in groups:
+                issue(M, gname)
     torch.cuda.synchronize(dev)
 
     graphs = {}
     for M in M_SWEEP:
-        for name in TYPES:
+        for gname, _ in groups:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                issue(M, name)
-            graphs[(M, name)] = g
+                issue(M, gname)
+            graphs[(M, gname)] = g
     torch.cuda.synchronize(dev)
 
-    plan = {}
+    launches = {}
     launches_per_step = 0
     for M in M_SWEEP:
-        for name in TYPES:
-            p, l, s = q4.q4mm_plan_info(stack[name][0], M)
-            plan[(M, name)] = {"path": p, "launches": l, "splits": s}
+        for gname, names in groups:
+            p, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M)
+            if len(names) > 1 and p != q4.Q4MM_PATH_MMA:
+                l *= len(names)  # above the threshold a group runs one call per weight
+            launches[(M, gname)] = l
             launches_per_step += l * layers
 
     wbytes = {name: synthetic.QWEN7B_LINEARS[name][0] * synthetic.QWEN7B_LINEARS[name][1]
               * BLOCK_BYTES_PER_WEIGHT for name in TYPES}
     step_wbytes = sum(wbytes[n] * layers for n in TYPES) * len(M_SWEEP)
 
-    def algo_bytes(M, name):
-        N, K = synthetic.QWEN7B_LINEARS[name]
-        return wbytes[name] + 4.0 * M * K + 4.0 * M * N
+    def algo_bytes(M, gname):
+        """Bytes a call must move: packed weights once, x once, y once."""
+        names = dict(groups)[gname]
+        K = synthetic.QWEN7B_LINEARS[names[0]][1]
+        return sum(wbytes[n] + 4.0 * M * synthetic.QWEN7B_LINEARS[n][0] for n in names) + 4.0 * M * K
 
     ev = {}
 
     def step(record):
         for M in M_SWEEP:
-            for name in TYPES:
+            for gname, _ in groups:
                 if record:
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    graphs[(M, name)].replay()
+                    graphs[(M, gname)].replay()
                     b.record(stream)
-                    ev.setdefault((M, name), []).append((a, b))
+                    ev.setdefault((M, gname), []).append((a, b))
                 else:
-                    graphs[(M, name)].replay()
+                    graphs[(M, gname)].replay()
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -319,30 +337,31 @@ def run_gpu(args):
     ms_per_step = ms / args.steps
     value = step_wbytes * world / (ms_per_step * 1e-3) / 1e9
 
-    # per-(M, type) kernel durations over the timed region
+    # per-(M, call) durations over the timed region: each graph replay is the
+    # `layers` calls of one kind, bracketed by events on the launching stream
     per = {}
     for key, pairs in ev.items():
-        per[key] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) / layers  # ms per launch
+        per[key] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) / layers  # ms per call
     peak, peak_kind = _peaks()
-    dom_bytes = sum(algo_bytes(M, n) for M in M_SWEEP for n in DOMINANT)
-    dom_ms = sum(per[(M, n)] for M in M_SWEEP for n in DOMINANT)
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    # roofline over every launch of the step (one kernel function serves them all):
+    # algorithmic bytes per call / event-timed duration per call
+    tot_bytes = sum(algo_bytes(M, g) for M in M_SWEEP for g, _ in groups)
+    tot_ms = sum(per[(M, g)] for M in M_SWEEP for g, _ in groups)
+    n_launch = sum(launches[(M, g)] for M in M_SWEEP for g, _ in groups)
+    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     traffic = None
-    if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash():
+    if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash() and \
+            TRAFFIC.get("grouped") == (not args.separate):
         traffic = TRAFFIC.get("bytes_per_launch")
     per_m = {}
     for M in M_SWEEP:
-        t = sum(per[(M, n)] * layers for n in TYPES)
+        t = sum(per[(M, g)] * layers for g, _ in groups)
         b = sum(wbytes[n] * layers for n in TYPES)
         per_m[str(M)] = {
             "weight_gbs": b / (t * 1e-3) / 1e9,
             "token_rows_per_s": M / (t * 1e-3),
             "frac_of_measured_hbm": b / (t * 1e-3) / 1e9 / peak,
-            "paths": sorted({plan[(M, n)]["path"] for n in TYPES}),
-            "gate_us": per[(M, "gate_proj")] * 1e3,
-            "down_us": per[(M, "down_proj")] * 1e3,
-            "q_us": per[(M, "q_proj")] * 1e3,
-            "k_us": per[(M, "k_proj")] * 1e3,
+            "call_us": {g: per[(M, g)] * 1e3 for g, _ in groups},
         }
 
     # ---- end to end through the public API: pinned host x in, host y out ----
@@ -355,8 +374,8 @@ def run_gpu(args):
         for M in M_SWEEP:
             xs[(M, 3584)].copy_(pin_x[(M, 3584)], non_blocking=True)
             xs[(M, 18944)].copy_(pin_x[(M, 18944)], non_blocking=True)
-            for name in TYPES:
-                graphs[(M, name)].replay()
+            for gname, _ in groups:
+                graphs[(M, gname)].replay()
             out_host[M].copy_(ys[(M, "down_proj")], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -392,6 +411,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (%.2f GB packed weight stack, streamed once per M)"
                              % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU",
+                       "calls_per_layer": [g for g, _ in groups],
                        "m_threshold": q4.q4mm_get_m_threshold()},
             "token_rows_per_s": sum(M_SWEEP) * world / (ms_per_step * 1e-3),
             "per_M": per_m,
@@ -399,8 +419,9 @@ def run_gpu(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "kernel": "q4mm gate/up/down launches (all M of the sweep)",
-                         "algorithmic_bytes_per_launch": "0.5625*N*K + 4*M*K + 4*M*N"},
+                         "kernel": "mma_kernel, every launch of one step (%d launches)" % (n_launch * layers),
+                         "algorithmic_bytes_per_launch": tot_bytes / n_launch,
+                         "algorithmic_bytes_rule": "0.5625*sum(N_i*K) + 4*M*K + 4*M*sum(N_i) per call"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
@@ -487,6 +508,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="one call per linear instead of grouping q/k/v and gate/up")
     ap.add_argument("--path-sweep", action="store_true",
                     help="time both kernel paths per M and print the measured M threshold")
     args = ap.parse_args()

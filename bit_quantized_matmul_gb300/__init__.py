@@ -32,6 +32,7 @@ Q4MM_FORCE_TC = 0x4
 Q4MM_ROW_BY_ROW = 0x8
 Q4MM_FORCE_MMA = 0x10
 Q4MM_M_MAX = 4096
+Q4MM_GROUP_MAX = 4
 Q4MM_NOALLOC_PARTIAL_BYTES = 614400
 Q4MM_PATH_SIMT = 1
 Q4MM_PATH_TC = 2
@@ -45,7 +46,7 @@ BLOCK_BYTES = 18
 EXPORTS = (
     "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
-    "q4mm_forward_noalloc", "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
+    "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
     "q4_status_string",
 )
 
@@ -69,6 +70,7 @@ _sig = {
     "q4mm_argmax": [_p, _p, _p, _p, _i64, _p],
     "q4mm_argmax_ex": [_p, _p, _p, _p, _i64, _u32, _p],
     "q4mm_forward_noalloc": [_p, _p, _p, _i64, _p],
+    "q4mm_forward_group": [_p, ctypes.c_int, _p, _p, _i64, _u32, _p],
     "q4mm_select_path": [_p, _i64, _u32],
     "q4mm_plan_info": [_p, _i64, _u32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                        ctypes.POINTER(ctypes.c_int)],
@@ -244,6 +246,30 @@ def q4mm_forward_noalloc(W: Q4Weight, x: torch.Tensor, y: torch.Tensor, stream=N
         _check(_lib.q4mm_forward_noalloc(W.handle, x.data_ptr(), y.data_ptr(), M, _stream(stream)),
                "q4mm_forward_noalloc")
     return y
+
+
+def q4mm_forward_group(Ws, x: torch.Tensor, ys=None, flags: int = 0, stream=None):
+    """[x @ W_i^T for W_i in Ws] in one launch per 8 token rows (weights sharing K)."""
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if not 1 <= len(Ws) <= Q4MM_GROUP_MAX:
+        raise ValueError("1 to %d weights" % Q4MM_GROUP_MAX)
+    if x.dim() != 2 or any(W.K != x.shape[1] for W in Ws):
+        raise ValueError("x must be [M, K] with the K of every weight")
+    if ys is None:
+        ys = [torch.empty((M, W.N), dtype=torch.float32, device=x.device) for W in Ws]
+    if len(ys) != len(Ws):
+        raise ValueError("one output per weight")
+    for W, y in zip(Ws, ys):
+        _dev_f32(y, "y")
+        if tuple(y.shape) != (M, W.N):
+            raise ValueError("y must be [M, %d]" % W.N)
+    hw = (ctypes.c_void_p * len(Ws))(*[W.handle for W in Ws])
+    hy = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_forward_group(hw, len(Ws), x.data_ptr(), hy, M, int(flags), _stream(stream)),
+               "q4mm_forward_group")
+    return ys
 
 
 def q4mm_argmax_ex(W: Q4Weight, x: torch.Tensor, flags: int = 0, want_max: bool = True, stream=None):

@@ -356,6 +356,53 @@ int q4mm_forward_ex(const q4_weight* W, const float* x, float* y, int64_t M, uin
   return run(W, x, y, nullptr, nullptr, M, flags, stream);
 }
 
+int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
+                       int64_t M, uint32_t flags, cudaStream_t stream) {
+  if (!W || !x || !y || count < 1 || count > Q4MM_GROUP_MAX) return Q4_ERR_INVALID_ARG;
+  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA)) return Q4_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    if (!W[i] || !y[i]) return Q4_ERR_INVALID_ARG;
+    if (W[i]->w.K != W[0]->w.K || W[i]->w.device != W[0]->w.device) return Q4_ERR_INVALID_ARG;
+  }
+  if (M < 0) return Q4_ERR_INVALID_ARG;
+  if (M > Q4MM_M_MAX) return Q4_ERR_SHAPE;
+  if (M == 0) return Q4_OK;
+  if (!aligned16(x)) return Q4_ERR_ALIGN;
+  for (int i = 0; i < count; ++i)
+    if (!aligned16(y[i])) return Q4_ERR_ALIGN;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (dev != W[0]->w.device) return Q4_ERR_INVALID_ARG;
+  {
+    DeviceScratch& ds = g_dev[dev];
+    std::lock_guard<std::mutex> lock(ds.mu);
+    st = init_device_locked(dev, ds);
+    if (st) return st;
+    const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
+    if (choose_path(ds, M, flags) == Q4MM_PATH_MMA) {
+      MmaLaunch L;
+      L.count = count;
+      int64_t tiles = 0;
+      for (int i = 0; i < count; ++i) {
+        L.W[i] = &W[i]->w;
+        L.y[i] = y[i];
+        tiles += W[i]->w.tiles;
+      }
+      const MmaPlan plan = mma_plan_tiles(tiles, W[0]->w.KBP, ds.num_sms);
+      Workspace ws;
+      st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws);
+      if (st) return st;
+      return launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
+    }
+  }
+  for (int i = 0; i < count; ++i) {  // tensor-core path: one call per weight
+    st = run(W[i], x, y[i], nullptr, nullptr, M, flags, stream);
+    if (st) return st;
+  }
+  return Q4_OK;
+}
+
 int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                 cudaStream_t stream) {
   if (!idx) return Q4_ERR_INVALID_ARG;

@@ -91,12 +91,24 @@ struct MmaPlan {
   int64_t kbp_per_split;  // block pairs per split
 };
 
-// mma.sync streaming kernel (small and medium M).
+// mma.sync streaming kernel (small and medium M).  One launch may cover up to
+// MMA_GROUP_MAX weights that share K and the activations; the K partition is
+// planned from their total tile count.
+constexpr int MMA_GROUP_MAX = Q4MM_GROUP_MAX;
+struct MmaLaunch {
+  int count = 0;
+  const Weight* W[MMA_GROUP_MAX] = {};
+  float* y[MMA_GROUP_MAX] = {};
+};
 MmaPlan mma_plan(const Weight* W, int num_sms);
+MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms);
 size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant);
+size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant);
 int mma_launch_count(int64_t M, bool batch_invariant);
 int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
                const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
+int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
+                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
 
 // CUDA-core streaming kernel.
 MmaPlan simt_plan(const Weight* W, int num_sms);

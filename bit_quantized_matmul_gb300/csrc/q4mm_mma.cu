@@ -53,9 +53,20 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 constexpr int NSLOT = 4;                    // ring depth (a power of two)
 constexpr int XSTAGES = 3;                  // converter staging slots (chunks in flight)
 
-struct MmaArgs {
+// One weight of a launch.  A launch covers the tiles of up to MMA_GROUP_MAX
+// weights that share K and the activations (e.g. the q, k and v projections):
+// global tile t belongs to the last weight whose tile_start <= t.
+struct MmaWeight {
   const uint4* nib;     // fragment layout, 16 bytes per (tile, pair, rg, lane)
   const uint8_t* scl;   // scale plane, 512 bytes per (tile, pair)
+  float* y;             // [mrows, N] rows of this launch, or null (greedy pick)
+  int64_t N;
+  int tile_start;       // first global tile
+};
+
+struct MmaArgs {
+  MmaWeight w[MMA_GROUP_MAX];
+  int nweights;
   const float* x;       // [mrows, K] activations of this launch
   int64_t K, KBP;       // K, block pairs
   int mrows;            // token rows in this launch
@@ -195,7 +206,13 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t tile = blockIdx.x;
+  int wi = 0;
+#pragma unroll
+  for (int i = 1; i < MMA_GROUP_MAX; ++i)
+    if (i < a.nweights && (int)blockIdx.x >= a.w[i].tile_start) wi = i;
+  const int64_t tile = (int64_t)blockIdx.x - a.w[wi].tile_start;  // tile within its weight
+  const uint4* nib_w = a.w[wi].nib;
+  const uint8_t* scl_w = a.w[wi].scl;
   const int split = blockIdx.y;
   const int64_t bp0 = (int64_t)split * a.kbp_per_split;
   const int64_t bp1 = min(a.KBP, bp0 + a.kbp_per_split);
@@ -210,7 +227,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // depend on an earlier kernel)
   const int rgp = warp & 3, sl = (warp >> 2) & 3;
   const int n_i = (compute && npairs > sl) ? (npairs - sl + SLICES - 1) / SLICES : 0;
-  const uint4* wp = a.nib + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
+  const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
   constexpr int64_t WSTEP = SLICES * 8 * 32;  // uint4 between a slice's consecutive pairs
   uint4 wb[PREFETCH][2];
 #pragma unroll
@@ -342,7 +359,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     const int oa = ((tql) ^ h) * 16, ob = ((tql + 1) ^ h) * 16;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
     const float* xr = a.x + bp0 * 64 + 4 * ct;
-    const uint8_t* sg = a.scl + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
+    const uint8_t* sg = scl_w + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
     // Stage chunk c: this thread's 16 bytes of every token row (k = 4ct..4ct+3)
     // and its two 16-byte pieces of the chunk's scales.  Each thread reads back
     // only what it copied, so completion needs no barrier.
@@ -469,27 +486,47 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       }
     }
   }
-  finish_tile<MAXM>(a.e, val, row, tile, 0, mrows, split, (int)tile, &s_flag, kred,
+  // this weight's outputs; partial sums and counters indexed by the global tile
+  EpiArgs e = a.e;
+  e.y = a.w[wi].y;
+  e.N = a.w[wi].N;
+  e.partial = a.e.partial + (int64_t)a.w[wi].tile_start * TILE_N;
+  finish_tile<MAXM>(e, val, row, tile, 0, mrows, split, (int)blockIdx.x, &s_flag, kred,
                     []() { __syncthreads(); });
 }
 
 template <int C, bool DENSE>
-int launch_c(const Weight* W, const float* x, int mrows, float* y, int32_t* idx, float* maxval,
+int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
   using S = MmaCfg<C>;
+  const Weight* W0 = L.W[0];
   MmaArgs a;
-  a.nib = reinterpret_cast<const uint4*>(W->nib);
-  a.scl = reinterpret_cast<const uint8_t*>(W->d);
+  int tiles = 0;
+  for (int i = 0; i < MMA_GROUP_MAX; ++i) {
+    if (i < L.count) {
+      const Weight* W = L.W[i];
+      a.w[i].nib = reinterpret_cast<const uint4*>(W->nib);
+      a.w[i].scl = reinterpret_cast<const uint8_t*>(W->d);
+      a.w[i].y = L.y[i] ? L.y[i] + mb * W->N : nullptr;
+      a.w[i].N = W->N;
+      a.w[i].tile_start = tiles;
+      tiles += (int)W->tiles;
+    } else {
+      a.w[i] = a.w[0];
+      a.w[i].tile_start = 1 << 30;
+    }
+  }
+  a.nweights = L.count;
   a.x = x;
-  a.K = W->K;
-  a.KBP = W->KBP;
+  a.K = W0->K;
+  a.KBP = W0->KBP;
   a.mrows = mrows;
   a.kbp_per_split = plan.kbp_per_split;
   a.status = ws.status;
-  a.e.N = W->N;
-  a.e.N_pad = W->N_pad;
+  a.e.N = W0->N;
+  a.e.N_pad = (int64_t)tiles * TILE_N;
   a.e.M = mrows;
-  a.e.y = y ? y + mb * W->N : nullptr;
+  a.e.y = nullptr;
   a.e.idx = idx ? idx + mb : nullptr;
   a.e.maxval = (idx && maxval) ? maxval + mb : nullptr;
   a.e.splits = plan.splits;
@@ -497,16 +534,16 @@ int launch_c(const Weight* W, const float* x, int mrows, float* y, int32_t* idx,
   a.e.counters = ws.counters;
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
-  a.e.tiles = (int)W->tiles;
+  a.e.tiles = tiles;
   static bool attr_set[64] = {};
-  if (!attr_set[W->device & 63]) {
+  if (!attr_set[W0->device & 63]) {
     if (cudaFuncSetAttribute(mma_kernel<C, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
-    attr_set[W->device & 63] = true;
+    attr_set[W0->device & 63] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)W->tiles, (unsigned)plan.splits, 1);
+  cfg.gridDim = dim3((unsigned)tiles, (unsigned)plan.splits, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
@@ -524,26 +561,32 @@ int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (M
 
 }  // namespace
 
-MmaPlan mma_plan(const Weight* W, int num_sms) {
-  // K partition from N and K only (never from M).  One CTA per SM: splits =
+MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms) {
+  // K partition from the shapes only (never from M).  One CTA per SM: splits =
   // floor(SMs / tiles) for a single wave, at least one, and small enough that
   // each CTA keeps at least two block pairs.
   MmaPlan p;
-  int64_t sp = (int64_t)num_sms / W->tiles;
-  int64_t cap = W->KBP / 2;
+  int64_t sp = (int64_t)num_sms / tiles;
+  int64_t cap = KBP / 2;
   if (cap < 1) cap = 1;
   if (sp < 1) sp = 1;
   if (sp > cap) sp = cap;
-  p.kbp_per_split = (W->KBP + sp - 1) / sp;
-  p.splits = (int)((W->KBP + p.kbp_per_split - 1) / p.kbp_per_split);
+  p.kbp_per_split = (KBP + sp - 1) / sp;
+  p.splits = (int)((KBP + p.kbp_per_split - 1) / p.kbp_per_split);
   return p;
 }
 
-size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant) {
+MmaPlan mma_plan(const Weight* W, int num_sms) { return mma_plan_tiles(W->tiles, W->KBP, num_sms); }
+
+size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant) {
   if (p.splits <= 1) return 0;
   const int64_t rpl = rows_per_launch(batch_invariant);
   const int64_t ml = M < rpl ? M : rpl;
-  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(float);
+  return (size_t)p.splits * (size_t)ml * (size_t)(tiles * TILE_N) * sizeof(float);
+}
+
+size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant) {
+  return mma_partial_bytes_tiles(W->tiles, p, M, batch_invariant);
 }
 
 int mma_launch_count(int64_t M, bool batch_invariant) {
@@ -551,30 +594,42 @@ int mma_launch_count(int64_t M, bool batch_invariant) {
   return (int)((M + rpl - 1) / rpl);
 }
 
-int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
-               const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s) {
+int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
+                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s) {
+  int64_t tiles = 0;
+  for (int i = 0; i < L.count; ++i) tiles += L.W[i]->tiles;
+  if (plan.splits > 1 && tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
+  const int64_t K = L.W[0]->K;
   const int64_t rpl = rows_per_launch(batch_invariant);
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
-    if (plan.splits > 1 && W->tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
-    const float* xs = x + mb * W->K;
+    const float* xs = x + mb * K;
     int st;
     if (batch_invariant) {
       switch (mrows) {
-        case 1: st = launch_c<1, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
-        case 2: st = launch_c<2, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
-        default: st = launch_c<3, false>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        case 1: st = launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        case 2: st = launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        default: st = launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
       }
     } else {
       switch ((3 * mrows + 7) / 8) {  // column groups of this launch
-        case 1: st = launch_c<1, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
-        case 2: st = launch_c<2, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
-        default: st = launch_c<3, true>(W, xs, mrows, y, idx, maxval, plan, ws, mb, s); break;
+        case 1: st = launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        case 2: st = launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        default: st = launch_c<3, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
       }
     }
     if (st) return st;
   }
   return Q4_OK;
+}
+
+int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
+               const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s) {
+  MmaLaunch L;
+  L.count = 1;
+  L.W[0] = W;
+  L.y[0] = y;
+  return launch_mma_group(L, x, M, idx, maxval, plan, batch_invariant, ws, s);
 }
 
 }  // namespace q4

@@ -153,6 +153,29 @@ Q4_API int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* 
 Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                    uint32_t flags, cudaStream_t stream);
 
+/* Most weights one q4mm_forward_group call takes. */
+#define Q4MM_GROUP_MAX 4
+
+/* y_i = x @ W_i^T for up to Q4MM_GROUP_MAX weights that share K and the same
+ * activations (the q, k and v projections, or the gate and up projections, of
+ * one decoder layer), in one kernel launch per 8 token rows instead of one per
+ * weight: the activations are staged once and the fixed cost of a launch is
+ * paid once ("Why LLM Decoding Is Slow, and Why Batching Is (Almost) Free",
+ * §4: every weight is still read exactly once per call).
+ *   W       host array of `count` handles, all with the same K, on the current
+ *           device; 1 <= count <= Q4MM_GROUP_MAX.
+ *   x       device, fp32 [M, K] row-major, 16-byte aligned.
+ *   y       host array of `count` device pointers, y[i] fp32 [M, N_i],
+ *           16-byte aligned, fully overwritten; distinct, non-overlapping.
+ *   flags   0, Q4MM_FORCE_MMA or Q4MM_BATCH_INVARIANT (others: INVALID_ARG).
+ * Each y_i is within the q4mm_forward tolerance.  The K partition depends on
+ * the group's shapes (not on M), so in batch-invariant mode row r of every y_i
+ * is bit-identical whatever M is; it may differ in the last bits from a
+ * single-weight call of the same W_i.  At or above the M threshold (without
+ * flags) the call runs the tensor-core kernel once per weight instead. */
+Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
+                              int64_t M, uint32_t flags, cudaStream_t stream);
+
 /* Capacity of the split-K partial sums of q4mm_forward_noalloc (600 KiB). */
 #define Q4MM_NOALLOC_PARTIAL_BYTES 614400
 

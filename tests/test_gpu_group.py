@@ -1,0 +1,106 @@
+"""GPU checks of q4mm_forward_group: several weights that share K and the
+activations (a decoder layer's q/k/v or gate/up projections) in one launch.
+Each output is compared element by element with the oracle's bound."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import acts, assert_within_bound, weights
+
+pytestmark = pytest.mark.gpu
+
+q4 = pytest.importorskip("bit_quantized_matmul_gb300")
+
+
+def _group(shapes, config):
+    ws = [weights(config, i, N, K) for i, (N, K) in enumerate(shapes)]
+    Ws = [q4.q4_quantize(torch.from_numpy(w).cuda()) for w in ws]
+    blocks = [oracle.quantize(w) for w in ws]
+    return Ws, blocks
+
+
+@pytest.mark.parametrize("shapes,Ms", [
+    ([(3584, 3584), (512, 3584), (512, 3584)], (1, 5, 8, 13)),   # q, k, v
+    ([(300, 1024), (130, 1024)], (1, 3, 17)),                     # ragged tiles
+    ([(18944, 3584), (18944, 3584)], (2,)),                       # gate, up
+])
+def test_group_matches_oracle(shapes, Ms):
+    Ws, blocks = _group(shapes, 95)
+    K = shapes[0][1]
+    for M in Ms:
+        x_np = acts(95, M, K)
+        ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x_np).cuda())
+        torch.cuda.synchronize()
+        assert q4.q4_device_status() == q4.Q4_OK
+        for i, (y, b) in enumerate(zip(ys, blocks)):
+            _, y64, bound = oracle.matmul(b, x_np)
+            assert_within_bound(y.cpu().numpy(), y64, bound, "group weight %d M=%d" % (i, M))
+    for W in Ws:
+        W.free()
+
+
+def test_group_of_one_equals_single_call():
+    Ws, _ = _group([(896, 896)], 96)
+    x = torch.from_numpy(acts(96, 6, 896)).cuda()
+    (yg,) = q4.q4mm_forward_group(Ws, x, flags=q4.Q4MM_FORCE_MMA)
+    ys = q4.q4mm_forward_ex(Ws[0], x, q4.Q4MM_FORCE_MMA)
+    assert torch.equal(yg.view(torch.int32), ys.view(torch.int32))
+    Ws[0].free()
+
+
+def test_group_batch_invariant_rows():
+    Ws, _ = _group([(3584, 3584), (512, 3584), (512, 3584)], 97)
+    inv = q4.Q4MM_BATCH_INVARIANT
+    big = torch.from_numpy(acts(97, 7, 3584)).cuda()
+    y7 = q4.q4mm_forward_group(Ws, big, flags=inv)
+    for r in (0, 3, 6):
+        y1 = q4.q4mm_forward_group(Ws, big[r:r + 1].contiguous(), flags=inv)
+        for a, b in zip(y7, y1):
+            assert torch.equal(a[r].view(torch.int32), b[0].view(torch.int32)), r
+    for W in Ws:
+        W.free()
+
+
+def test_group_above_threshold_uses_per_weight_calls():
+    Ws, blocks = _group([(300, 1024), (256, 1024)], 98)
+    M = q4.q4mm_get_m_threshold() + 3
+    x_np = acts(98, M, 1024)
+    ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x_np).cuda())
+    for y, b in zip(ys, blocks):
+        _, y64, bound = oracle.matmul(b, x_np)
+        assert_within_bound(y.cpu().numpy(), y64, bound, "group M=%d" % M)
+    for W in Ws:
+        W.free()
+
+
+def test_group_argument_errors():
+    Ws, _ = _group([(300, 1024), (256, 1024)], 99)
+    other = q4.q4_quantize(torch.from_numpy(weights(99, 7, 128, 512)).cuda())
+    lib = q4.raw_library()
+    x = torch.zeros((4, 1024), device="cuda")
+    ys = [torch.zeros((4, W.N), device="cuda") for W in Ws]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call(handles, outs, M=4, flags=0, xp=None):
+        hw = (ctypes.c_void_p * max(1, len(handles)))(*handles)
+        hy = (ctypes.c_void_p * max(1, len(outs)))(*outs)
+        return lib.q4mm_forward_group(hw, len(handles), ctypes.c_void_p(xp or x.data_ptr()), hy, M,
+                                      flags, stream)
+
+    hs = [W.handle for W in Ws]
+    ps = [y.data_ptr() for y in ys]
+    assert call(hs, ps) == q4.Q4_OK
+    assert call([], []) == q4.Q4_ERR_INVALID_ARG
+    assert call(hs * 3, ps * 3) == q4.Q4_ERR_INVALID_ARG                    # 6 > Q4MM_GROUP_MAX
+    assert call([hs[0], other.handle], ps) == q4.Q4_ERR_INVALID_ARG         # K differs
+    assert call(hs, [ps[0], None]) == q4.Q4_ERR_INVALID_ARG                 # null output
+    assert call(hs, [ps[0], ps[1] + 4]) == q4.Q4_ERR_ALIGN
+    assert call(hs, ps, flags=q4.Q4MM_FORCE_SIMT) == q4.Q4_ERR_INVALID_ARG
+    assert call(hs, ps, M=q4.Q4MM_M_MAX + 1) == q4.Q4_ERR_SHAPE
+    assert call(hs, ps, M=0) == q4.Q4_OK
+    torch.cuda.synchronize()
+    for W in Ws + [other]:
+        W.free()
