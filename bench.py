@@ -43,9 +43,9 @@ BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
 # DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
 # hash of the kernel source it was taken on (null once the kernel changes).
 TRAFFIC = {
-    "source_hash": "07d52c2b615d8d08",
+    "source_hash": "938737a0525490c3",
     "grouped": True,
-    "bytes_per_launch": 32935861,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
+    "bytes_per_launch": 32937611,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
     "capture": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                "--clock-control none -k regex:mma_kernel -s 96 -c 96 python bench.py --layers 4 "
                "--steps 2 --warmup 3 --no-cpu-baseline (one step: 4 layers x 4 calls x 6 M)",
@@ -483,13 +483,17 @@ def run_path_sweep(args):
                 out.setdefault(name, {}).setdefault(str(M), {})[pname] = {
                     "us": us, "weight_gbs": wb / us / 1e3, "rows_per_s": M / us * 1e6}
                 del g
-    # threshold: smallest M from which the tcgen05 path is at least as fast as
-    # the streaming mma.sync path on the large shapes (gate, down) for every
-    # larger M of the sweep
+    # threshold: smallest M of the sweep from which one decoder layer (q, o like
+    # q_proj; k, v like k_proj; gate, up like gate_proj; down) takes no longer
+    # on the tcgen05 path than on the streaming path, for every larger M too
+    weight = {"q_proj": 2, "k_proj": 2, "gate_proj": 2, "down_proj": 1}
+
+    def layer_us(M, path):
+        return sum(c * out[n][str(M)][path]["us"] for n, c in weight.items())
+
     thr = None
     for i, M in enumerate(sweep):
-        if all(out[n][str(m)]["tc"]["us"] <= out[n][str(m)]["mma"]["us"]
-               for n in ("gate_proj", "down_proj") for m in sweep[i:]):
+        if all(layer_us(m, "tc") <= layer_us(m, "mma") for m in sweep[i:]):
             thr = M
             break
     print(json.dumps({"path_sweep": out, "measured_threshold": thr, "layers": layers,
