@@ -66,8 +66,8 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MAXM]
 #pragma unroll
       for (int m = 0; m < MAXM; ++m)
         if (m < mcount) e.partial[((int64_t)split * e.M + m0 + m) * e.N_pad + n] = val[m];
+      __threadfence();  // the writers' partial sums are visible before the count
     }
-    __threadfence();
     sync();
     if (row == 0) {
       const unsigned prev = atomicAdd(&e.counters[counter_slot], 1u);
@@ -75,11 +75,11 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MAXM]
     }
     sync();
     if (!*s_flag) return;
-    __threadfence();
     if (row >= 0) {
+      __threadfence();
       // ascending split order per output; the loads of a batch of splits for
       // every token row are issued before any of them is added
-      constexpr int SB = 4;
+      constexpr int SB = MAXM <= 2 ? 8 : (MAXM <= 5 ? 4 : 2);  // splits loaded per batch
       const int64_t sstride = e.M * e.N_pad;
       const float* pp = e.partial + (m0 * e.N_pad + n);
 #pragma unroll

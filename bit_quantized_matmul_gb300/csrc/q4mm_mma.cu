@@ -117,6 +117,27 @@ __device__ __forceinline__ void mma_bf16_acc(float (&d)[4], const uint32_t (&a)[
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Two fp32 accumulators in one 64-bit register pair: acc += s * (c0, c1), one
+// packed instruction, each half an ordinary fp32 fma.  `ss` holds {s, s}.
+__device__ __forceinline__ unsigned long long dup2(float s) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
+}
+__device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long long ss, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 rc;\n\t"
+      "mov.b64 rc, {%2, %3};\n\t"
+      "fma.rn.f32x2 %0, %1, rc, %0;\n\t}"
+      : "+l"(acc)
+      : "l"(ss), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ float2 split2(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
 __device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -268,13 +289,20 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   }
   __syncthreads();
 
-  float acc[2][C][4];
+  // accumulators: [rg][cg][row R0 / R1] as {column 2tq, column 2tq + 1} pairs
+  // (packed fp32x2 updates) up to two column groups; as four floats [rg][cg][e]
+  // for three, where the extra registers of the packed form would spill
+  constexpr bool PACKED = C <= 2;
+  unsigned long long acc[2][C][2];
+  float accf[2][C][4];
 #pragma unroll
   for (int r = 0; r < 2; ++r)
 #pragma unroll
-    for (int cg = 0; cg < C; ++cg)
+    for (int cg = 0; cg < C; ++cg) {
+      acc[r][cg][0] = acc[r][cg][1] = 0ull;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[r][cg][e] = 0.0f;
+      for (int e = 0; e < 4; ++e) accf[r][cg][e] = 0.0f;
+    }
 
   if (compute) {
     const int g = lane >> 2;
@@ -318,10 +346,17 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           }
           const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
           const __half2* q1 = reinterpret_cast<const __half2*>(&sv1);
-          const float s00 = h ? __high2float(q0[0]) : __low2float(q0[0]);
-          const float s01 = h ? __high2float(q0[1]) : __low2float(q0[1]);
-          const float s10 = h ? __high2float(q1[0]) : __low2float(q1[0]);
-          const float s11 = h ? __high2float(q1[1]) : __low2float(q1[1]);
+          const float f00 = h ? __high2float(q0[0]) : __low2float(q0[0]);
+          const float f01 = h ? __high2float(q0[1]) : __low2float(q0[1]);
+          const float f10 = h ? __high2float(q1[0]) : __low2float(q1[0]);
+          const float f11 = h ? __high2float(q1[1]) : __low2float(q1[1]);
+          unsigned long long s00 = 0, s01 = 0, s10 = 0, s11 = 0;
+          if constexpr (PACKED) {
+            s00 = dup2(f00);
+            s01 = dup2(f01);
+            s10 = dup2(f10);
+            s11 = dup2(f11);
+          }
           const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
 #pragma unroll
           for (int cg = 0; cg < C; ++cg) {
@@ -329,17 +364,27 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             float d[4];
             mma_bf16_first(d, a00, bf.x, bf.y);
             mma_bf16_acc(d, a01, bf.z, bf.w);
-            acc[0][cg][0] = fmaf(s00, d[0], acc[0][cg][0]);
-            acc[0][cg][1] = fmaf(s00, d[1], acc[0][cg][1]);
-            acc[0][cg][2] = fmaf(s01, d[2], acc[0][cg][2]);
-            acc[0][cg][3] = fmaf(s01, d[3], acc[0][cg][3]);
+            if constexpr (PACKED) {
+              ffma2(acc[0][cg][0], s00, d[0], d[1]);
+              ffma2(acc[0][cg][1], s01, d[2], d[3]);
+            } else {
+              accf[0][cg][0] = fmaf(f00, d[0], accf[0][cg][0]);
+              accf[0][cg][1] = fmaf(f00, d[1], accf[0][cg][1]);
+              accf[0][cg][2] = fmaf(f01, d[2], accf[0][cg][2]);
+              accf[0][cg][3] = fmaf(f01, d[3], accf[0][cg][3]);
+            }
             float e[4];
             mma_bf16_first(e, a10, bf.x, bf.y);
             mma_bf16_acc(e, a11, bf.z, bf.w);
-            acc[1][cg][0] = fmaf(s10, e[0], acc[1][cg][0]);
-            acc[1][cg][1] = fmaf(s10, e[1], acc[1][cg][1]);
-            acc[1][cg][2] = fmaf(s11, e[2], acc[1][cg][2]);
-            acc[1][cg][3] = fmaf(s11, e[3], acc[1][cg][3]);
+            if constexpr (PACKED) {
+              ffma2(acc[1][cg][0], s10, e[0], e[1]);
+              ffma2(acc[1][cg][1], s11, e[2], e[3]);
+            } else {
+              accf[1][cg][0] = fmaf(f10, e[0], accf[1][cg][0]);
+              accf[1][cg][1] = fmaf(f10, e[1], accf[1][cg][1]);
+              accf[1][cg][2] = fmaf(f11, e[2], accf[1][cg][2]);
+              accf[1][cg][3] = fmaf(f11, e[3], accf[1][cg][3]);
+            }
           }
         }
         if ((i & 1) && c + NSLOT < nchunks) {  // this warp is done with the slot
@@ -462,9 +507,17 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #pragma unroll
       for (int cg = 0; cg < C; ++cg)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < 4; ++e) {
+          float v;
+          if constexpr (PACKED) {
+            const float2 pr = split2(acc[r][cg][e >> 1]);
+            v = (e & 1) ? pr.y : pr.x;
+          } else {
+            v = accf[r][cg][e];
+          }
           red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * (TILE_N + 1) + (2 * rgp + r) * 16 + g +
-              8 * (e >> 1)] = acc[r][cg][e];
+              8 * (e >> 1)] = v;
+        }
   }
   __syncthreads();
 
