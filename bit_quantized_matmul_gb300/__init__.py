@@ -46,7 +46,8 @@ BLOCK_BYTES = 18
 EXPORTS = (
     "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
-    "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
+    "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_argmax_rows", "q4_verify_greedy",
+    "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
     "q4_status_string",
 )
 
@@ -71,6 +72,8 @@ _sig = {
     "q4mm_argmax_ex": [_p, _p, _p, _p, _i64, _u32, _p],
     "q4mm_forward_noalloc": [_p, _p, _p, _i64, _p],
     "q4mm_forward_group": [_p, ctypes.c_int, _p, _p, _i64, _u32, _p],
+    "q4mm_argmax_rows": [_p, _p, _i64, _p, _i64, _p, _p, _p],
+    "q4_verify_greedy": [_p, _p, _i64, _p, _i64, _p, _p],
     "q4mm_select_path": [_p, _i64, _u32],
     "q4mm_plan_info": [_p, _i64, _u32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                        ctypes.POINTER(ctypes.c_int)],
@@ -270,6 +273,39 @@ def q4mm_forward_group(Ws, x: torch.Tensor, ys=None, flags: int = 0, stream=None
         _check(_lib.q4mm_forward_group(hw, len(Ws), x.data_ptr(), hy, M, int(flags), _stream(stream)),
                "q4mm_forward_group")
     return ys
+
+
+def q4mm_argmax_rows(W: Q4Weight, x: torch.Tensor, rows: torch.Tensor, want_max: bool = True,
+                     stream=None):
+    """Greedy pick (idx int32 [R], max fp32 [R] or None) for the x rows listed in `rows`."""
+    _dev_f32(x, "x")
+    if x.dim() != 2 or x.shape[1] != W.K:
+        raise ValueError("x must be [rows, %d]" % W.K)
+    if rows.dtype != torch.int32 or not rows.is_cuda or not rows.is_contiguous():
+        raise ValueError("rows must be a contiguous int32 CUDA tensor")
+    R = rows.numel()
+    idx = torch.empty((R,), dtype=torch.int32, device=x.device)
+    mx = torch.empty((R,), dtype=torch.float32, device=x.device) if want_max else None
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_argmax_rows(W.handle, x.data_ptr(), x.shape[0], rows.data_ptr(), R, idx.data_ptr(),
+                                     mx.data_ptr() if mx is not None else None, _stream(stream)),
+               "q4mm_argmax_rows")
+    return idx, mx
+
+
+def q4_verify_greedy(idx: torch.Tensor, draft: torch.Tensor, offsets: torch.Tensor, stream=None):
+    """accepted[s]: leading positions of segment s where idx == draft (-1: malformed segment)."""
+    for t, n in ((idx, "idx"), (draft, "draft"), (offsets, "offsets")):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous int32 CUDA tensor" % n)
+    if idx.numel() != draft.numel():
+        raise ValueError("idx and draft differ in length")
+    S = offsets.numel() - 1
+    acc = torch.empty((max(S, 0),), dtype=torch.int32, device=idx.device)
+    with torch.cuda.device(idx.device):
+        _check(_lib.q4_verify_greedy(idx.data_ptr(), draft.data_ptr(), idx.numel(), offsets.data_ptr(), max(S, 0),
+                                     acc.data_ptr(), _stream(stream)), "q4_verify_greedy")
+    return acc
 
 
 def q4mm_argmax_ex(W: Q4Weight, x: torch.Tensor, flags: int = 0, want_max: bool = True, stream=None):

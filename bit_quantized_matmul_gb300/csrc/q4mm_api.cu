@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -405,6 +406,41 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
   return Q4_OK;
 }
 
+int q4mm_argmax_rows(const q4_weight* Wh, const float* x, int64_t x_rows, const int32_t* rows,
+                     int64_t R, int32_t* idx, float* maxval, cudaStream_t stream) {
+  if (!Wh || !x || !rows || !idx) return Q4_ERR_INVALID_ARG;
+  if (R < 0 || x_rows < 1 || x_rows > INT32_MAX) return Q4_ERR_INVALID_ARG;
+  if (R > Q4MM_M_MAX) return Q4_ERR_SHAPE;
+  if (R == 0) return Q4_OK;
+  if (!aligned16(x) || !aligned16(idx) || (maxval && !aligned16(maxval))) return Q4_ERR_ALIGN;
+  const Weight* W = &Wh->w;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (dev != W->device) return Q4_ERR_INVALID_ARG;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  const MmaPlan plan = mma_plan(W, ds.num_sms);
+  Workspace ws;
+  st = workspace_get(dev, mma_partial_bytes(W, plan, R, false), 0, &ws);
+  if (st) return st;
+  MmaLaunch L;
+  L.count = 1;
+  L.W[0] = W;
+  L.y[0] = nullptr;
+  return launch_mma_group(L, x, R, idx, maxval, plan, false, ws, stream, rows, x_rows);
+}
+
+int q4_verify_greedy(const int32_t* idx, const int32_t* draft, int64_t total, const int32_t* offsets,
+                     int64_t S, int32_t* accepted, cudaStream_t stream) {
+  if (!idx || !draft || !offsets || !accepted || total < 0 || S < 0 || S > INT32_MAX - 128)
+    return Q4_ERR_INVALID_ARG;
+  if (S == 0) return Q4_OK;
+  return launch_verify(idx, draft, total, offsets, (int)S, accepted, stream);
+}
+
 int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                 cudaStream_t stream) {
   if (!idx) return Q4_ERR_INVALID_ARG;
@@ -485,7 +521,7 @@ int q4_device_status(void) {
     const unsigned zero = 0;
     if (cudaMemcpy(ds.ws.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
       return Q4_ERR_CUDA;
-    return Q4_ERR_TIMEOUT;
+    return (v & STATUS_TIMEOUT) ? Q4_ERR_TIMEOUT : Q4_ERR_INVALID_ARG;
   }
   return Q4_OK;
 }

@@ -63,7 +63,7 @@ struct Weight {
 
 // Per-device scratch shared by all handles on that device.
 struct Workspace {
-  unsigned int* status = nullptr;      // device status word (Q4_ERR_TIMEOUT ...)
+  unsigned int* status = nullptr;      // device status word: STATUS_* bits
   unsigned int* counters = nullptr;    // split-K arrival counters, self-resetting
   unsigned long long* keys = nullptr;  // argmax keys [Q4MM_M_MAX], self-resetting
   unsigned int* argmax_done = nullptr; // argmax completion counter
@@ -73,6 +73,10 @@ struct Workspace {
   size_t xop_bytes = 0;
 };
 constexpr int MAX_COUNTERS = 1 << 16;
+
+// Bits of the device status word (read and cleared by q4_device_status).
+constexpr unsigned STATUS_TIMEOUT = 1u;   // a bounded wait ran out
+constexpr unsigned STATUS_BAD_ROW = 2u;   // a row index of q4mm_argmax_rows was out of range
 
 // Returns Q4_OK and fills *ws with at least the requested capacities.
 int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws);
@@ -108,7 +112,12 @@ int mma_launch_count(int64_t M, bool batch_invariant);
 int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
                const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
-                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
+                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s,
+                     const int32_t* xrows = nullptr, int64_t x_rows = 0);
+
+// Greedy verification of draft tokens per request (see q4_verify_greedy).
+int launch_verify(const int32_t* idx, const int32_t* draft, int64_t total, const int32_t* offsets,
+                  int S, int32_t* accepted, cudaStream_t s);
 
 // CUDA-core streaming kernel.
 MmaPlan simt_plan(const Weight* W, int num_sms);

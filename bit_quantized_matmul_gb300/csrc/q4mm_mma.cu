@@ -67,7 +67,9 @@ struct MmaWeight {
 struct MmaArgs {
   MmaWeight w[MMA_GROUP_MAX];
   int nweights;
-  const float* x;       // [mrows, K] activations of this launch
+  const float* x;       // [mrows, K] activations of this launch, or the whole x with xrows
+  const int32_t* xrows; // null, or token row m of this launch is row xrows[m] of x
+  int64_t x_rows;       // rows of x when xrows is given (indices are checked)
   int64_t K, KBP;       // K, block pairs
   int mrows;            // token rows in this launch
   int64_t kbp_per_split;
@@ -403,6 +405,22 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     const int s2 = pc & 1;
     const int oa = ((tql) ^ h) * 16, ob = ((tql + 1) ^ h) * 16;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+    // row m of this launch: x row xrows[m] when a row list is given (checked:
+    // an index outside [0, x_rows) reads zeros and sets STATUS_BAD_ROW)
+    int64_t xoff[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      xoff[m] = -1;
+      if (m < mrows) {
+        if (a.xrows == nullptr) {
+          xoff[m] = (int64_t)m * a.K;
+        } else {
+          const int32_t r = __ldg(a.xrows + m);
+          if (r >= 0 && (int64_t)r < a.x_rows) xoff[m] = (int64_t)r * a.K;
+          else if (ct == 0 && split == 0) atomicOr(a.status, STATUS_BAD_ROW);
+        }
+      }
+    }
     const float* xr = a.x + bp0 * 64 + 4 * ct;
     const uint8_t* sg = scl_w + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
     // Stage chunk c: this thread's 16 bytes of every token row (k = 4ct..4ct+3)
@@ -416,9 +434,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         if (k_ok) {
 #pragma unroll
           for (int m = 0; m < MAXM; ++m)
-            if (m < mrows)
+            if (xoff[m] >= 0)
               cp_async16(smem_u32(xs + m * (CHUNK_K * 4) + ct * 16),
-                         xr + (int64_t)m * a.K + (int64_t)c * CHUNK_K);
+                         xr + xoff[m] + (int64_t)c * CHUNK_K);
         }
         const int scl_bytes = min(CHUNK_PAIRS, npairs - c * CHUNK_PAIRS) * PAIR_SCL_BYTES;
 #pragma unroll
@@ -462,7 +480,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #pragma unroll
           for (int mm = 0; mm < MG; ++mm) {
             v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (m0 + mm < mrows && k_ok)
+            if (m0 + mm < mrows && k_ok && xoff[m0 + mm] >= 0)
               v[mm] = *reinterpret_cast<const float4*>(xs + (m0 + mm) * (CHUNK_K * 4) + ct * 16);
           }
 #pragma unroll
@@ -493,7 +511,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after the previous kernel
   __syncthreads();
   if (s_err) {
-    if (tid == 0) atomicOr(a.status, (unsigned)Q4_ERR_TIMEOUT);
+    if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
     return;
   }
 
@@ -550,7 +568,8 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 
 template <int C, bool DENSE>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
-             const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
+             const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
+             const int32_t* xrows, int64_t x_rows) {
   using S = MmaCfg<C>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
@@ -571,6 +590,8 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   }
   a.nweights = L.count;
   a.x = x;
+  a.xrows = xrows;
+  a.x_rows = x_rows;
   a.K = W0->K;
   a.KBP = W0->KBP;
   a.mrows = mrows;
@@ -648,7 +669,8 @@ int mma_launch_count(int64_t M, bool batch_invariant) {
 }
 
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
-                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s) {
+                     const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s,
+                     const int32_t* xrows, int64_t x_rows) {
   int64_t tiles = 0;
   for (int i = 0; i < L.count; ++i) tiles += L.W[i]->tiles;
   if (plan.splits > 1 && tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
@@ -656,19 +678,20 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   const int64_t rpl = rows_per_launch(batch_invariant);
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
-    const float* xs = x + mb * K;
+    const float* xs = xrows ? x : x + mb * K;
+    const int32_t* xr = xrows ? xrows + mb : nullptr;
     int st;
     if (batch_invariant) {
       switch (mrows) {
-        case 1: st = launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
-        case 2: st = launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
-        default: st = launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        case 1: st = launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        case 2: st = launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        default: st = launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
       }
     } else {
       switch ((3 * mrows + 7) / 8) {  // column groups of this launch
-        case 1: st = launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
-        case 2: st = launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
-        default: st = launch_c<3, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s); break;
+        case 1: st = launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        case 2: st = launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        default: st = launch_c<3, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
       }
     }
     if (st) return st;

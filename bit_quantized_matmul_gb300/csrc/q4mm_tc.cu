@@ -36,7 +36,7 @@
 //                the activation operand of a unit into one smem stage
 //   warps 18-21  MMA issuers (every fourth unit each); warp 18 also owns the
 //                TMEM allocation
-// Every mbarrier wait is bounded; on expiry the CTA records Q4_ERR_TIMEOUT in
+// Every mbarrier wait is bounded; on expiry the CTA records STATUS_TIMEOUT in
 // the device status word, drains what it issued, frees TMEM and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     tmem_dealloc(tmem, TMEM_COLS);
   }
   if (*err != 0) {
-    if (tid == 0) atomicOr(a.status, (unsigned)Q4_ERR_TIMEOUT);
+    if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
     return;
   }
   if (warp < EPI_WARP0 || warp >= EPI_WARP0 + 4) return;  // warps 8-11 own the rows now

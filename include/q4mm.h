@@ -210,6 +210,33 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
 Q4_API int q4mm_forward_noalloc(const q4_weight* W, const float* x, float* y, int64_t M,
                                 cudaStream_t stream);
 
+/* Greedy pick for selected rows of a ragged continuous-batching step: only
+ * the rows that need logits (the last prefill row of a request, its verify
+ * rows, decode rows) go through the LM head, without gathering them first.
+ *   x       device, fp32 [x_rows, K] row-major, 16-byte aligned (the step's
+ *           hidden states); 1 <= x_rows <= INT32_MAX.
+ *   rows    device, int32 [R]: the x row of each output; an index outside
+ *           [0, x_rows) reads zeros and makes the next q4_device_status()
+ *           return Q4_ERR_INVALID_ARG (it is checked on the device, never read
+ *           out of bounds).
+ *   idx     device, int32 [R]; maxval device, fp32 [R] or NULL.
+ *   R       0 <= R <= Q4MM_M_MAX.
+ * Same result as q4mm_argmax on the gathered rows (streaming kernel). */
+Q4_API int q4mm_argmax_rows(const q4_weight* W, const float* x, int64_t x_rows, const int32_t* rows,
+                            int64_t R, int32_t* idx, float* maxval, cudaStream_t stream);
+
+/* Greedy verification of speculative draft tokens, one result per request:
+ * accepted[s] = the number of leading positions j of request s's segment
+ * [offsets[s], offsets[s+1]) with idx[j] == draft[j] (the request keeps the
+ * drafts up to the first disagreement), or -1 if the segment is malformed
+ * (decreasing offsets, or outside [0, total)).
+ *   idx, draft  device, int32 [total] (idx from q4mm_argmax / _rows; draft[j]
+ *               the token proposed at the position idx[j] predicts).
+ *   offsets     device, int32 [S + 1].  accepted: device, int32 [S]. */
+Q4_API int q4_verify_greedy(const int32_t* idx, const int32_t* draft, int64_t total,
+                            const int32_t* offsets, int64_t S, int32_t* accepted,
+                            cudaStream_t stream);
+
 /* The kernel path (Q4MM_PATH_*) a call with these arguments would take, or a
  * negative status. */
 Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
@@ -229,7 +256,8 @@ Q4_API int q4mm_set_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_m_threshold(void);
 
 /* Synchronize the current device and return (then clear) the device status
- * word: Q4_OK, or Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out, or
+ * word: Q4_OK; Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out;
+ * Q4_ERR_INVALID_ARG if q4mm_argmax_rows met a row index out of range; or
  * Q4_ERR_CUDA if the device reports an error. */
 Q4_API int q4_device_status(void);
 

@@ -64,3 +64,5 @@ def test_null_arguments_rejected_on_host(q4):
     assert lib.q4mm_select_path(None, 1, 0) == -q4.Q4_ERR_INVALID_ARG
     assert lib.q4mm_forward_noalloc(None, None, None, 4, None) == q4.Q4_ERR_INVALID_ARG
     assert lib.q4mm_forward_group(None, 1, None, None, 4, 0, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_argmax_rows(None, None, 1, None, 1, None, None, None) == q4.Q4_ERR_INVALID_ARG
+    assert lib.q4_verify_greedy(None, None, 0, None, 1, None, None) == q4.Q4_ERR_INVALID_ARG
