@@ -40,8 +40,8 @@ DeviceScratch g_dev[MAX_DEVICES];
 // Below this M the streaming mma.sync kernel is used, at or above it the
 // tcgen05 kernel.  Measured on GB300 over one Qwen2.5-7B decoder layer's seven
 // linears (bench.py --path-sweep, M in 1..256): the streaming kernel is faster
-// for the whole layer up to M = 64, the tensor-core kernel from M = 128.
-constexpr int64_t DEFAULT_M_THRESHOLD = 128;
+// for the whole layer up to M = 8, the tensor-core kernel from M = 16.
+constexpr int64_t DEFAULT_M_THRESHOLD = 16;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -1,4 +1,5 @@
-// q4mm_tc.cu — tensor-core (tcgen05 / TMEM) path of the Q4_0 matmul.
+// q4mm_tc.cu — tensor-core (tcgen05 / TMEM) path of the Q4_0 matmul, for
+// many token rows.
 //
 // For several token rows this is the "GEMM" side of the kernel split in
 // "Why Continuous Batching Slowed Down My LLM Inference Engine"
@@ -8,34 +9,31 @@
 // weights are dequantized on the fly inside the kernel.
 //
 // Exactness.  The result must match the fp64 reference to about fp32
-// accuracy, so the tensor-core operands are exact:
-//   A (weights)     (q - 8), small integers, exact in bf16, written by the
-//                   CUDA cores straight into tensor memory: bf16(128 + q) is
-//                   0x4300 | q, and subtracting 136 is exact;
+// accuracy, so every tensor-core product is exact:
+//   A (weights)     w = (q - 8) * d has at most 14 significant bits (a 4-bit
+//                   integer times the 11-bit significand of the fp16 scale),
+//                   so it is the exact sum of two bf16 terms: hi = bf16(w)
+//                   (round to nearest) and lo = w - hi.  The CUDA cores form
+//                   both and write them into tensor memory.
 //   B (activations) x split into three bf16 terms x0 + x1 + x2 == x exactly
 //                   (pre-pass kernel), stacked along the MMA's N dimension
-//                   (term t of token row m is B row t*MTR + m), so one
-//                   128 x NB x 16 MMA covers every term and row of a tile;
-//   per-block scale the fp16 scale d of each 32-weight block is applied on
-//                   the CUDA cores: the block's accumulator
-//                   D_b[n, t*MTR + m] = sum_{k in b} (q-8) x_t[m, k] is read
-//                   back from TMEM and folded as acc = fma(d, (D0+D1)+D2, acc).
+//                   (term t of token row m is B row t*MTR + m).
+// With the scale inside A, one fp32 accumulator in tensor memory takes the
+// whole K range: per k-step two MMAs (hi, lo) of 128 x NB x 16, NB up to 240
+// (80 token rows per CTA), and the CUDA cores read the accumulator once at
+// the end: y[m, n] = (D[n, m] + D[n, MTR+m]) + D[n, 2 MTR+m].
 //
 // Work decomposition.  CTA = one 128-row weight tile (a TMEM lane per row) x
-// one K range (a split that depends on N and K only) x one tile of MTR token
-// rows (MTR = NB/3).  The K range is processed in units of U = 4 blocks; every
-// barrier, bulk copy and commit is per unit, because each such operation
-// costs tens of cycles of issue latency in the thread that executes it.
-// Roles (704 threads):
-//   warps  0- 7  converters: nibbles -> bf16 (q-8) in the TMEM A ring; two
-//                groups of four (one per TMEM lane quarter) take alternate units
-//   warps  8-15  epilogue: TMEM D ring -> scale -> fp32 accumulators; two
-//                groups take alternate units; their sums are added in a fixed
-//                order (even units + odd units) at the end
-//   warps 16-17  bulk-copy producers (alternate units): nibbles, scales and
-//                the activation operand of a unit into one smem stage
-//   warps 18-21  MMA issuers (every fourth unit each); warp 18 also owns the
-//                TMEM allocation
+// one K range (split from the shapes) x one tile of MTR token rows.  The K
+// range is processed in units of U = 4 blocks; every barrier, bulk copy and
+// commit is per unit.  Roles (320 threads):
+//   warps 0-7  converters: nibbles and scales -> hi/lo bf16 weights in the
+//              TMEM A ring; two groups of four (one per TMEM lane quarter)
+//              take alternate units; warps 0-3 also run the epilogue
+//   warp  8    bulk-copy producer: nibbles, scales and the activation
+//              operand of a unit into one smem stage
+//   warp  9    MMA issuer (one thread, so the accumulator's MMAs are ordered);
+//              owns the TMEM allocation
 // Every mbarrier wait is bounded; on expiry the CTA records STATUS_TIMEOUT in
 // the device status word, drains what it issued, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -48,21 +46,15 @@ namespace q4 {
 namespace {
 
 constexpr int U = 4;                    // blocks per unit (two block pairs)
-constexpr int CONV_WARP0 = 0;           // 8 warps
-constexpr int EPI_WARP0 = 8;            // 8 warps
-constexpr int PROD_WARP0 = 16;          // 2 warps
-constexpr int MMA_WARP0 = 18;           // 4 warps
-constexpr int NPROD = 2;
-constexpr int NISS = 4;
-constexpr int TC_THREADS = 22 * 32;
+constexpr int PROD_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int TC_THREADS = 10 * 32;
 constexpr int TMEM_COLS = 512;
-constexpr int MAX_STAGES = 16;
+constexpr int EPI_ROWS = 16;            // token rows per epilogue chunk
 // Barriers are per unit, in a ring of NBR units: unit u uses index u % NBR at
 // phase parity (u / NBR) & 1.  Every role handles its units in order and NBR is
-// a multiple of the role strides (2 and 4), so a waiter has always observed the
-// previous phase of the same barrier before it waits for the next one; a
-// parity wait can never run two phases ahead, however the four MMA issuers and
-// the independently progressing warps interleave.
+// a multiple of the role strides (1 and 2), so a waiter has always observed
+// the previous phase of the same barrier before it waits for the next one.
 constexpr int NBR = 64;
 constexpr int SMEM_BUDGET = 200 * 1024;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // 1 s bound on any wait
@@ -76,21 +68,19 @@ struct Cfg {
   static constexpr int BOP_OFF = SCL_OFF + SCL_BYTES;
   static constexpr int BOP_BLOCK = 64 * NB;            // 2 k-steps x NB rows x 16 k x 2 B
   static constexpr int STAGE_BYTES = BOP_OFF + U * BOP_BLOCK;
-  static constexpr int A_UNIT_COLS = U * 16;           // 64
-  static constexpr int D_UNIT_COLS = U * NB;
-  static constexpr int NA = NB == 16 ? 3 : 2;
-  static constexpr int ND = (TMEM_COLS - NA * A_UNIT_COLS) / D_UNIT_COLS;
-  static constexpr int NSC = NA + ND;                  // scale ring (units)
-  static constexpr int DSL_BYTES = NSC * U * TILE_N * 4;
-  static constexpr int BAR_BYTES = 6 * NBR * 8 + 16;
-  static constexpr int NST_RAW = (SMEM_BUDGET - DSL_BYTES - BAR_BYTES) / STAGE_BYTES;
-  static constexpr int NST = NST_RAW > MAX_STAGES ? MAX_STAGES : NST_RAW;
-  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + DSL_BYTES + BAR_BYTES;
-  static_assert(NA * A_UNIT_COLS + ND * D_UNIT_COLS <= TMEM_COLS, "TMEM budget");
-  static_assert(ND >= 3 && NA >= 2 && NST >= 6, "pipeline too shallow");
-  static_assert(NBR % 4 == 0 && NBR > 2 * (NST + NA + ND), "barrier ring depth");
-  static_assert(MTR * TILE_N * 4 <= NST * STAGE_BYTES, "group-combine buffer");
-  static_assert(NB == 16 || NB == 32, "MMA N");
+  static constexpr int A_BLOCK_COLS = 32;              // [term hi/lo][k-step][8 columns]
+  static constexpr int A_UNIT_COLS = U * A_BLOCK_COLS;  // 128
+  static constexpr int NA_RAW = (TMEM_COLS - NB) / A_UNIT_COLS;
+  static constexpr int NA = NA_RAW > 3 ? 3 : NA_RAW;   // A ring (units)
+  static constexpr int BAR_BYTES = (4 * NBR + 1) * 8 + 16;
+  static constexpr int NST_RAW = (SMEM_BUDGET - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int NST = NST_RAW > 8 ? 8 : NST_RAW;
+  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + BAR_BYTES;
+  static constexpr int CHUNKS = MTR / EPI_ROWS;
+  static_assert(MTR % EPI_ROWS == 0 && 3 * MTR == NB, "token tile");
+  static_assert(NA * A_UNIT_COLS + NB <= TMEM_COLS, "TMEM budget");
+  static_assert(NA >= 2 && NST >= 2, "pipeline too shallow");
+  static_assert(NBR % 2 == 0 && NBR > 2 * (NST + NA), "barrier ring depth");
 };
 
 struct TcArgs {
@@ -294,13 +284,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
 }
 
 // (q - 8) for the nibble pair at bits (4p, 16 + 4p) of w, as exact bf16x2:
-// (w >> 4p) & 0x000F000F | 0x43004300 is the pair bf16(128 + q), and one
-// bf16x2 FMA, x * 1.0 + (-136.0), gives q - 8 exactly.
+// (w >> 4p) & 0x000F000F | 0x43004300 is bf16(128 + q), minus 136 is exact.
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
-  const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-  uint32_t r;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
+  uint32_t t, r;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(w >> (4 * p)));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
   return r;
+}
+
+// The two weights (q0 - 8) * d, (q1 - 8) * d of a bf16x2 (q - 8) pair as the
+// exact sums hi + lo of two bf16x2 values (see the file comment).
+__device__ __forceinline__ void scale_split(uint32_t qa, float d, uint32_t& hi, uint32_t& lo) {
+  const float p0 = __uint_as_float(qa << 16) * d;            // exact in fp32
+  const float p1 = __uint_as_float(qa & 0xFFFF0000u) * d;
+  const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);   // low half: p0
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - __low2float(h), p1 - __high2float(h));
+  lo = *reinterpret_cast<const uint32_t*>(&l);               // remainders are exact in bf16
 }
 
 // ----------------------------------------------------------------------------
@@ -371,18 +371,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   constexpr int MTR = C::MTR;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* dsl = reinterpret_cast<float*>(smem + C::NST * C::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE_BYTES + C::DSL_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE_BYTES);
   uint64_t* full = bars;           // unit data landed in its smem stage (tx count)
   uint64_t* empty = full + NBR;    // stage consumed: 4 converter warps + MMA commit
-  uint64_t* afull = empty + NBR;   // A operand written to TMEM: 4 converter warps
+  uint64_t* afull = empty + NBR;   // A terms written to TMEM: 4 converter warps
   uint64_t* afree = afull + NBR;   // MMAs of the unit done (A slot reusable): commit
-  uint64_t* dfull = afree + NBR;   // accumulators of the unit ready: commit
-  uint64_t* dfree = dfull + NBR;   // accumulators read back: 4 epilogue warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfree + NBR);
+  uint64_t* dfull = afree + NBR;   // every MMA of the CTA done: commit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
   volatile int* err = reinterpret_cast<volatile int*>(tmem_slot + 2);
   __shared__ int s_last;
-  __shared__ unsigned long long red[4][MTR];  // greedy-pick scratch of the epilogue
+  __shared__ unsigned long long red[4][EPI_ROWS];  // greedy-pick scratch of the epilogue
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -400,34 +398,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
       mbar_init(smem_u32(&empty[i]), 4 + 1);
       mbar_init(smem_u32(&afull[i]), 4);
       mbar_init(smem_u32(&afree[i]), 1);
-      mbar_init(smem_u32(&dfull[i]), 1);
-      mbar_init(smem_u32(&dfree[i]), 4);
     }
+    mbar_init(smem_u32(dfull), 1);
     *err = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == MMA_WARP0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == MMA_WARP) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_base = tmem;                                    // A ring columns
-  const uint32_t d_base = tmem + (uint32_t)(C::NA * C::A_UNIT_COLS);  // D ring columns
+  const uint32_t a_base = tmem;                                      // A ring columns
+  const uint32_t d_base = tmem + (uint32_t)(C::NA * C::A_UNIT_COLS);  // accumulator columns
 
-  float acc[MTR];
-#pragma unroll
-  for (int m = 0; m < MTR; ++m) acc[m] = 0.0f;
-
-  if (warp >= PROD_WARP0 && warp < PROD_WARP0 + NPROD) {
-    // ---------------- producers ----------------
+  if (warp == PROD_WARP) {
+    // ---------------- producer ----------------
     if (lane == 0) {
-      const int p = warp - PROD_WARP0;
-      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the activation operand of the pre-pass
       const uint8_t* nib_base = a.nib + ((int64_t)tile * a.KBP + bp0) * PAIR_NIB_BYTES;
       const uint8_t* scl_base = a.scl + ((int64_t)tile * a.KBP + bp0) * PAIR_SCL_BYTES;
       const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB2 + 2 * bp0) * (int64_t)C::BOP_BLOCK;
       int last = -1;
-      for (int u = p; u < nunits; u += NPROD) {
+      for (int u = 0; u < nunits; ++u) {
         const int st = u % C::NST;
         const int ub = min(U, nblk - u * U);
         if (u >= C::NST) {  // stage reuse: unit u - NST must be consumed
@@ -443,49 +435,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         last = u;
       }
       // drain: every copy this producer issued has landed before the CTA exits
-      for (int u = last; u >= 0 && u > last - C::NST; u -= NPROD)
+      for (int u = last; u >= 0 && u > last - C::NST; --u)
         mbar_drain(smem_u32(&full[u % NBR]), (u / NBR) & 1);
     }
-  } else if (warp >= MMA_WARP0) {
-    // ---------------- MMA issuers ----------------
+  } else if (warp == MMA_WARP) {
+    // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16(NB);
-      const int iss = warp - MMA_WARP0;
-      int last = -1;
-      for (int u = iss; u < nunits; u += NISS) {
-        const int st = u % C::NST, sa = u % C::NA, sd = u % C::ND;
+      uint32_t accumulate = 0;
+      bool ok = true;
+      for (int u = 0; u < nunits; ++u) {
+        const int st = u % C::NST, sa = u % C::NA;
         const int ub = min(U, nblk - u * U);
         const int bi = u % NBR;
         const uint32_t par = (u / NBR) & 1;
-        if (!mbar_wait(smem_u32(&full[bi]), par, err)) break;
-        if (!mbar_wait(smem_u32(&afull[bi]), par, err)) break;
-        if (u >= C::ND) {  // D slot reuse: unit u - ND must be read back
-          const int v = u - C::ND;
-          if (!mbar_wait(smem_u32(&dfree[v % NBR]), (v / NBR) & 1, err)) break;
+        if (!mbar_wait(smem_u32(&full[bi]), par, err) || !mbar_wait(smem_u32(&afull[bi]), par, err)) {
+          ok = false;
+          break;
         }
         tc_fence_after();
         const uint32_t bop = smem_u32(stages + st * C::STAGE_BYTES + C::BOP_OFF);
         const uint32_t acol = a_base + (uint32_t)(sa * C::A_UNIT_COLS);
-        const uint32_t dcol = d_base + (uint32_t)(sd * C::D_UNIT_COLS);
         for (int b = 0; b < ub; ++b) {
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             const uint64_t bd = smem_desc(bop + (uint32_t)(b * C::BOP_BLOCK + s * 32 * NB), 16u * NB, 128u);
-            mma_ts(dcol + (uint32_t)(b * NB), acol + (uint32_t)(b * 16 + 8 * s), bd, IDESC, s != 0);
+#pragma unroll
+            for (int term = 0; term < 2; ++term) {
+              mma_ts(d_base, acol + (uint32_t)(b * C::A_BLOCK_COLS + term * 16 + s * 8), bd, IDESC,
+                     accumulate);
+              accumulate = 1;
+            }
           }
         }
         mma_commit(smem_u32(&afree[bi]));
-        mma_commit(smem_u32(&dfull[bi]));
         mma_commit(smem_u32(&empty[bi]));
-        last = u;
       }
-      if (last >= 0)  // drain: the last commit covers every MMA this thread issued
-        mbar_drain(smem_u32(&dfull[last % NBR]), (last / NBR) & 1);
+      mma_commit(smem_u32(dfull));  // arrives once every MMA issued above has completed
+      mbar_drain(smem_u32(dfull), 0);
+      (void)ok;
     }
     __syncwarp();
-  } else if (warp < EPI_WARP0) {
+  } else {
     // ---------------- converters ----------------
-    const int q = warp & 3, g = (warp - CONV_WARP0) >> 2;
+    const int q = warp & 3, g = warp >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     // this row's place in the fragment layout
@@ -523,105 +516,97 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         const int w = u - C::NA;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&afree[w % NBR]), (w / NBR) & 1, err))) break;
       }
-      // The scale slot u % NSC was last read by the epilogue of unit u - NSC;
-      // the wait above orders it: MMA(u - NA) waited for the read-back of unit
-      // u - NA - ND = u - NSC.
-      float* dslu = dsl + (u % C::NSC) * (U * TILE_N);
-#pragma unroll
-      for (int b = 0; b < U; ++b) dslu[b * TILE_N + row] = dsc[b];
       const uint32_t acol = a_base + lane_off + (uint32_t)(sa * C::A_UNIT_COLS);
 #pragma unroll
-      for (int h = 0; h < U / 2; ++h) {
-        // TMEM column c of a block holds k = 2c, 2c + 1: the pair at
+      for (int b = 0; b < U; ++b) {
+        // TMEM column c of a term and k-step holds k = 2c, 2c + 1: the pair at
         // k0 = 16s + 2tq is column 8s + tq, the pair at k0 + 8 is 8s + 4 + tq
-        uint32_t av[32];
+        uint32_t av[32];  // [term][k-step][8 columns]
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb)
+        for (int tq = 0; tq < 4; ++tq) {
+          const uint32_t ws[2] = {v[b][tq].x, v[b][tq].y};
 #pragma unroll
-          for (int tq = 0; tq < 4; ++tq) {
-            const uint32_t ws[2] = {v[2 * h + bb][tq].x, v[2 * h + bb][tq].y};
-#pragma unroll
-            for (int st2 = 0; st2 < 2; ++st2) {
-              av[16 * bb + 8 * st2 + tq] = nib_pair_bf16(ws[st2], fup);
-              av[16 * bb + 8 * st2 + 4 + tq] = nib_pair_bf16(ws[st2], fup + 2);
-            }
+          for (int s = 0; s < 2; ++s) {
+            uint32_t hi, lo;
+            scale_split(nib_pair_bf16(ws[s], fup), dsc[b], hi, lo);
+            av[8 * s + tq] = hi;
+            av[16 + 8 * s + tq] = lo;
+            scale_split(nib_pair_bf16(ws[s], fup + 2), dsc[b], hi, lo);
+            av[8 * s + 4 + tq] = hi;
+            av[16 + 8 * s + 4 + tq] = lo;
           }
-        tmem_st32(acol + (uint32_t)(32 * h), av);
+        }
+        tmem_st32(acol + (uint32_t)(b * C::A_BLOCK_COLS), av);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&afull[bi]));
     }
-  } else {
-    // ---------------- epilogue ----------------
-    const int q = warp & 3, g = (warp - EPI_WARP0) >> 2;
-    const int row = q * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    for (int u = g; u < nunits; u += 2) {
-      const int sd = u % C::ND;
-      const int ub = min(U, nblk - u * U);
-      const int bi = u % NBR;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&dfull[bi]), (u / NBR) & 1, err))) break;
-      tc_fence_after();
-      const float* dslu = dsl + (u % C::NSC) * (U * TILE_N);
-      const uint32_t dcol = d_base + lane_off + (uint32_t)(sd * C::D_UNIT_COLS);
-      for (int b = 0; b < ub; ++b) {
-        float dv[NB];
-#pragma unroll
-        for (int c = 0; c < NB; c += 16) {
-          float t16[16];
-          tmem_ld16(dcol + (uint32_t)(b * NB + c), t16);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) dv[c + e] = t16[e];
-        }
-        tmem_wait_ld();
-        const float dsc = dslu[b * TILE_N + row];
-#pragma unroll
-        for (int m = 0; m < MTR; ++m)
-          if (m < mcount) acc[m] = fmaf(dsc, (dv[m] + dv[MTR + m]) + dv[2 * MTR + m], acc[m]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&dfree[bi]));
-    }
   }
 
-  // ---- combine the two epilogue groups (fixed order: even units + odd units) ----
+  // ---- epilogue: warps 0-3 read the accumulator once ----
   tc_fence_before();
   __syncthreads();
-  float* comb = reinterpret_cast<float*>(stages);
-  if (warp >= EPI_WARP0 + 4 && warp < EPI_WARP0 + 8) {
-    const int row = (warp & 3) * 32 + lane;
+  const bool skip = *err != 0;
+  __syncthreads();  // every thread has read the flag before the epilogue can raise it
+  if (warp < 4 && !skip) {
+    const bool ok = mbar_wait(smem_u32(dfull), 0, err);
+    // every epilogue thread takes the same decision
+    uint32_t any_bad;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.eq.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(any_bad)
+        : "r"((uint32_t)ok)
+        : "memory");
+    if (!any_bad) {
+      tc_fence_after();
+      const int row = warp * 32 + lane;
+      const uint32_t drow = d_base + ((uint32_t)(warp * 32) << 16);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after earlier kernels
+#pragma unroll 1
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        const int c0 = c * EPI_ROWS;
+        if (c0 >= mcount) break;  // the same for every split of this tile
+        float t0[16], t1[16], t2[16], val[EPI_ROWS];
+        tmem_ld16(drow + (uint32_t)c0, t0);
+        tmem_ld16(drow + (uint32_t)(MTR + c0), t1);
+        tmem_ld16(drow + (uint32_t)(2 * MTR + c0), t2);
+        tmem_wait_ld();
 #pragma unroll
-    for (int m = 0; m < MTR; ++m) comb[m * TILE_N + row] = acc[m];
+        for (int j = 0; j < EPI_ROWS; ++j) val[j] = (t0[j] + t1[j]) + t2[j];
+        finish_tile<EPI_ROWS>(a.e, val, row, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split,
+                              (tile * a.mtiles + mt) * C::CHUNKS + c, &s_last, red,
+                              []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
+      }
+    }
   }
+  tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP0) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  if (*err != 0) {
-    if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
-    return;
-  }
-  if (warp < EPI_WARP0 || warp >= EPI_WARP0 + 4) return;  // warps 8-11 own the rows now
-
-  const int row = (warp & 3) * 32 + lane;
-#pragma unroll
-  for (int m = 0; m < MTR; ++m) acc[m] += comb[m * TILE_N + row];
-  // named barrier over the 128 threads of warps 8-11
-  finish_tile<MTR>(a.e, acc, row, tile, m0, mcount, split, tile * a.mtiles + mt, &s_last, red,
-                   []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
+  if (*err != 0 && tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
 }
 
 constexpr int64_t TC_M_LAUNCH = 256;  // rows per launch pair (pre-pass + main)
 
-// MMA N for a launch of ml rows.  Batch-invariant mode always uses NB = 32 so
-// that neither the instruction shape nor the token tile depends on M.
+// MMA N (3 x token rows per CTA) for a launch of ml rows: as few token tiles
+// as the largest N (80 rows) needs, each as small as that count allows.
+// Forced with the batch-invariant flag: always NB = 96, independent of M.
 int nb_for(int64_t ml, bool batch_invariant) {
-  if (batch_invariant) return 32;
-  return ml <= Cfg<16>::MTR ? 16 : 32;
+  if (batch_invariant) return 96;
+  const int64_t passes = (ml + 79) / 80;
+  const int64_t r = (ml + passes - 1) / passes;
+  if (r <= 16) return 48;
+  if (r <= 32) return 96;
+  if (r <= 48) return 144;
+  if (r <= 64) return 192;
+  return 240;
 }
 
 template <int NB>
@@ -630,7 +615,7 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   using C = Cfg<NB>;
   const int mtiles = (int)((ml + C::MTR - 1) / C::MTR);
   const int64_t KB2 = 2 * W->KBP;
-  if (plan.splits > 1 && W->tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
+  if (plan.splits > 1 && W->tiles * mtiles * C::CHUNKS > MAX_COUNTERS) return Q4_ERR_SHAPE;
   {
     const int64_t total = (int64_t)mtiles * KB2 * 4 * C::MTR;
     const int64_t want = (total + 255) / 256;
@@ -644,6 +629,12 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
                              C::SMEM_BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W->device & 63] = true;
+  }
+  // greedy-pick completion count: one epilogue chunk per (tile, token chunk)
+  int64_t chunks = 0;
+  for (int mt = 0; mt < mtiles; ++mt) {
+    const int64_t rows = ml - (int64_t)mt * C::MTR < C::MTR ? ml - (int64_t)mt * C::MTR : C::MTR;
+    chunks += (rows + EPI_ROWS - 1) / EPI_ROWS;
   }
   TcArgs a;
   a.nib = W->nib;
@@ -665,7 +656,7 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.e.counters = ws.counters;
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
-  a.e.tiles = (int)(W->tiles * mtiles);
+  a.e.tiles = (int)(W->tiles * chunks);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)mtiles, (unsigned)W->tiles, (unsigned)plan.splits);
@@ -687,10 +678,13 @@ bool tc_kernel_built() { return true; }
 
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   TcPlan p;
-  p.m_tile = nb_for(M < TC_M_LAUNCH ? M : TC_M_LAUNCH, batch_invariant);
-  // K partition from N and K only: fill the SMs with one CTA each, balancing
-  // waves against units per CTA (+ a fixed per-CTA cost in unit terms).
-  const int64_t tiles = W->tiles;
+  const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
+  p.m_tile = nb_for(ml, batch_invariant);
+  const int64_t mtiles = (ml + p.m_tile / 3 - 1) / (p.m_tile / 3);
+  // K partition: fill the SMs, balancing waves against units per CTA (+ a
+  // fixed per-CTA cost in unit terms).  It depends on M through the token
+  // tiles, except in batch-invariant mode (one token tile of 32 rows assumed).
+  const int64_t tiles = W->tiles * (batch_invariant ? 1 : mtiles);
   int64_t best_s = 1, best_cost = -1;
   const int64_t smax = W->KBP < 64 ? W->KBP : 64;
   for (int64_t s = 1; s <= smax; ++s) {
@@ -728,9 +722,14 @@ int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx
               const TcPlan& plan, const Workspace& ws, cudaStream_t s) {
   for (int64_t mb = 0; mb < M; mb += TC_M_LAUNCH) {
     const int64_t ml = (M - mb) < TC_M_LAUNCH ? (M - mb) : TC_M_LAUNCH;
-    const int st = plan.m_tile == 16
-                       ? launch_nb<16>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s)
-                       : launch_nb<32>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s);
+    int st;
+    switch (plan.m_tile) {
+      case 48: st = launch_nb<48>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+      case 96: st = launch_nb<96>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+      case 144: st = launch_nb<144>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+      case 192: st = launch_nb<192>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+      default: st = launch_nb<240>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+    }
     if (st) return st;
   }
   return Q4_OK;
