@@ -43,9 +43,10 @@ BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
 # DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
 # hash of the kernel source it was taken on (null once the kernel changes).
 TRAFFIC = {
-    "source_hash": "938737a0525490c3",
+    "source_hash": "97451952e3f0b9d6",
     "grouped": True,
-    "bytes_per_launch": 32937611,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
+    "m_sweep": [1, 2, 3, 4, 5, 8],
+    "bytes_per_launch": 32961715,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
     "capture": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                "--clock-control none -k regex:mma_kernel -s 96 -c 96 python bench.py --layers 4 "
                "--steps 2 --warmup 3 --no-cpu-baseline (one step: 4 layers x 4 calls x 6 M)",
@@ -69,13 +70,18 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# the sources the streaming kernel (mma_kernel) is compiled from
+TRAFFIC_SOURCES = ("bit_quantized_matmul_gb300/csrc/q4mm_mma.cu",
+                   "bit_quantized_matmul_gb300/csrc/q4mm_epilogue.cuh",
+                   "bit_quantized_matmul_gb300/csrc/q4mm_internal.h",
+                   "include/q4mm.h")
+
+
 def _kernel_source_hash():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "bit_quantized_matmul_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -225,6 +231,7 @@ def run_gpu(args):
     import bit_quantized_matmul_gb300 as q4
     import synthetic
 
+    msw = tuple(args.m_sweep)
     world, rank, local = _dist()
     if world > 1:
         import torch.distributed as dist
@@ -238,11 +245,11 @@ def run_gpu(args):
 
     # activations: x for K=3584 inputs and K=18944 (down_proj) per M
     xs = {}
-    for M in M_SWEEP:
+    for M in msw:
         for K in (3584, 18944):
             xs[(M, K)] = torch.from_numpy(synthetic.normal(synthetic.act_seed(1, M) + K, (M, K))).to(dev)
     ys = {}
-    for M in M_SWEEP:
+    for M in msw:
         for name in TYPES:
             N, _ = synthetic.QWEN7B_LINEARS[name]
             ys[(M, name)] = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -261,13 +268,13 @@ def run_gpu(args):
 
     # warm the library (scratch allocation) before capture
     with torch.cuda.stream(stream):
-        for M in M_SWEEP:
+        for M in msw:
             for gname, _ in groups:
                 issue(M, gname)
     torch.cuda.synchronize(dev)
 
     graphs = {}
-    for M in M_SWEEP:
+    for M in msw:
         for gname, _ in groups:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -277,7 +284,7 @@ def run_gpu(args):
 
     launches = {}
     launches_per_step = 0
-    for M in M_SWEEP:
+    for M in msw:
         for gname, names in groups:
             p, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M)
             if len(names) > 1 and p != q4.Q4MM_PATH_MMA:
@@ -287,7 +294,7 @@ def run_gpu(args):
 
     wbytes = {name: synthetic.QWEN7B_LINEARS[name][0] * synthetic.QWEN7B_LINEARS[name][1]
               * BLOCK_BYTES_PER_WEIGHT for name in TYPES}
-    step_wbytes = sum(wbytes[n] * layers for n in TYPES) * len(M_SWEEP)
+    step_wbytes = sum(wbytes[n] * layers for n in TYPES) * len(msw)
 
     def algo_bytes(M, gname):
         """Bytes a call must move: packed weights once, x once, y once."""
@@ -298,7 +305,7 @@ def run_gpu(args):
     ev = {}
 
     def step(record):
-        for M in M_SWEEP:
+        for M in msw:
             for gname, _ in groups:
                 if record:
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -345,16 +352,17 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     # roofline over every launch of the step (one kernel function serves them all):
     # algorithmic bytes per call / event-timed duration per call
-    tot_bytes = sum(algo_bytes(M, g) for M in M_SWEEP for g, _ in groups)
-    tot_ms = sum(per[(M, g)] for M in M_SWEEP for g, _ in groups)
-    n_launch = sum(launches[(M, g)] for M in M_SWEEP for g, _ in groups)
+    tot_bytes = sum(algo_bytes(M, g) for M in msw for g, _ in groups)
+    tot_ms = sum(per[(M, g)] for M in msw for g, _ in groups)
+    n_launch = sum(launches[(M, g)] for M in msw for g, _ in groups)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     traffic = None
     if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash() and \
-            TRAFFIC.get("grouped") == (not args.separate):
+            TRAFFIC.get("grouped") == (not args.separate) and \
+            TRAFFIC.get("m_sweep", list(M_SWEEP)) == list(msw):
         traffic = TRAFFIC.get("bytes_per_launch")
     per_m = {}
-    for M in M_SWEEP:
+    for M in msw:
         t = sum(per[(M, g)] * layers for g, _ in groups)
         b = sum(wbytes[n] * layers for n in TYPES)
         per_m[str(M)] = {
@@ -366,12 +374,12 @@ def run_gpu(args):
 
     # ---- end to end through the public API: pinned host x in, host y out ----
     pin_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    out_host = {M: torch.empty((M, 3584), dtype=torch.float32).pin_memory() for M in M_SWEEP}
+    out_host = {M: torch.empty((M, 3584), dtype=torch.float32).pin_memory() for M in msw}
     h2d = sum(v.numel() * 4 for v in pin_x.values())
     d2h = sum(v.numel() * 4 for v in out_host.values())
 
     def e2e_step():
-        for M in M_SWEEP:
+        for M in msw:
             xs[(M, 3584)].copy_(pin_x[(M, 3584)], non_blocking=True)
             xs[(M, 18944)].copy_(pin_x[(M, 18944)], non_blocking=True)
             for gname, _ in groups:
@@ -395,7 +403,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(layers=1)
+        cpu = cpu_oracle_sample(layers=1, Ms=msw)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if world > 1:
@@ -406,20 +414,23 @@ def run_gpu(args):
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": layers, "M_sweep": list(M_SWEEP),
+            "config": {"workload": WORKLOAD if msw == M_SWEEP else
+                       WORKLOAD.replace("M sweep 1,2,3,4,5,8", "M sweep " + ",".join(map(str, msw))),
+                       "layers": layers, "M_sweep": list(msw),
                        "weights": "Q4_0 (18 B per 32 weights), N(0,0.02^2)", "activations": "fp32 N(0,1)",
                        "l2": "inputs larger than L2 (%.2f GB packed weight stack, streamed once per M)"
                              % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "calls_per_layer": [g for g, _ in groups],
                        "m_threshold": q4.q4mm_get_m_threshold()},
-            "token_rows_per_s": sum(M_SWEEP) * world / (ms_per_step * 1e-3),
+            "token_rows_per_s": sum(msw) * world / (ms_per_step * 1e-3),
             "per_M": per_m,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "kernel": "mma_kernel, every launch of one step (%d launches)" % (n_launch * layers),
+                         "kernel": "q4mm kernels (mma_kernel below the M threshold, xop_kernel + tc_kernel "
+                                   "from it), every launch of one step (%d launches)" % (n_launch * layers),
                          "algorithmic_bytes_per_launch": tot_bytes / n_launch,
                          "algorithmic_bytes_rule": "0.5625*sum(N_i*K) + 4*M*K + 4*M*sum(N_i) per call"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -512,6 +523,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--m-sweep", type=lambda v: [int(t) for t in v.split(",")], default=list(M_SWEEP),
+                    help="token-row counts of the step (default 1,2,3,4,5,8)")
     ap.add_argument("--separate", action="store_true",
                     help="one call per linear instead of grouping q/k/v and gate/up")
     ap.add_argument("--path-sweep", action="store_true",

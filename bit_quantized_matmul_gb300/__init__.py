@@ -33,7 +33,7 @@ Q4MM_ROW_BY_ROW = 0x8
 Q4MM_FORCE_MMA = 0x10
 Q4MM_M_MAX = 4096
 Q4MM_GROUP_MAX = 4
-Q4MM_NOALLOC_PARTIAL_BYTES = 614400
+Q4MM_NOALLOC_PARTIAL_BYTES = 1228800
 Q4MM_PATH_SIMT = 1
 Q4MM_PATH_TC = 2
 Q4MM_PATH_ROW_BY_ROW = 3

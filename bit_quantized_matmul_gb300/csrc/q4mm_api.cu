@@ -191,6 +191,9 @@ int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace*
       cudaGetLastError();
       return Q4_ERR_NOMEM;
     }
+    // idle partial-sum words are zero (q4mm_epilogue.cuh)
+    if (cudaMemset(ds.ws.partial, 0, want) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return Q4_ERR_CUDA;
     ds.ws.partial_bytes = want;
   }
   if (xop_bytes > ds.ws.xop_bytes) {

@@ -67,7 +67,7 @@ struct Workspace {
   unsigned int* counters = nullptr;    // split-K arrival counters, self-resetting
   unsigned long long* keys = nullptr;  // argmax keys [Q4MM_M_MAX], self-resetting
   unsigned int* argmax_done = nullptr; // argmax completion counter
-  float* partial = nullptr;            // split-K partial sums
+  unsigned long long* partial = nullptr;  // split-K partial sums (flagged words, zero when idle)
   size_t partial_bytes = 0;
   void* xop = nullptr;                 // tensor-core activation operand
   size_t xop_bytes = 0;

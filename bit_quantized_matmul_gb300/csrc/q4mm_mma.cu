@@ -35,6 +35,8 @@
 // order depends on M.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "q4mm_epilogue.cuh"
 #include "q4mm_internal.h"
 
@@ -52,6 +54,10 @@ constexpr int CHUNK_PAIRS = 8;              // block pairs per ring slot (512 k)
 constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 constexpr int NSLOT = 4;                    // ring depth (a power of two)
 constexpr int XSTAGES = 3;                  // converter staging slots (chunks in flight)
+// row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
+// the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
+// 32 different banks and the per-row reads stay consecutive
+constexpr int RED_LD = TILE_N + 4;
 
 // One weight of a launch.  A launch covers the tiles of up to MMA_GROUP_MAX
 // weights that share K and the activations (e.g. the q, k and v projections):
@@ -74,6 +80,7 @@ struct MmaArgs {
   int mrows;            // token rows in this launch
   int64_t kbp_per_split;
   unsigned int* status; // device status word (bounded-wait expiry)
+  int cluster;          // 1: the K splits of a tile are one thread-block cluster
   EpiArgs e;
 };
 
@@ -87,8 +94,11 @@ struct MmaCfg {
   // converter staging: per slot the chunk's raw fp32 x rows and its scales
   static constexpr int XSLOT = MAXM * CHUNK_K * 4 + CHUNK_PAIRS * PAIR_SCL_BYTES;
   static constexpr int XRAW_OFF = RING;
-  static constexpr int RED = SLICES * C * 8 * (TILE_N + 1) * 4;  // per-slice sums for the gather
-  static constexpr int BAR_OFF = RING + XSTAGES * XSLOT > RED ? RING + XSTAGES * XSLOT : RED;
+  static constexpr int RED = SLICES * C * 8 * RED_LD * 4;  // per-slice sums for the gather
+  static constexpr int XCH_OFF = (RED + 15) / 16 * 16;  // cluster split-K: this CTA's sums
+  static constexpr int XCH = MAXM * TILE_N * 4;           // [token row][tile row] fp32
+  static constexpr int BAR_OFF = RING + XSTAGES * XSLOT > XCH_OFF + XCH ? RING + XSTAGES * XSLOT
+                                                                       : XCH_OFF + XCH;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static constexpr int PREFETCH = 2;  // weight pairs in flight per warp (registers)
 };
@@ -150,6 +160,33 @@ __device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Thread-block cluster: barrier over every thread of every CTA of the cluster
+// (all of them are resident together), and reads of another CTA's shared
+// memory through the cluster window.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -225,6 +262,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ unsigned long long kred[4][MAXM];
   __shared__ int s_flag;
+  __shared__ unsigned s_arrival;  // split-K arrival word of this CTA
   __shared__ volatile int s_err;
 
   const int tid = threadIdx.x;
@@ -504,20 +542,27 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       }
       mbar_arrive(smem_u32(&bfull[slot]));
     }
+    // arrival number for the split-K epilogue, drawn once the last chunk is
+    // handed over: the compute warps still have up to a ring of chunks to go,
+    // which hides the atomic's latency, and CTAs draw in about the order they
+    // finish (the previous launch has reset the word)
+    if (ct == 0 && a.e.splits > 1 && !a.cluster) s_arrival = split_arrive(&a.e.counters[blockIdx.x]);
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after the previous kernel
   __syncthreads();
-  if (s_err) {
+  const bool failed = s_err != 0;
+  // a CTA of a cluster stays for the cluster barriers below whatever happened
+  if (failed && !a.cluster) {
     if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
     return;
   }
 
   // ---- gather: per tile row and MMA column, the four K slices ----
-  float* red = reinterpret_cast<float*>(smem);  // [SLICES][C*8][TILE_N + 1]
-  constexpr int RS = C * 8 * (TILE_N + 1);
+  float* red = reinterpret_cast<float*>(smem);  // [SLICES][C*8][RED_LD]
+  constexpr int RS = C * 8 * RED_LD;
   if (compute) {
     const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
@@ -533,37 +578,111 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           } else {
             v = accf[r][cg][e];
           }
-          red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * (TILE_N + 1) + (2 * rgp + r) * 16 + g +
+          red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RED_LD + (2 * rgp + r) * 16 + g +
               8 * (e >> 1)] = v;
         }
   }
   __syncthreads();
 
-  const int row = tid < TILE_N ? tid : -1;
-  float val[MAXM];
+  // all threads take part from here: thread tid owns tile row tid % 128 for
+  // the token rows tid / 128 + 5k, so the split-K reads of the last CTA are
+  // spread over the whole CTA and issued in a single round
+  constexpr int MGROUPS = KERNEL_THREADS / TILE_N;
+  constexpr int MT = (MAXM + MGROUPS - 1) / MGROUPS;
+  static_assert(KERNEL_THREADS % TILE_N == 0, "whole groups of tile rows");
+  const int row = tid % TILE_N, mfirst = tid / TILE_N;
+  float val[MT];
 #pragma unroll
-  for (int m = 0; m < MAXM; ++m) val[m] = 0.0f;
-  if (row >= 0) {
+  for (int k = 0; k < MT; ++k) {
+    const int m = mfirst + k * MGROUPS;
+    val[k] = 0.0f;
+    if (m < mrows) {
+      const int c0 = DENSE ? 3 * m : 8 * m;
+      float v = 0.0f;
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-      if (m < mrows) {
-        const int c0 = DENSE ? 3 * m : 8 * m;
-        float v = 0.0f;
+      for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each slice 0..3
 #pragma unroll
-        for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each slice 0..3
-#pragma unroll
-          for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * (TILE_N + 1) + row];
-        val[m] = v;
-      }
+        for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * RED_LD + row];
+      val[k] = v;
     }
   }
+  if (a.cluster) {
+    // K splits of this tile = the CTAs of this cluster, rank = split.  Each
+    // CTA publishes its sums in its own shared memory; after the cluster
+    // barrier CTA r adds up the r-th share of the tile's outputs, reading the
+    // splits' sums in ascending split order (the same order and operations as
+    // the global-memory path), then a second barrier keeps every CTA's shared
+    // memory alive until its peers have read it.
+    float* xch = reinterpret_cast<float*>(smem + S::XCH_OFF);
+#pragma unroll
+    for (int k = 0; k < MT; ++k) {
+      const int m = mfirst + k * MGROUPS;
+      if (m < mrows) xch[m * TILE_N + row] = val[k];
+    }
+    const uint32_t nsplit = (uint32_t)a.e.splits;
+    const bool layout_ok = cluster_rank() == (uint32_t)split && cluster_size() == nsplit;
+    cluster_sync_all();
+    if (!failed && layout_ok) {
+      float* y = a.w[wi].y;
+      const int64_t N = a.w[wi].N;
+      const int outs = mrows * TILE_N;
+      const int per = (outs + (int)nsplit - 1) / (int)nsplit;
+      const int o_end = min(outs, (split + 1) * per);
+      const uint32_t xa = smem_u32(xch);
+      for (int o = split * per + tid; o < o_end; o += KERNEL_THREADS) {
+        float t[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          t[s] = s < (int)nsplit ? ld_cluster(cluster_map(xa + 4u * (uint32_t)o, (uint32_t)s)) : 0.0f;
+        float v = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          if (s < (int)nsplit) v += t[s];
+        const int64_t n = tile * TILE_N + (o % TILE_N);
+        if (n < N) y[(int64_t)(o / TILE_N) * N + n] = v;
+      }
+    }
+    cluster_sync_all();
+    if ((failed || !layout_ok) && tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
+    return;
+  }
+
   // this weight's outputs; partial sums and counters indexed by the global tile
   EpiArgs e = a.e;
   e.y = a.w[wi].y;
   e.N = a.w[wi].N;
   e.partial = a.e.partial + (int64_t)a.w[wi].tile_start * TILE_N;
-  finish_tile<MAXM>(e, val, row, tile, 0, mrows, split, (int)blockIdx.x, &s_flag, kred,
-                    []() { __syncthreads(); });
+  finish_tile<MT, MGROUPS, MAXM>(e, val, row, mfirst, tile, 0, mrows, split, s_arrival,
+                                 (int)blockIdx.x, &s_flag, kred, []() { __syncthreads(); });
+}
+
+// Clusters of `size` CTAs of this kernel that the device holds at once (0 if
+// none or unknown), per device, cached.
+template <int C, bool DENSE>
+int cluster_capacity(int device, int size) {
+  static std::atomic<int> cache[64][9];  // value + 1; 0 = not yet asked
+  if (size < 2 || size > 8) return 0;
+  std::atomic<int>& slot = cache[device & 63][size];
+  const int c = slot.load();
+  if (c > 0) return c - 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, (unsigned)size, 1);
+  cfg.blockDim = dim3(KERNEL_THREADS);
+  cfg.dynamicSmemBytes = MmaCfg<C>::BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)size;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  slot.store(n + 1);
+  return n;
 }
 
 template <int C, bool DENSE>
@@ -606,6 +725,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.e.splits = plan.splits;
   a.e.partial = ws.partial;
   a.e.counters = ws.counters;
+  a.e.status = ws.status;
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
   a.e.tiles = tiles;
@@ -616,16 +736,28 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63] = true;
   }
+  // Split-K through distributed shared memory when the K splits of every tile
+  // fit in one cluster of at most 4 CTAs and all the launch's clusters are
+  // resident at once; otherwise (and for the greedy pick) through global
+  // memory.  Both add the splits in the same order.  (Measured on GB300 for
+  // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
+  // clusters of 5 lost to it.)
+  a.cluster = plan.splits > 1 && plan.splits <= 4 && idx == nullptr &&
+              tiles <= cluster_capacity<C, DENSE>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles, (unsigned)plan.splits, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = (unsigned)plan.splits;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.cluster ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
@@ -645,6 +777,7 @@ MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms) {
   if (cap < 1) cap = 1;
   if (sp < 1) sp = 1;
   if (sp > cap) sp = cap;
+  if (sp > MAX_SPLITS) sp = MAX_SPLITS;  // the arrival count field of the epilogue
   p.kbp_per_split = (KBP + sp - 1) / sp;
   p.splits = (int)((KBP + p.kbp_per_split - 1) / p.kbp_per_split);
   return p;
@@ -656,7 +789,7 @@ size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool 
   if (p.splits <= 1) return 0;
   const int64_t rpl = rows_per_launch(batch_invariant);
   const int64_t ml = M < rpl ? M : rpl;
-  return (size_t)p.splits * (size_t)ml * (size_t)(tiles * TILE_N) * sizeof(float);
+  return (size_t)p.splits * (size_t)ml * (size_t)(tiles * TILE_N) * sizeof(unsigned long long);
 }
 
 size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant) {

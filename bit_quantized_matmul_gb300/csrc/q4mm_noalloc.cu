@@ -32,7 +32,6 @@ constexpr int NA_COUNTERS = 4096;
 constexpr size_t NA_COUNTER_OFF = NA_HEAD;
 constexpr size_t NA_KEYS_OFF = NA_COUNTER_OFF + NA_COUNTERS * sizeof(unsigned);
 constexpr size_t NA_PARTIAL_OFF = NA_KEYS_OFF + Q4MM_M_MAX * sizeof(unsigned long long);
-constexpr size_t NA_ZEROED = NA_PARTIAL_OFF;  // everything before the partials starts at zero
 constexpr size_t NA_TOTAL = NA_PARTIAL_OFF + Q4MM_NOALLOC_PARTIAL_BYTES;
 static_assert(NA_PARTIAL_OFF % 256 == 0, "partial sums must stay 256-byte aligned");
 
@@ -49,8 +48,9 @@ struct NoAllocDevice {
 NoAllocDevice g_na[NA_MAX_DEVICES];
 
 // Once per device, with that device current: find the array's address, read
-// the SM count the K partition depends on, and clear the words that must
-// start at zero (the counters reset themselves after every launch).
+// the SM count the K partition depends on, and clear the array: counters,
+// keys and partial-sum words start at zero (and every launch leaves them so,
+// up to the counters' epochs).
 int setup_locked(int dev, NoAllocDevice& d) {
   if (d.ready) return Q4_OK;
   void* p = nullptr;
@@ -61,7 +61,7 @@ int setup_locked(int dev, NoAllocDevice& d) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return Q4_ERR_CUDA;
-  if (cudaMemset(p, 0, NA_ZEROED) != cudaSuccess) return Q4_ERR_CUDA;
+  if (cudaMemset(p, 0, NA_TOTAL) != cudaSuccess) return Q4_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
   d.base = static_cast<unsigned char*>(p);
   d.num_sms = sms;
@@ -106,7 +106,7 @@ extern "C" int q4mm_forward_noalloc(const q4_weight* Wh, const float* x, float* 
   ws.argmax_done = reinterpret_cast<unsigned*>(d.base + 4);
   ws.counters = reinterpret_cast<unsigned*>(d.base + NA_COUNTER_OFF);
   ws.keys = reinterpret_cast<unsigned long long*>(d.base + NA_KEYS_OFF);
-  ws.partial = reinterpret_cast<float*>(d.base + NA_PARTIAL_OFF);
+  ws.partial = reinterpret_cast<unsigned long long*>(d.base + NA_PARTIAL_OFF);
   ws.partial_bytes = Q4MM_NOALLOC_PARTIAL_BYTES;
   ws.xop = nullptr;
   ws.xop_bytes = 0;

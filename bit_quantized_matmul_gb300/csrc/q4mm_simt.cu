@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_kernel(const SimtArgs a) {
   __shared__ float red[MT][TILE_N];
   __shared__ unsigned long long kred[4][MT];
   __shared__ int s_flag;
+  __shared__ unsigned s_arrival;  // split-K arrival word of this CTA
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
@@ -75,6 +76,9 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_kernel(const SimtArgs a) {
   const uint4* nibp = a.nib + ((tile * a.KBP) * 8 + rg) * 32 + lane;
   const uint2* sclp = a.scl + ((tile * a.KBP) * 8 + rg) * 8 + g;
   const int64_t kmax = a.K;
+  // arrival number for the split-K epilogue (stream order: the previous
+  // launch has reset the word); the barrier before the epilogue publishes it
+  if (threadIdx.x == 0 && a.e.splits > 1) s_arrival = split_arrive(&a.e.counters[tile]);
 
   float acc0[MT], acc1[MT];  // rows R0 = 16rg + g and R1 = R0 + 8
 #pragma unroll
@@ -152,8 +156,8 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_kernel(const SimtArgs a) {
   float val[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) val[m] = row >= 0 ? red[m][row] : 0.0f;
-  finish_tile<MT>(a.e, val, row, tile, 0, a.mrows, split, (int)tile, &s_flag, kred,
-                  []() { __syncthreads(); });
+  finish_tile<MT, 1, MT>(a.e, val, row, 0, tile, 0, a.mrows, split, s_arrival, (int)tile, &s_flag,
+                         kred, []() { __syncthreads(); });
 }
 
 constexpr int64_t SIMT_M_LAUNCH = 8;  // token rows per launch
@@ -165,7 +169,7 @@ MmaPlan simt_plan(const Weight* W, int num_sms) { return mma_plan(W, num_sms); }
 size_t simt_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M) {
   if (p.splits <= 1) return 0;
   const int64_t ml = M < SIMT_M_LAUNCH ? M : SIMT_M_LAUNCH;
-  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(float);
+  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(unsigned long long);
 }
 
 int simt_launch_count(int64_t M) { return (int)((M + SIMT_M_LAUNCH - 1) / SIMT_M_LAUNCH); }
@@ -192,6 +196,7 @@ int launch_simt(const Weight* W, const float* x, int64_t M, float* y, int32_t* i
     a.e.splits = plan.splits;
     a.e.partial = ws.partial;
     a.e.counters = ws.counters;
+    a.e.status = ws.status;
     a.e.keys = ws.keys + mb;
     a.e.argmax_done = ws.argmax_done;
     a.e.tiles = (int)W->tiles;

@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
   volatile int* err = reinterpret_cast<volatile int*>(tmem_slot + 2);
   __shared__ int s_last;
+  __shared__ unsigned s_arrival;  // split-K arrival word of this CTA
   __shared__ unsigned long long red[4][EPI_ROWS];  // greedy-pick scratch of the epilogue
 
   const int tid = threadIdx.x;
@@ -434,6 +435,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         bulk_g2s(sb + C::BOP_OFF, bop_base + (int64_t)u * U * C::BOP_BLOCK, ub * C::BOP_BLOCK, fb);
         last = u;
       }
+      // arrival number for the split-K epilogue, drawn once every copy is
+      // issued, so that its latency hides behind the last units (earlier
+      // launches reset the word)
+      if (a.e.splits > 1) s_arrival = split_arrive(&a.e.counters[tile * a.mtiles + mt]);
       // drain: every copy this producer issued has landed before the CTA exits
       for (int u = last; u >= 0 && u > last - C::NST; --u)
         mbar_drain(smem_u32(&full[u % NBR]), (u / NBR) & 1);
@@ -567,10 +572,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
       const int row = warp * 32 + lane;
       const uint32_t drow = d_base + ((uint32_t)(warp * 32) << 16);
       asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after earlier kernels
+      const unsigned arrival = s_arrival;
+      const int nchunk = (mcount + EPI_ROWS - 1) / EPI_ROWS;  // the same for every split
 #pragma unroll 1
-      for (int c = 0; c < C::CHUNKS; ++c) {
+      for (int c = 0; c < nchunk; ++c) {
         const int c0 = c * EPI_ROWS;
-        if (c0 >= mcount) break;  // the same for every split of this tile
         float t0[16], t1[16], t2[16], val[EPI_ROWS];
         tmem_ld16(drow + (uint32_t)c0, t0);
         tmem_ld16(drow + (uint32_t)(MTR + c0), t1);
@@ -578,9 +584,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < EPI_ROWS; ++j) val[j] = (t0[j] + t1[j]) + t2[j];
-        finish_tile<EPI_ROWS>(a.e, val, row, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split,
-                              (tile * a.mtiles + mt) * C::CHUNKS + c, &s_last, red,
-                              []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
+        finish_tile<EPI_ROWS, 1, EPI_ROWS>(
+            a.e, val, row, 0, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split, arrival,
+            c == nchunk - 1 ? tile * a.mtiles + mt : -1, &s_last, red,
+            []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
       }
     }
   }
@@ -615,7 +622,7 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   using C = Cfg<NB>;
   const int mtiles = (int)((ml + C::MTR - 1) / C::MTR);
   const int64_t KB2 = 2 * W->KBP;
-  if (plan.splits > 1 && W->tiles * mtiles * C::CHUNKS > MAX_COUNTERS) return Q4_ERR_SHAPE;
+  if (plan.splits > 1 && W->tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   {
     const int64_t total = (int64_t)mtiles * KB2 * 4 * C::MTR;
     const int64_t want = (total + 255) / 256;
@@ -654,6 +661,7 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.e.splits = plan.splits;
   a.e.partial = ws.partial;
   a.e.counters = ws.counters;
+  a.e.status = ws.status;
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
   a.e.tiles = (int)(W->tiles * chunks);
@@ -685,8 +693,13 @@ TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   // fixed per-CTA cost in unit terms).  It depends on M through the token
   // tiles, except in batch-invariant mode (one token tile of 32 rows assumed).
   const int64_t tiles = W->tiles * (batch_invariant ? 1 : mtiles);
+  // at least 16 blocks (four units) per split: the split-K epilogue runs once
+  // per 16 token rows of every CTA, so very short K ranges cost more than
+  // they save
   int64_t best_s = 1, best_cost = -1;
-  const int64_t smax = W->KBP < 64 ? W->KBP : 64;
+  int64_t smax = W->KBP / 8;
+  if (smax < 1) smax = 1;
+  if (smax > 64) smax = 64;
   for (int64_t s = 1; s <= smax; ++s) {
     const int64_t kbps = (W->KBP + s - 1) / s;  // block pairs per split
     const int64_t waves = (tiles * s + num_sms - 1) / num_sms;
@@ -704,7 +717,7 @@ TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
 size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M) {
   if (p.splits <= 1) return 0;
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
-  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(float);
+  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(unsigned long long);
 }
 
 size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) {

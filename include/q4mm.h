@@ -176,8 +176,8 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
 Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
                               int64_t M, uint32_t flags, cudaStream_t stream);
 
-/* Capacity of the split-K partial sums of q4mm_forward_noalloc (600 KiB). */
-#define Q4MM_NOALLOC_PARTIAL_BYTES 614400
+/* Capacity of the split-K partial sums of q4mm_forward_noalloc (1200 KiB). */
+#define Q4MM_NOALLOC_PARTIAL_BYTES 1228800
 
 /* y = x @ W^T without allocating any device memory.  (The pages have no
  * counterpart: this is a library concern.)
@@ -187,7 +187,7 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * at that moment use this call instead: a serving process that gave all free
  * device memory to its own pool (the allocation would fail), or a step that
  * must not wait for the whole device, as cudaFree does.  Its scratch is one
- * fixed device array in the library (about 0.65 MB per device, created when the
+ * fixed device array in the library (about 1.3 MB per device, created when the
  * library's device code is loaded), so this call allocates nothing.  (As for
  * any CUDA library, the runtime may still load kernel code on first use.)
  *
@@ -195,7 +195,7 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * Always runs the streaming mma.sync kernel with its usual K partition: the
  * results are bit-identical to q4mm_forward_ex(W, x, y, M, Q4MM_FORCE_MMA).
  * Returns Q4_ERR_SHAPE, before any launch, if the call's split-K partial
- * sums (splits x min(M, 8) x N rounded up to 128 x 4 bytes) exceed
+ * sums (splits x min(M, 8) x N rounded up to 128 x 8 bytes) exceed
  * Q4MM_NOALLOC_PARTIAL_BYTES.  On a 152-SM GB300 every linear layer of a
  * 7B decoder (N, K up to 18944) fits at any M; q4mm_forward has no such limit.
  *
