@@ -130,7 +130,8 @@ int launch_simt(const Weight* W, const float* x, int64_t M, float* y, int32_t* i
 struct TcPlan {
   int splits;
   int64_t kbp_per_split;  // block pairs per split
-  int m_tile;             // MMA N (16 or 32)
+  int m_tile;             // MMA N (3 x token rows per CTA)
+  int num_sms;            // SMs of the device (one CTA per SM)
 };
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant);
 size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M);

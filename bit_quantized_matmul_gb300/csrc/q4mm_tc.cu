@@ -76,11 +76,11 @@ struct Cfg {
   static constexpr int NST_RAW = (SMEM_BUDGET - BAR_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_RAW > 8 ? 8 : NST_RAW;
   static constexpr int SMEM_BYTES = NST * STAGE_BYTES + BAR_BYTES;
-  static constexpr int CHUNKS = MTR / EPI_ROWS;
   static_assert(MTR % EPI_ROWS == 0 && 3 * MTR == NB, "token tile");
   static_assert(NA * A_UNIT_COLS + NB <= TMEM_COLS, "TMEM budget");
   static_assert(NA >= 2 && NST >= 2, "pipeline too shallow");
   static_assert(NBR % 2 == 0 && NBR > 2 * (NST + NA), "barrier ring depth");
+  static_assert(NST * STAGE_BYTES >= MTR * TILE_N * 4, "epilogue sums fit over the stages");
 };
 
 struct TcArgs {
@@ -90,6 +90,7 @@ struct TcArgs {
   int64_t KBP, KB2;    // block pairs, padded blocks (2 * KBP)
   int64_t kbp_per_split;
   int mtiles;
+  int rs;              // 1: split-K by reduce-scatter (every CTA of the launch resident at once)
   unsigned int* status;
   EpiArgs e;
 };
@@ -379,9 +380,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   uint64_t* dfull = afree + NBR;   // every MMA of the CTA done: commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
   volatile int* err = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  __shared__ int s_last;
+  __shared__ int s_last[2];
   __shared__ unsigned s_arrival;  // split-K arrival word of this CTA
-  __shared__ unsigned long long red[4][EPI_ROWS];  // greedy-pick scratch of the epilogue
+  __shared__ unsigned long long red[2][4][EPI_ROWS];  // greedy-pick scratch of the epilogue
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -435,10 +436,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         bulk_g2s(sb + C::BOP_OFF, bop_base + (int64_t)u * U * C::BOP_BLOCK, ub * C::BOP_BLOCK, fb);
         last = u;
       }
-      // arrival number for the split-K epilogue, drawn once every copy is
-      // issued, so that its latency hides behind the last units (earlier
-      // launches reset the word)
-      if (a.e.splits > 1) s_arrival = split_arrive(&a.e.counters[tile * a.mtiles + mt]);
       // drain: every copy this producer issued has landed before the CTA exits
       for (int u = last; u >= 0 && u > last - C::NST; --u)
         mbar_drain(smem_u32(&full[u % NBR]), (u / NBR) & 1);
@@ -550,44 +547,158 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     }
   }
 
-  // ---- epilogue: warps 0-3 read the accumulator once ----
+  // ---- epilogue: warps 0-7 read the accumulator once.  Warps w and w + 4
+  // reach the same TMEM lanes (32 (w % 4) ...); quad q = w / 4 takes the
+  // chunks of 16 token rows c = q, q + 2, ... ----
   tc_fence_before();
   __syncthreads();
   const bool skip = *err != 0;
   __syncthreads();  // every thread has read the flag before the epilogue can raise it
-  if (warp < 4 && !skip) {
+  if (warp < 8 && !skip) {
     const bool ok = mbar_wait(smem_u32(dfull), 0, err);
     // every epilogue thread takes the same decision
     uint32_t any_bad;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.eq.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(any_bad)
         : "r"((uint32_t)ok)
         : "memory");
     if (!any_bad) {
       tc_fence_after();
-      const int row = warp * 32 + lane;
-      const uint32_t drow = d_base + ((uint32_t)(warp * 32) << 16);
+      const int quad = warp >> 2;
+      const int row = (warp & 3) * 32 + lane;
+      const uint32_t drow = d_base + ((uint32_t)((warp & 3) * 32) << 16);
       asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and scratch: after earlier kernels
+      if (a.e.splits > 1 && !a.rs) {
+        // last-CTA exchange: the arrival is drawn once the accumulator is
+        // complete, so the CTA that draws last is the last to finish and its
+        // peers' partial sums are already on their way
+        if (warp == 0 && lane == 0) s_arrival = split_arrive(&a.e.counters[tile * a.mtiles + mt]);
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+      }
       const unsigned arrival = s_arrival;
       const int nchunk = (mcount + EPI_ROWS - 1) / EPI_ROWS;  // the same for every split
+      if (a.rs) {
+        // Reduce-scatter: CTA `split` owns tile rows [r0, r1) of every token
+        // row.  Each CTA keeps all its sums in shared memory and stores the
+        // other CTAs' rows to global memory (64-bit words with a zero high
+        // half, which no flagged reader accepts); then the tile's CTAs meet at
+        // a barrier on the tile's arrival word, and each adds up its own rows
+        // over the splits in ascending order (the order of every other path).
+        // All CTAs of the launch are resident together, so the barrier
+        // completes; one thread per CTA polls the word, with back-off.
+        float* xch = reinterpret_cast<float*>(stages);  // [MTR][TILE_N]; the stages are dead
+        const int S = a.e.splits;
+        const int r0 = split * TILE_N / S, r1 = (split + 1) * TILE_N / S;
+        const int64_t sstride = a.e.M * a.e.N_pad;
+        unsigned long long* part = a.e.partial + m0 * a.e.N_pad + (int64_t)tile * TILE_N;
+        const bool mine = row >= r0 && row < r1;
 #pragma unroll 1
-      for (int c = 0; c < nchunk; ++c) {
-        const int c0 = c * EPI_ROWS;
-        float t0[16], t1[16], t2[16], val[EPI_ROWS];
-        tmem_ld16(drow + (uint32_t)c0, t0);
-        tmem_ld16(drow + (uint32_t)(MTR + c0), t1);
-        tmem_ld16(drow + (uint32_t)(2 * MTR + c0), t2);
-        tmem_wait_ld();
+        for (int c = quad; c < nchunk; c += 2) {
+          const int c0 = c * EPI_ROWS;
+          float t0[16], t1[16], t2[16];
+          tmem_ld16(drow + (uint32_t)c0, t0);
+          tmem_ld16(drow + (uint32_t)(MTR + c0), t1);
+          tmem_ld16(drow + (uint32_t)(2 * MTR + c0), t2);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < EPI_ROWS; ++j) val[j] = (t0[j] + t1[j]) + t2[j];
-        finish_tile<EPI_ROWS, 1, EPI_ROWS>(
-            a.e, val, row, 0, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split, arrival,
-            c == nchunk - 1 ? tile * a.mtiles + mt : -1, &s_last, red,
-            []() { asm volatile("bar.sync 1, 128;" ::: "memory"); });
+          for (int j = 0; j < EPI_ROWS; ++j) {
+            const int m = c0 + j;
+            if (m < mcount) {
+              const float v = (t0[j] + t1[j]) + t2[j];
+              xch[m * TILE_N + row] = v;
+              if (!mine)
+                __stcg(part + (int64_t)split * sstride + (int64_t)m * a.e.N_pad + row,
+                       (unsigned long long)__float_as_uint(v));
+            }
+          }
+        }
+        __threadfence();  // this CTA's stores before its arrival
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        const int et = warp * 32 + lane;  // 0..255
+        if (et == 0) {
+          unsigned* ctr = &a.e.counters[tile * a.mtiles + mt];
+          const unsigned w = split_arrive(ctr);
+          if (arrival_last(w, S)) {
+            __threadfence();  // every peer's stores are visible before the epoch moves on
+            atomicExch(ctr, arrival_next(w));  // the others see the epoch move on
+          } else {
+            const unsigned ep = w >> ARRIVAL_BITS;
+            unsigned long long t_start = 0;
+            for (uint32_t n = 1;; ++n) {
+              unsigned cur;
+              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(ctr) : "memory");
+              if ((cur >> ARRIVAL_BITS) != ep) break;
+              __nanosleep(100);
+              if ((n & 63u) == 0u) {
+                const unsigned long long now = globaltimer();
+                if (t_start == 0) t_start = now;
+                else if (now - t_start > WAIT_NS) {
+                  atomicOr(a.e.status, STATUS_TIMEOUT);
+                  break;
+                }
+              }
+            }
+          }
+          __threadfence();
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");  // every peer's rows are visible
+        // own rows: OB outputs per thread at a time, every split of them read
+        // before anything is added or stored
+        const int rows = r1 - r0, outs = rows * mcount;
+        constexpr int OB = 4, SB = 8;
+        for (int ob = et; ob < outs; ob += 256 * OB) {
+          float acc[OB];
+#pragma unroll
+          for (int q = 0; q < OB; ++q) acc[q] = 0.0f;
+          for (int s0 = 0; s0 < S; s0 += SB) {
+            float t[OB][SB];
+#pragma unroll
+            for (int q = 0; q < OB; ++q) {
+              const int o = ob + 256 * q;
+              const int m = o / rows, r = r0 + o % rows;
+#pragma unroll
+              for (int j = 0; j < SB; ++j) {
+                const int sj = s0 + j;
+                t[q][j] = 0.0f;
+                if (o < outs && sj < S)
+                  t[q][j] = sj == split ? xch[m * TILE_N + r]
+                                        : __uint_as_float((uint32_t)__ldcg(
+                                              part + (int64_t)sj * sstride + (int64_t)m * a.e.N_pad + r));
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < OB; ++q)
+#pragma unroll
+              for (int j = 0; j < SB; ++j)
+                if (s0 + j < S) acc[q] += t[q][j];
+          }
+#pragma unroll
+          for (int q = 0; q < OB; ++q) {
+            const int o = ob + 256 * q;
+            const int64_t n = (int64_t)tile * TILE_N + r0 + o % rows;
+            if (o < outs && n < a.e.N) a.e.y[(m0 + o / rows) * a.e.N + n] = acc[q];
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = quad; c < nchunk; c += 2) {
+          const int c0 = c * EPI_ROWS;
+          float t0[16], t1[16], t2[16], val[EPI_ROWS];
+          tmem_ld16(drow + (uint32_t)c0, t0);
+          tmem_ld16(drow + (uint32_t)(MTR + c0), t1);
+          tmem_ld16(drow + (uint32_t)(2 * MTR + c0), t2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < EPI_ROWS; ++j) val[j] = (t0[j] + t1[j]) + t2[j];
+          finish_tile<EPI_ROWS, 1, EPI_ROWS>(
+              a.e, val, row, 0, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split, arrival,
+              c == 0 ? tile * a.mtiles + mt : -1, &s_last[quad], red[quad],
+              [quad]() { asm volatile("bar.sync %0, 128;" ::"r"(3 + quad) : "memory"); });
+        }
       }
     }
   }
@@ -665,6 +776,10 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
   a.e.tiles = (int)(W->tiles * chunks);
+  // reduce-scatter exchange when every CTA of the launch is resident at once
+  // (one CTA per SM), otherwise (and for the greedy pick) the last CTA of a
+  // tile adds up all its splits
+  a.rs = plan.splits > 1 && idx == nullptr && mtiles * W->tiles * plan.splits <= plan.num_sms;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)mtiles, (unsigned)W->tiles, (unsigned)plan.splits);
@@ -686,6 +801,7 @@ bool tc_kernel_built() { return true; }
 
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   TcPlan p;
+  p.num_sms = num_sms;
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
   p.m_tile = nb_for(ml, batch_invariant);
   const int64_t mtiles = (ml + p.m_tile / 3 - 1) / (p.m_tile / 3);
