@@ -286,9 +286,11 @@ def run_gpu(args):
     launches_per_step = 0
     for M in msw:
         for gname, names in groups:
-            p, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M)
-            if len(names) > 1 and p != q4.Q4MM_PATH_MMA:
-                l *= len(names)  # above the threshold a group runs one call per weight
+            if len(names) > 1 and M < q4.q4mm_get_group_m_threshold():
+                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M, q4.Q4MM_FORCE_MMA)  # one launch for the group
+            else:
+                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M)
+                l *= len(names)  # single calls, or one call per weight of a group
             launches[(M, gname)] = l
             launches_per_step += l * layers
 
@@ -422,7 +424,8 @@ def run_gpu(args):
                              % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "calls_per_layer": [g for g, _ in groups],
-                       "m_threshold": q4.q4mm_get_m_threshold()},
+                       "m_threshold": q4.q4mm_get_m_threshold(),
+                       "group_m_threshold": q4.q4mm_get_group_m_threshold()},
             "token_rows_per_s": sum(msw) * world / (ms_per_step * 1e-3),
             "per_M": per_m,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -461,9 +464,10 @@ def run_path_sweep(args):
     layers = args.layers
     stack = build_stack(q4, torch, dev, layers)
     stream = torch.cuda.Stream(dev)
-    sweep = (1, 2, 3, 4, 5, 6, 8, 16, 32, 64, 128, 256)
+    sweep = (1, 2, 3, 4, 5, 6, 8, 16, 24, 32, 48, 64, 128, 256)
     paths = {"simt": q4.Q4MM_FORCE_SIMT, "mma": q4.Q4MM_FORCE_MMA, "tc": q4.Q4MM_FORCE_TC}
     out = {}
+    groups_out = {}
     for M in sweep:
         xs = {K: torch.from_numpy(synthetic.normal(synthetic.act_seed(5, M) + K, (M, K))).to(dev)
               for K in (3584, 18944)}
@@ -494,6 +498,36 @@ def run_path_sweep(args):
                 out.setdefault(name, {}).setdefault(str(M), {})[pname] = {
                     "us": us, "weight_gbs": wb / us / 1e3, "rows_per_s": M / us * 1e6}
                 del g
+        # grouped calls on the streaming path (one launch for the group); on
+        # the tensor-core path a group is one call per weight
+        for gname, names in GROUPS:
+            if len(names) < 2:
+                continue
+            K = synthetic.QWEN7B_LINEARS[names[0]][1]
+            ys = [torch.empty((M, synthetic.QWEN7B_LINEARS[n][0]), dtype=torch.float32, device=dev)
+                  for n in names]
+
+            def issue_group():
+                for li in range(layers):
+                    q4.q4mm_forward_group([stack[n][li] for n in names], xs[K], ys=ys,
+                                          flags=q4.Q4MM_FORCE_MMA, stream=stream)
+            with torch.cuda.stream(stream):
+                issue_group()
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue_group()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(5):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            groups_out.setdefault(gname, {})[str(M)] = {"mma_group_us": a.elapsed_time(b) * 1e3 / (5 * layers)}
+            del g
     # threshold: smallest M of the sweep from which one decoder layer (q, o like
     # q_proj; k, v like k_proj; gate, up like gate_proj; down) takes no longer
     # on the tcgen05 path than on the streaming path, for every larger M too
@@ -507,8 +541,27 @@ def run_path_sweep(args):
         if all(layer_us(m, "tc") <= layer_us(m, "mma") for m in sweep[i:]):
             thr = M
             break
-    print(json.dumps({"path_sweep": out, "measured_threshold": thr, "layers": layers,
-                      "sweep": list(sweep)}), flush=True)
+    # grouped calls: q/k/v and gate/up as one streaming launch each, against
+    # one tensor-core call per weight (o and down are single calls either way)
+    like = {"q_proj": "q_proj", "k_proj": "k_proj", "v_proj": "k_proj", "gate_proj": "gate_proj",
+            "up_proj": "gate_proj"}
+    for gname, names in GROUPS:
+        if gname in groups_out:
+            for M in sweep:
+                groups_out[gname][str(M)]["tc_us"] = sum(out[like[n]][str(M)]["tc"]["us"] for n in names)
+
+    def group_layer(M, path):
+        key = "tc_us" if path == "tc" else "mma_group_us"
+        return sum(groups_out[g][str(M)][key] for g in groups_out)
+
+    gthr = None
+    for i, M in enumerate(sweep):
+        if all(group_layer(m, "tc") <= group_layer(m, "mma") for m in sweep[i:]):
+            gthr = M
+            break
+    print(json.dumps({"path_sweep": out, "measured_threshold": thr, "groups": groups_out,
+                      "measured_group_threshold": gthr, "layers": layers, "sweep": list(sweep)}),
+          flush=True)
     for name in TYPES:
         for W in stack[name]:
             W.free()

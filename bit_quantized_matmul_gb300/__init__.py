@@ -47,7 +47,8 @@ EXPORTS = (
     "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
     "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_argmax_rows", "q4_verify_greedy",
-    "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4_device_status",
+    "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4mm_set_group_m_threshold",
+    "q4mm_get_group_m_threshold", "q4_device_status",
     "q4_status_string",
 )
 
@@ -79,6 +80,8 @@ _sig = {
                        ctypes.POINTER(ctypes.c_int)],
     "q4mm_set_m_threshold": [_i64],
     "q4mm_get_m_threshold": [],
+    "q4mm_set_group_m_threshold": [_i64],
+    "q4mm_get_group_m_threshold": [],
     "q4_device_status": [],
     "q4_status_string": [ctypes.c_int],
 }
@@ -87,6 +90,7 @@ for _name, _args in _sig.items():
     _f.argtypes = _args
     _f.restype = ctypes.c_int
 _lib.q4mm_get_m_threshold.restype = ctypes.c_int64
+_lib.q4mm_get_group_m_threshold.restype = ctypes.c_int64
 _lib.q4_status_string.restype = ctypes.c_char_p
 
 
@@ -358,6 +362,14 @@ def q4mm_set_m_threshold(m: int):
 
 def q4mm_get_m_threshold() -> int:
     return int(_lib.q4mm_get_m_threshold())
+
+
+def q4mm_set_group_m_threshold(m: int):
+    _check(_lib.q4mm_set_group_m_threshold(int(m)), "q4mm_set_group_m_threshold")
+
+
+def q4mm_get_group_m_threshold() -> int:
+    return int(_lib.q4mm_get_group_m_threshold())
 
 
 def q4_device_status() -> int:

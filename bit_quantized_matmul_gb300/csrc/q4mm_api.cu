@@ -43,6 +43,13 @@ DeviceScratch g_dev[MAX_DEVICES];
 // for the whole layer up to M = 8, the tensor-core kernel from M = 16.
 constexpr int64_t DEFAULT_M_THRESHOLD = 16;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
+// Grouped calls (q4mm_forward_group) stay on the streaming kernel longer: there
+// one launch covers the whole group, while the tensor-core path runs once per
+// weight.  Measured the same way over a layer's q/k/v and gate/up groups: the
+// one streaming launch per group is faster up to M = 24, the per-weight
+// tensor-core calls from M = 32.
+constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 32;
+std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -386,7 +393,9 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
     st = init_device_locked(dev, ds);
     if (st) return st;
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
-    if (choose_path(ds, M, flags) == Q4MM_PATH_MMA) {
+    const bool streaming = (flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 ||
+                           !tc_supported(ds) || M < g_group_m_threshold.load();
+    if (streaming) {
       MmaLaunch L;
       L.count = count;
       int64_t tiles = 0;
@@ -508,6 +517,14 @@ int q4mm_set_m_threshold(int64_t m) {
 }
 
 int64_t q4mm_get_m_threshold(void) { return g_m_threshold.load(); }
+
+int q4mm_set_group_m_threshold(int64_t m) {
+  if (m < 1 || m > Q4MM_M_MAX + 1) return Q4_ERR_INVALID_ARG;
+  g_group_m_threshold.store(m);
+  return Q4_OK;
+}
+
+int64_t q4mm_get_group_m_threshold(void) { return g_group_m_threshold.load(); }
 
 int q4_device_status(void) {
   int dev;

@@ -51,6 +51,14 @@ def test_status_strings_and_threshold(q4):
     with pytest.raises(q4.Q4Error) as e:
         q4.q4mm_set_m_threshold(0)
     assert e.value.status == q4.Q4_ERR_INVALID_ARG
+    old_g = q4.q4mm_get_group_m_threshold()
+    assert old_g >= 1
+    q4.q4mm_set_group_m_threshold(9)
+    assert q4.q4mm_get_group_m_threshold() == 9
+    q4.q4mm_set_group_m_threshold(old_g)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.q4mm_set_group_m_threshold(q4.Q4MM_M_MAX + 2)
+    assert e.value.status == q4.Q4_ERR_INVALID_ARG
 
 
 def test_null_arguments_rejected_on_host(q4):

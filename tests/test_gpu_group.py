@@ -66,7 +66,7 @@ def test_group_batch_invariant_rows():
 
 def test_group_above_threshold_uses_per_weight_calls():
     Ws, blocks = _group([(300, 1024), (256, 1024)], 98)
-    M = q4.q4mm_get_m_threshold() + 3
+    M = q4.q4mm_get_group_m_threshold() + 3
     x_np = acts(98, M, 1024)
     ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x_np).cuda())
     for y, b in zip(ys, blocks):
