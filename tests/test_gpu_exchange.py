@@ -1,0 +1,116 @@
+"""GPU parity of the split-K exchanges, against the CPU oracle.
+
+The streaming kernel adds the K splits of a tile either inside a thread-block
+cluster (at most 4 splits, all clusters resident at once) or through flagged
+64-bit words in global memory; the tensor-core kernel either reduce-scatters
+among the splits (a launch of one wave) or lets the last CTA of a tile add them
+up.  The shapes here are chosen to land on each of those paths on a 152-SM
+GB300 (the plan is read back through q4mm_plan_info), and every result is
+compared element by element with the oracle's bound.  A second test alternates
+shapes that share the counter slots, so that each call depends on the previous
+one having reset them."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import acts, assert_within_bound, weights
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+K = 3584
+
+
+@pytest.fixture(scope="module")
+def q4():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import bit_quantized_matmul_gb300 as q4
+
+    torch.cuda.set_device(0)
+    return q4
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _setup(q4, N, config):
+    w = weights(config, N % 11, N, K)
+    return q4.q4_quantize(torch.from_numpy(w).to(DEV)), oracle.quantize(w)
+
+
+# N -> K splits of the streaming kernel on 152 SMs: 32 tiles -> 4, 40 -> 3,
+# 63 -> 2 (all three within the GPU's cluster capacity: cluster path); 28 -> 5
+# (global-memory path)
+STREAM_CASES = [(4000, 4), (5000, 3), (8000, 2), (3584, 5)]
+
+
+@pytest.mark.parametrize("N,splits", STREAM_CASES)
+def test_streaming_split_exchange_matches_oracle(q4, N, splits):
+    W, blocks = _setup(q4, N, 70)
+    _, _, s = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
+    if _sms() == 152:
+        assert s == splits
+    for M in (1, 3, 8, 11):  # one, two and three column groups; two launches
+        x = acts(70, M, K, salt=N)
+        y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), q4.Q4MM_FORCE_MMA).cpu().numpy()
+        _, y64, bound = oracle.matmul(blocks, x)
+        assert_within_bound(y, y64, bound, "mma N=%d M=%d" % (N, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
+
+
+def test_streaming_cluster_greedy_pick_matches_oracle(q4):
+    # the greedy pick always takes the global-memory exchange, also on a
+    # shape whose plain calls use clusters
+    N = 4000
+    W, blocks = _setup(q4, N, 71)
+    M = 6
+    x = acts(71, M, K)
+    idx, mx = q4.q4mm_argmax(W, torch.from_numpy(x).to(DEV))
+    _, y64, bound = oracle.matmul(blocks, x)
+    idx = idx.cpu().numpy()
+    for m in range(M):
+        order = np.argsort(-y64[m], kind="stable")
+        if y64[m, order[0]] - y64[m, order[1]] > 2 * bound[m].max():
+            assert idx[m] == order[0], m
+        assert abs(float(mx.cpu().numpy()[m]) - y64[m, idx[m]]) <= bound[m, idx[m]]
+    W.free()
+
+
+# tensor-core path: 3584 rows = 28 tiles split 5 ways at these M (one wave:
+# reduce-scatter); batch-invariant mode plans for one token tile, so M = 100
+# there runs several waves (last-CTA exchange)
+@pytest.mark.parametrize("M,flags", [(16, "tc"), (48, "tc"), (64, "tc"), (100, "tc"), (100, "inv_tc")])
+def test_tensor_core_split_exchange_matches_oracle(q4, M, flags):
+    N = 3584
+    W, blocks = _setup(q4, N, 72)
+    f = q4.Q4MM_FORCE_TC if flags == "tc" else (q4.Q4MM_FORCE_TC | q4.Q4MM_BATCH_INVARIANT)
+    x = acts(72, M, K, salt=M)
+    y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), f).cpu().numpy()
+    _, y64, bound = oracle.matmul(blocks, x)
+    assert_within_bound(y, y64, bound, "tc %s M=%d" % (flags, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
+
+
+def test_alternating_shapes_share_counter_slots(q4):
+    # calls of different split counts and exchanges use the same counter slots
+    # and partial-sum words one after the other; every result stays right
+    cases = [(4000, 8, q4.Q4MM_FORCE_MMA), (300, 3, q4.Q4MM_FORCE_MMA), (3584, 5, q4.Q4MM_FORCE_MMA),
+             (3584, 32, q4.Q4MM_FORCE_TC), (8000, 1, q4.Q4MM_FORCE_MMA), (512, 20, q4.Q4MM_FORCE_TC)]
+    prepared = []
+    for i, (N, M, f) in enumerate(cases):
+        W, blocks = _setup(q4, N, 73 + i)
+        x = acts(73, M, K, salt=i)
+        _, y64, bound = oracle.matmul(blocks, x)
+        prepared.append((W, torch.from_numpy(x).to(DEV), f, y64, bound, N, M))
+    for rep in range(3):
+        for W, xd, f, y64, bound, N, M in prepared:
+            y = q4.q4mm_forward_ex(W, xd, f).cpu().numpy()
+            assert_within_bound(y, y64, bound, "rep %d N=%d M=%d" % (rep, N, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    for p in prepared:
+        p[0].free()
