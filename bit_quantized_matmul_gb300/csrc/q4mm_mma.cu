@@ -14,18 +14,22 @@
 //
 //   16 compute warps  warp w takes row groups 2(w&3), 2(w&3)+1 (32 rows) and
 //                     K slice w>>2: block pairs bp0 + slice + 4i.  Its lanes
-//                     load their 16-byte weight fragments straight from HBM
-//                     into registers (coalesced, 1 KB per warp and pair, four
-//                     pairs in flight) — in the fragment layout they are
-//                     exactly the A registers of m16n8k16 MMAs once unpacked
-//                     to exact bf16 (q - 8).  No CTA barrier in the loop.
+//                     copy their 16-byte weight fragments (coalesced, 1 KB per
+//                     warp and pair) and lanes 0..7 the pair's 128 bytes of
+//                     fp16 scales from HBM into the warp's private cp.async
+//                     ring, two pairs ahead; each lane reads back its own
+//                     fragments, which in the fragment layout are exactly the
+//                     A registers of m16n8k16 MMAs once unpacked to exact bf16
+//                     (q - 8).  The first pairs are on their way before the
+//                     kernel waits for the previous one on the stream (weights
+//                     never depend on it).  No CTA barrier in the loop.
 //   4 converter warps stage, per chunk of 8 block pairs, the activations as
 //                     exact three-term bf16 B fragments (x = x0 + x1 + x2,
 //                     term t of row m in MMA column 3m + t, or column t of the
-//                     row's own column group in batch-invariant mode) and the
-//                     chunk's fp16 scales, into a 4-slot shared-memory ring
-//                     with full/empty mbarriers (every wait bounded).  Their
-//                     inputs arrive by cp.async two chunks ahead.
+//                     row's own column group in batch-invariant mode) into a
+//                     4-slot shared-memory ring with full/empty mbarriers
+//                     (every wait bounded).  The fp32 rows arrive by cp.async
+//                     four or five chunks ahead.
 //
 // Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
 // fp32 registers; the block's fp16 scale is applied on the CUDA cores,
@@ -53,7 +57,17 @@ constexpr int KERNEL_THREADS = COMPUTE_THREADS + CONV_THREADS;
 constexpr int CHUNK_PAIRS = 8;              // block pairs per ring slot (512 k)
 constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 constexpr int NSLOT = 4;                    // ring depth (a power of two)
-constexpr int XSTAGES = 3;                  // converter staging slots (chunks in flight)
+// Block pairs in flight per compute warp (its private cp.async ring) and the
+// unroll of its pair loop.  Measured on GB300 over the 7B decoder layers at
+// M = 1..8: a ring of two pairs with the loop unrolled twice (slot indices and
+// the once-per-chunk barrier steps become compile-time constants) beat rings
+// of 3, 4 and 8 pairs, four-fold unrolling and loading the next pair early.
+#ifndef Q4MM_WD
+#define Q4MM_WD 2
+#endif
+#ifndef Q4MM_UNROLL
+#define Q4MM_UNROLL 2
+#endif
 // row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
 // the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
 // 32 different banks and the per-row reads stay consecutive
@@ -88,19 +102,25 @@ template <int C>
 struct MmaCfg {
   static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
   static constexpr int BF_PAIR = C * 1024;  // B fragments of a pair: [cg][h][32 slots] x 16 B
-  static constexpr int SCL_OFF = CHUNK_PAIRS * BF_PAIR;
-  static constexpr int SLOT = SCL_OFF + CHUNK_PAIRS * PAIR_SCL_BYTES;
+  static constexpr int SLOT = CHUNK_PAIRS * BF_PAIR;
   static constexpr int RING = NSLOT * SLOT;
-  // converter staging: per slot the chunk's raw fp32 x rows and its scales
-  static constexpr int XSLOT = MAXM * CHUNK_K * 4 + CHUNK_PAIRS * PAIR_SCL_BYTES;
+  // converter staging: per slot the chunk's raw fp32 x rows
+  static constexpr int XSTAGES = C == 3 ? 5 : 6;  // chunks of x in flight + the one converted
+  static constexpr int XSLOT = MAXM * CHUNK_K * 4;
   static constexpr int XRAW_OFF = RING;
   static constexpr int RED = SLICES * C * 8 * RED_LD * 4;  // per-slice sums for the gather
   static constexpr int XCH_OFF = (RED + 15) / 16 * 16;  // cluster split-K: this CTA's sums
   static constexpr int XCH = MAXM * TILE_N * 4;           // [token row][tile row] fp32
-  static constexpr int BAR_OFF = RING + XSTAGES * XSLOT > XCH_OFF + XCH ? RING + XSTAGES * XSLOT
-                                                                       : XCH_OFF + XCH;
+  // weight pairs in flight per compute warp: a private ring of WD slots, each
+  // the warp's 16-byte fragments of its two row groups (1 KB) and their fp16
+  // scales (128 B), filled by cp.async
+  static constexpr int WD = Q4MM_WD;
+  static constexpr int WSLOT = 1024 + 128;
+  static constexpr int WR_OFF = RING + XSTAGES * XSLOT;
+  static constexpr int WR = COMPUTE_WARPS * WD * WSLOT;
+  static constexpr int BAR_OFF = WR_OFF + WR > XCH_OFF + XCH ? WR_OFF + WR : XCH_OFF + XCH;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
-  static constexpr int PREFETCH = 2;  // weight pairs in flight per warp (registers)
+  static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
 // bf16 pair (q - 8) for nibble pair p of word w: 0x4300 | q is bf16(128 + q),
@@ -148,14 +168,6 @@ __device__ __forceinline__ float2 split2(unsigned long long v) {
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
-}
-
-__device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -258,7 +270,7 @@ template <int C, bool DENSE>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
   using S = MmaCfg<C>;
   constexpr int MAXM = S::MAXM;
-  constexpr int PREFETCH = S::PREFETCH;
+  constexpr int WD = S::WD;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ unsigned long long kred[4][MAXM];
   __shared__ int s_flag;
@@ -284,20 +296,33 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   uint64_t* bempty = bfull + NSLOT;
   const bool compute = warp < COMPUTE_WARPS;
 
+  // the next kernel on the stream may be scheduled now: its CTAs take the SMs
+  // this launch leaves idle or gives back and start their own weight stream
+  // (weights never depend on an earlier kernel) while this one finishes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // compute warps: first weight loads before anything else (weights never
   // depend on an earlier kernel)
   const int rgp = warp & 3, sl = (warp >> 2) & 3;
   const int n_i = (compute && npairs > sl) ? (npairs - sl + SLICES - 1) / SLICES : 0;
   const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
   constexpr int64_t WSTEP = SLICES * 8 * 32;  // uint4 between a slice's consecutive pairs
-  uint4 wb[PREFETCH][2];
-#pragma unroll
-  for (int u = 0; u < PREFETCH; ++u) {
-    wb[u][0] = wb[u][1] = make_uint4(0u, 0u, 0u, 0u);
-    if (u < n_i) {
-      wb[u][0] = ld_stream16(wp + u * WSTEP);
-      wb[u][1] = ld_stream16(wp + u * WSTEP + 32);
+  // ring slot j of this warp: [row group 2rgp, 2rgp + 1][lane][16 B] of
+  // nibbles, then the 128 scale bytes of the two row groups ([rg][g][4 x fp16])
+  const uint32_t wring = smem_u32(smem + S::WR_OFF + warp * (WD * S::WSLOT));
+  const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
+  constexpr int64_t SSTEP = SLICES * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
+  auto fetch = [&](int i) {  // pair i of this warp's K slice into slot i % WD
+    if (i < n_i) {
+      const uint32_t d = wring + (uint32_t)(i % WD) * S::WSLOT;
+      cp_async16(d + lane * 16, wp + (int64_t)i * WSTEP);
+      cp_async16(d + 512u + lane * 16, wp + (int64_t)i * WSTEP + 32);
+      if (lane < 8) cp_async16(d + 1024u + lane * 16, sp + (int64_t)i * SSTEP);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");  // one group per pair, empty or not
+  };
+  if (compute) {
+#pragma unroll
+    for (int u = 0; u < WD; ++u) fetch(u);
   }
 
   // zero the B-fragment columns no converter writes: the last column group
@@ -348,11 +373,27 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     const int g = lane >> 2;
     const int lsw0 = (lane ^ ((sl & 1) * 4)) * 16;        // slot of this lane, h = 0
     const int lsw1 = (lane ^ ((sl & 1) * 4 + 1)) * 16;    // h = 1
-    for (int i0 = 0; i0 < n_i; i0 += PREFETCH) {
-#pragma unroll
-      for (int u = 0; u < PREFETCH; ++u) {
-        const int i = i0 + u;
-        if (i >= n_i) break;
+    // the 16-byte words and scales of pair i of this warp, once they are in
+    // (this lane's groups complete in order, WD - 1 may still fly; the warp
+    // barrier makes lanes 0..7's scale copies visible to all lanes)
+    auto load_pair = [&](int i, uint4& a0, uint4& a1, uint2& s0, uint2& s1) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
+      __syncwarp();
+      const uint32_t src = wring + (uint32_t)(i % WD) * S::WSLOT;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a0.x), "=r"(a0.y), "=r"(a0.z), "=r"(a0.w) : "r"(src + lane * 16) : "memory");
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a1.x), "=r"(a1.y), "=r"(a1.z), "=r"(a1.w) : "r"(src + 512u + lane * 16) : "memory");
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s0.x), "=r"(s0.y) : "r"(src + 1024u + g * 8) : "memory");
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s1.x), "=r"(s1.y) : "r"(src + 1088u + g * 8) : "memory");
+    };
+    {
+#if Q4MM_UNROLL == 2
+#pragma unroll 2
+#elif Q4MM_UNROLL == 4
+#pragma unroll 4
+#endif
+      for (int i = 0; i < n_i; ++i) {
         const int c = i >> 1;
         const int slot = c & (NSLOT - 1);
         if ((i & 1) == 0 &&
@@ -360,14 +401,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           s_err = 1;
           goto compute_done;
         }
-        const uint4 w0 = wb[u][0], w1 = wb[u][1];
+        uint4 w0, w1;
+        uint2 sv0, sv1;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
+        load_pair(i, w0, w1, sv0, sv1);
         const int pc = sl + 4 * (i & 1);  // pair within the chunk
         const uint8_t* sb = smem + slot * S::SLOT;
-        const uint2 sv0 = *reinterpret_cast<const uint2*>(sb + S::SCL_OFF + pc * PAIR_SCL_BYTES +
-                                                          ((2 * rgp) * 8 + g) * 8);
-        const uint2 sv1 = *reinterpret_cast<const uint2*>(sb + S::SCL_OFF + pc * PAIR_SCL_BYTES +
-                                                          ((2 * rgp + 1) * 8 + g) * 8);
-        // sv.x = d(R0, b0), d(R0, b1); sv.y = d(R1, b0), d(R1, b1) of each row group
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t a00[4], a01[4], a10[4], a11[4];  // [rg][k-step]
@@ -380,9 +418,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             a10[p] = nib_pair(y0, p);
             a11[p] = nib_pair(y1, p);
           }
-          if (h == 1 && i + PREFETCH < n_i) {  // refill once the pair's words are unpacked
-            wb[u][0] = ld_stream16(wp + (int64_t)(i + PREFETCH) * WSTEP);
-            wb[u][1] = ld_stream16(wp + (int64_t)(i + PREFETCH) * WSTEP + 32);
+          // refill the slot once every lane has unpacked both its words (the
+          // shared loads have completed, so the copy cannot overtake them)
+          if (h == 1) {
+            __syncwarp();
+            fetch(i + WD);
           }
           const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
           const __half2* q1 = reinterpret_cast<const __half2*>(&sv1);
@@ -434,6 +474,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       }
     }
   compute_done:;
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy into the ring outlives the loop
   } else {
     // ---- converter warps ----
     const int ct = tid - COMPUTE_THREADS;  // k = 4ct .. 4ct + 3 of each chunk
@@ -460,13 +501,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       }
     }
     const float* xr = a.x + bp0 * 64 + 4 * ct;
-    const uint8_t* sg = scl_w + (tile * a.KBP + bp0) * PAIR_SCL_BYTES;
-    // Stage chunk c: this thread's 16 bytes of every token row (k = 4ct..4ct+3)
-    // and its two 16-byte pieces of the chunk's scales.  Each thread reads back
-    // only what it copied, so completion needs no barrier.
+    // Stage chunk c: this thread's 16 bytes of every token row (k = 4ct..4ct+3).
+    // Each thread reads back only what it copied, so completion needs no barrier.
     auto stage = [&](int c) {
       if (c < nchunks) {
-        uint8_t* xs = smem + S::XRAW_OFF + (c % XSTAGES) * S::XSLOT;
+        uint8_t* xs = smem + S::XRAW_OFF + (c % S::XSTAGES) * S::XSLOT;
         const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
         const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
         if (k_ok) {
@@ -476,39 +515,25 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
               cp_async16(smem_u32(xs + m * (CHUNK_K * 4) + ct * 16),
                          xr + xoff[m] + (int64_t)c * CHUNK_K);
         }
-        const int scl_bytes = min(CHUNK_PAIRS, npairs - c * CHUNK_PAIRS) * PAIR_SCL_BYTES;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int q = ct + r * CONV_THREADS;
-          if (q * 16 < scl_bytes)
-            cp_async16(smem_u32(xs + MAXM * CHUNK_K * 4 + q * 16),
-                       sg + (int64_t)c * CHUNK_PAIRS * PAIR_SCL_BYTES + q * 16);
-        }
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    stage(0);
-    stage(1);
+    constexpr int XLEAD = S::XSTAGES - 1;  // chunks of x staged ahead of the one converted
+#pragma unroll
+    for (int c = 0; c < XLEAD; ++c) stage(c);
     for (int c = 0; c < nchunks; ++c) {
       const int slot = c & (NSLOT - 1);
       uint8_t* sb = smem + slot * S::SLOT;
-      const uint8_t* xs = smem + S::XRAW_OFF + (c % XSTAGES) * S::XSLOT;
+      const uint8_t* xs = smem + S::XRAW_OFF + (c % S::XSTAGES) * S::XSLOT;
       const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
       const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // chunk c staged (c + 1 may be in flight)
-      stage(c + 2);  // refills the slot read in the previous iteration
+      // chunk c staged (the next XLEAD - 1 may be in flight)
+      asm volatile("cp.async.wait_group %0;" ::"n"(XLEAD - 1) : "memory");
+      stage(c + XLEAD);  // refills the slot read in the previous iteration
       if (c >= NSLOT &&
           !mbar_wait_bounded(smem_u32(&bempty[slot]), (uint32_t)(((c / NSLOT) + 1) & 1), &s_err)) {
         s_err = 1;
         break;
-      }
-      const int scl_bytes = min(CHUNK_PAIRS, npairs - c * CHUNK_PAIRS) * PAIR_SCL_BYTES;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int q = ct + r * CONV_THREADS;
-        if (q * 16 < scl_bytes)
-          *reinterpret_cast<uint4*>(sb + S::SCL_OFF + q * 16) =
-              *reinterpret_cast<const uint4*>(xs + MAXM * CHUNK_K * 4 + q * 16);
       }
       if (pair_ok) {
         constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows read back together
