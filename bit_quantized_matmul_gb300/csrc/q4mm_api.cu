@@ -46,9 +46,10 @@ std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 // Grouped calls (q4mm_forward_group) stay on the streaming kernel longer: there
 // one launch covers the whole group, while the tensor-core path runs once per
 // weight.  Measured the same way over a layer's q/k/v and gate/up groups: the
-// one streaming launch per group is faster up to M = 24, the per-weight
-// tensor-core calls from M = 32.
-constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 32;
+// one streaming launch per group is faster up to M = 16 (77.6 against 114.3 us
+// for the two groups), the per-weight tensor-core calls from M = 24 (114.6
+// against 115.9 us, nearly a tie).
+constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 24;
 std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

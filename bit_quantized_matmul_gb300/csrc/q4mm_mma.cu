@@ -68,6 +68,11 @@ constexpr int NSLOT = 4;                    // ring depth (a power of two)
 #ifndef Q4MM_UNROLL
 #define Q4MM_UNROLL 2
 #endif
+// largest K split whose CTAs exchange partial sums through a thread-block
+// cluster (distributed shared memory) instead of global memory
+#ifndef Q4MM_CLUSTER_MAX
+#define Q4MM_CLUSTER_MAX 4
+#endif
 // row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
 // the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
 // 32 different banks and the per-row reads stay consecutive
@@ -767,7 +772,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // memory.  Both add the splits in the same order.  (Measured on GB300 for
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
-  a.cluster = plan.splits > 1 && plan.splits <= 4 && idx == nullptr &&
+  a.cluster = plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
               tiles <= cluster_capacity<C, DENSE>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles, (unsigned)plan.splits, 1);
