@@ -568,6 +568,70 @@ def run_path_sweep(args):
     return 0
 
 
+def run_kv_append(args):
+    """KV-cache append of a Qwen2.5-0.5B-shaped cache (24 layers, 2 KV heads,
+    head_dim 64, bf16): a 2,049-row prefill into one slot and a decode step of
+    64 requests, with V as a transposed view.  Prints one JSON line; bytes
+    moved = new rows read + the same bytes written."""
+    import numpy as np
+    import torch
+
+    import bit_quantized_matmul_gb300 as q4
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L, H, D, slots, cap = 24, 2, 64, 64, 4096
+    kc = torch.zeros((L, slots, H, cap, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    stream = torch.cuda.Stream(dev)
+    cases = {}
+    for name, reqs, ctx in (("prefill_2049", [(0, 2049)], 0), ("decode_64x1", [(s, 1) for s in range(slots)], 2049)):
+        total = sum(n for _, n in reqs)
+        g = torch.Generator(device="cpu").manual_seed(0x4B58)
+        k_new = torch.randn((L, total, H, D), generator=g).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((L, H, total, D), generator=g).to(torch.bfloat16).to(dev).transpose(1, 2)
+        offsets = torch.tensor(np.concatenate([[0], np.cumsum([n for _, n in reqs])]), dtype=torch.int32,
+                               device=dev)
+        slot = torch.tensor([s for s, _ in reqs], dtype=torch.int32, device=dev)
+        pos = torch.full((len(reqs),), ctx, dtype=torch.int32, device=dev)
+        reps = 50
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                q4.q4_kv_append(kc, vc, k_new, v_new, offsets, slot, pos, stream=stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(reps):
+                    q4.q4_kv_append(kc, vc, k_new, v_new, offsets, slot, pos, stream=stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(max(1, args.steps)):
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)
+        us = statistics.median(times)
+        row_bytes = 2 * L * H * D * 2  # K and V of one packed row, all layers
+        moved = 2 * total * row_bytes
+        cases[name] = {"us_per_append": us, "gbs": moved / (us * 1e-6) / 1e9, "bytes_moved": moved,
+                       "rows": total, "context": ctx,
+                       # a cache grown by concatenation re-copies every request's rows each step
+                       "bytes_a_concatenating_cache_copies": sum(ctx + n for _, n in reqs) * row_bytes}
+    assert q4.q4_device_status() == q4.Q4_OK
+    peak, kind = _peaks()
+    line = {"metric": "KV-cache append GB/s (new rows read + written)", "unit": "GB/s",
+            "value": cases["prefill_2049"]["gbs"], "n_gpus": 1, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": "qwen2.5-0.5b KV cache (24 layers, 2 KV heads, head_dim 64, "
+                                                         "bf16, V a transposed view), one launch per append",
+                                            "l2": "new rows hot in L2, as the producing kernel leaves them"},
+            "cases": cases, "peak_gbs": peak, "peak_source": kind,
+            "frac_of_peak": cases["prefill_2049"]["gbs"] / peak}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -582,7 +646,11 @@ def main():
                     help="one call per linear instead of grouping q/k/v and gate/up")
     ap.add_argument("--path-sweep", action="store_true",
                     help="time both kernel paths per M and print the measured M threshold")
+    ap.add_argument("--kv-append", action="store_true",
+                    help="time the KV-cache append (q4_kv_append) instead of the matmul step")
     args = ap.parse_args()
+    if args.kv_append:
+        return run_kv_append(args)
     if args.path_sweep:
         return run_path_sweep(args)
     if args.impl == "reference":

@@ -50,6 +50,7 @@ EXPORTS = (
     "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4mm_set_group_m_threshold",
     "q4mm_get_group_m_threshold", "q4_device_status",
     "q4_status_string",
+    "q4_kv_append",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -75,6 +76,8 @@ _sig = {
     "q4mm_forward_group": [_p, ctypes.c_int, _p, _p, _i64, _u32, _p],
     "q4mm_argmax_rows": [_p, _p, _i64, _p, _i64, _p, _p, _p],
     "q4_verify_greedy": [_p, _p, _i64, _p, _i64, _p, _p],
+    "q4_kv_append": [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(_i64),
+                     ctypes.POINTER(_i64), _p, _p, _p, _i64, _i64, _p],
     "q4mm_select_path": [_p, _i64, _u32],
     "q4mm_plan_info": [_p, _i64, _u32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                        ctypes.POINTER(ctypes.c_int)],
@@ -310,6 +313,42 @@ def q4_verify_greedy(idx: torch.Tensor, draft: torch.Tensor, offsets: torch.Tens
         _check(_lib.q4_verify_greedy(idx.data_ptr(), draft.data_ptr(), idx.numel(), offsets.data_ptr(), max(S, 0),
                                      acc.data_ptr(), _stream(stream)), "q4_verify_greedy")
     return acc
+
+
+def q4_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                 offsets: torch.Tensor, slot: torch.Tensor, pos: torch.Tensor, stream=None):
+    """Write the step's new K/V rows into a preallocated cache, in place.
+
+    k_cache, v_cache: contiguous [layers, slots, heads, capacity, head_dim];
+    k_new, v_new: [layers, total, heads, head_dim] views (head_dim contiguous,
+    any other strides) of the same dtype (2- or 4-byte elements);
+    offsets int32 [S + 1], slot and pos int32 [S], all on the cache's device.
+    """
+    if k_cache.dim() != 5 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or \
+            not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [layers, slots, heads, capacity, head_dim] of one shape")
+    if k_new.dim() != 4 or v_new.shape != k_new.shape:
+        raise ValueError("new rows must be [layers, total, heads, head_dim] views of one shape")
+    L, slots, H, cap, D = k_cache.shape
+    if k_new.shape[0] != L or k_new.shape[2] != H or k_new.shape[3] != D or k_new.stride(3) != 1 or \
+            v_new.stride(3) != 1:
+        raise ValueError("new rows do not match the cache shape (or head_dim is not contiguous)")
+    for t in (v_cache, k_new, v_new):
+        if t.dtype != k_cache.dtype or t.device != k_cache.device:
+            raise ValueError("caches and new rows must share dtype and device")
+    for t, n in ((offsets, "offsets"), (slot, "slot"), (pos, "pos")):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.device != k_cache.device:
+            raise ValueError("%s must be a contiguous int32 tensor on the cache's device" % n)
+    S = slot.numel()
+    if offsets.numel() != S + 1 or pos.numel() != S:
+        raise ValueError("offsets must have S + 1 entries and pos S")
+    with torch.cuda.device(k_cache.device):
+        ks = (_i64 * 3)(*k_new.stride()[:3])
+        vs = (_i64 * 3)(*v_new.stride()[:3])
+        _check(_lib.q4_kv_append(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                 L, slots, H, D, cap, k_cache.element_size(), ks, vs, offsets.data_ptr(),
+                                 slot.data_ptr(), pos.data_ptr(), S, k_new.shape[1], _stream(stream)),
+               "q4_kv_append")
 
 
 def q4mm_argmax_ex(W: Q4Weight, x: torch.Tensor, flags: int = 0, want_max: bool = True, stream=None):

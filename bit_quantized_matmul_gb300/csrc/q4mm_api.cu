@@ -454,6 +454,45 @@ int q4_verify_greedy(const int32_t* idx, const int32_t* draft, int64_t total, co
   return launch_verify(idx, draft, total, offsets, (int)S, accepted, stream);
 }
 
+int q4_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t layers,
+                 int64_t slots, int64_t heads, int64_t head_dim, int64_t capacity, int elem_bytes,
+                 const int64_t* k_strides, const int64_t* v_strides, const int32_t* offsets,
+                 const int32_t* slot, const int32_t* pos, int64_t S, int64_t total, cudaStream_t stream) {
+  constexpr int64_t LIM = (int64_t)1 << 31;
+  if (layers < 1 || slots < 1 || heads < 1 || head_dim < 1 || capacity < 1 || layers >= LIM ||
+      slots >= LIM || heads >= LIM || head_dim >= LIM || capacity >= LIM ||
+      (elem_bytes != 2 && elem_bytes != 4) || S < 0 || S >= INT32_MAX || total < 0 || total >= INT32_MAX ||
+      !k_strides || !v_strides)
+    return Q4_ERR_INVALID_ARG;
+  int64_t stride[6];
+  for (int i = 0; i < 3; ++i) {
+    if (k_strides[i] < 0 || v_strides[i] < 0 || k_strides[i] >= (LIM << 28) || v_strides[i] >= (LIM << 28))
+      return Q4_ERR_INVALID_ARG;
+    stride[i] = k_strides[i] * elem_bytes;
+    stride[3 + i] = v_strides[i] * elem_bytes;
+  }
+  if (S == 0 || total == 0) return Q4_OK;
+  if (!k_cache || !v_cache || !k_new || !v_new || !offsets || !slot || !pos) return Q4_ERR_INVALID_ARG;
+  const int64_t row_bytes = head_dim * elem_bytes;
+  if (total * ((row_bytes + 15) / 16) >= INT32_MAX || 2 * layers * heads >= INT32_MAX)
+    return Q4_ERR_INVALID_ARG;  // the kernel's 32-bit item index within a plane
+  bool aligned = row_bytes % 16 == 0 && aligned16(k_cache) && aligned16(v_cache) && aligned16(k_new) &&
+                 aligned16(v_new);
+  for (int i = 0; i < 6; ++i) aligned = aligned && stride[i] % 16 == 0;
+  if (!aligned) return Q4_ERR_ALIGN;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);  // the status word the kernel reports to
+  if (st) return st;
+  return launch_kv_append(static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
+                          static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), layers,
+                          slots, heads, row_bytes, capacity, stride, offsets, slot, pos, (int)S, total,
+                          ds.ws.status, ds.num_sms, stream);
+}
+
 int q4mm_argmax(const q4_weight* W, const float* x, int32_t* idx, float* maxval, int64_t M,
                 cudaStream_t stream) {
   if (!idx) return Q4_ERR_INVALID_ARG;

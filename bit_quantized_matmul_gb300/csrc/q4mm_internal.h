@@ -77,6 +77,7 @@ constexpr int MAX_COUNTERS = 1 << 16;
 // Bits of the device status word (read and cleared by q4_device_status).
 constexpr unsigned STATUS_TIMEOUT = 1u;   // a bounded wait ran out
 constexpr unsigned STATUS_BAD_ROW = 2u;   // a row index of q4mm_argmax_rows was out of range
+constexpr unsigned STATUS_KV_RANGE = 4u;  // a q4_kv_append request was out of range (not written)
 
 // Returns Q4_OK and fills *ws with at least the requested capacities.
 int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws);
@@ -114,6 +115,14 @@ int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* id
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
                      const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s,
                      const int32_t* xrows = nullptr, int64_t x_rows = 0);
+
+// KV-cache append of one step (see q4_kv_append); sizes in elements except
+// row_bytes and the source strides (bytes: K layer, token, head, then V's).
+int launch_kv_append(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k_new, const uint8_t* v_new,
+                     int64_t layers, int64_t slots, int64_t heads, int64_t row_bytes, int64_t capacity,
+                     const int64_t (&stride)[6], const int32_t* offsets,
+                     const int32_t* slot, const int32_t* pos, int S, int64_t total, unsigned* status,
+                     int num_sms, cudaStream_t s);
 
 // Greedy verification of draft tokens per request (see q4_verify_greedy).
 int launch_verify(const int32_t* idx, const int32_t* draft, int64_t total, const int32_t* offsets,

@@ -238,6 +238,47 @@ Q4_API int q4_verify_greedy(const int32_t* idx, const int32_t* draft, int64_t to
                             const int32_t* offsets, int64_t S, int32_t* accepted,
                             cudaStream_t stream);
 
+/* KV-cache append of one continuous-batching step into a preallocated cache
+ * ("A non-contiguous KV cache cuts Qwen2 decode speed by 59 % at 2k context in
+ * Candle on Metal", §"Cause and workaround": a cache that grows by
+ * concatenation re-copies itself on every append when the new V rows are a
+ * strided view; writing only the new rows into a buffer that is already in
+ * place does not).  One launch writes the new K and V rows of every layer and
+ * every request; nothing already cached is read or moved.
+ *   k_cache, v_cache  device, [layers][slots][heads][capacity][head_dim]
+ *                     elements of elem_bytes (2 or 4) each, contiguous,
+ *                     caller-owned; slot sl's position p of (layer, head) is
+ *                     one head_dim row.
+ *   k_new, v_new      device, the step's new rows: K element (l, t, h, d) at
+ *                     k_new + l*k_strides[0] + t*k_strides[1] +
+ *                     h*k_strides[2] + d (host arrays of 3 strides, in
+ *                     elements, head_dim contiguous), V likewise with
+ *                     v_strides; t over the step's packed rows [0, total).  A
+ *                     transposed or otherwise strided view (such as V after
+ *                     prefill) is read in place.
+ *   offsets           device, int32 [S + 1], non-decreasing: request s owns
+ *                     packed rows [offsets[s], offsets[s+1]); rows outside
+ *                     every request are not cached.
+ *   slot, pos         device, int32 [S]: request s's cache slot and the
+ *                     position of its first new row (its current length).
+ *                     Row offsets[s] + j goes to position pos[s] + j; the
+ *                     caller advances its lengths.
+ * Host-checked: sizes >= 1 (layers, slots, heads, head_dim, capacity below
+ * 2^31; S and total below 2^31 - 1; total * head_dim * elem_bytes / 16 and
+ * 2 * layers * heads below 2^31 - 1), elem_bytes 2 or 4, stride arrays given
+ * and every stride in [0, 2^59) (INVALID_ARG); head_dim * elem_bytes, every
+ * stride * elem_bytes and every base address multiples of 16 bytes (ALIGN).  S = 0 or total = 0: a no-op.
+ * On the device, a request whose slot is outside [0, slots), whose position
+ * is negative, or whose rows would pass capacity or total is not written at
+ * all (the other requests are) and q4_device_status then reports
+ * Q4_ERR_INVALID_ARG.  Asynchronous on stream; the same bytes as the source,
+ * whatever the element type. */
+Q4_API int q4_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                        int64_t layers, int64_t slots, int64_t heads, int64_t head_dim,
+                        int64_t capacity, int elem_bytes, const int64_t* k_strides,
+                        const int64_t* v_strides, const int32_t* offsets, const int32_t* slot,
+                        const int32_t* pos, int64_t S, int64_t total, cudaStream_t stream);
+
 /* The kernel path (Q4MM_PATH_*) a call with these arguments would take, or a
  * negative status. */
 Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);

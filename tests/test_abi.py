@@ -74,3 +74,28 @@ def test_null_arguments_rejected_on_host(q4):
     assert lib.q4mm_forward_group(None, 1, None, None, 4, 0, None) == q4.Q4_ERR_INVALID_ARG
     assert lib.q4mm_argmax_rows(None, None, 1, None, 1, None, None, None) == q4.Q4_ERR_INVALID_ARG
     assert lib.q4_verify_greedy(None, None, 0, None, 1, None, None) == q4.Q4_ERR_INVALID_ARG
+
+
+def test_kv_append_arguments_checked_on_host(q4):
+    lib = q4.raw_library()
+    a16 = 4096  # aligned stand-in addresses: these calls return before any CUDA call
+
+    I3 = ctypes.c_int64 * 3
+
+    def call(p=a16, layers=2, slots=2, heads=2, head_dim=64, cap=16, eb=2, st=128, S=1, total=1, off=a16,
+             strides=True):
+        ks, vs = I3(0, st, 64), I3(0, 64, 128)
+        return lib.q4_kv_append(p, p, p, p, layers, slots, heads, head_dim, cap, eb, ks if strides else None,
+                                vs, off, off, off, S, total, None)
+
+    assert call(layers=0) == q4.Q4_ERR_INVALID_ARG
+    assert call(eb=3) == q4.Q4_ERR_INVALID_ARG
+    assert call(st=-1) == q4.Q4_ERR_INVALID_ARG
+    assert call(strides=False) == q4.Q4_ERR_INVALID_ARG
+    assert call(S=-1) == q4.Q4_ERR_INVALID_ARG
+    assert call(S=0) == q4.Q4_OK and call(total=0) == q4.Q4_OK  # nothing to write
+    assert call(p=None) == q4.Q4_ERR_INVALID_ARG
+    assert call(off=None) == q4.Q4_ERR_INVALID_ARG
+    assert call(head_dim=12) == q4.Q4_ERR_ALIGN     # 24-byte rows
+    assert call(st=100) == q4.Q4_ERR_ALIGN          # 200-byte token stride
+    assert call(p=a16 + 8) == q4.Q4_ERR_ALIGN
