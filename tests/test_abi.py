@@ -99,3 +99,4 @@ def test_kv_append_arguments_checked_on_host(q4):
     assert call(head_dim=12) == q4.Q4_ERR_ALIGN     # 24-byte rows
     assert call(st=100) == q4.Q4_ERR_ALIGN          # 200-byte token stride
     assert call(p=a16 + 8) == q4.Q4_ERR_ALIGN
+    assert call(total=2 ** 30) == q4.Q4_ERR_INVALID_ARG  # 8 vectors per row: past the 32-bit item index

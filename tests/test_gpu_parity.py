@@ -236,3 +236,24 @@ def test_argmax_exact_ties_pick_lowest_index(q4):
     idx, mx = q4.q4mm_argmax(W, torch.from_numpy(x).to(DEV))
     assert int(idx.item()) == 310
     W.free()
+
+
+def test_forward_at_the_largest_m(q4):
+    # M = Q4MM_M_MAX in one call (tensor-core path, several token tiles), every
+    # output of a seeded sample of rows against the oracle; the streaming path
+    # (8 rows per launch) on the same rows
+    N, K = 300, 1024
+    w = weights(52, 3, N, K)
+    blocks = oracle.quantize(w)
+    W = q4.q4_quantize(torch.from_numpy(w).to(DEV))
+    M = q4.Q4MM_M_MAX
+    x = acts(52, M, K)
+    xd = torch.from_numpy(x).to(DEV)
+    rows = np.sort(np.random.default_rng(52).choice(M, 96, replace=False))
+    rows[-1] = M - 1
+    _, y64, bound = oracle.matmul(blocks, x[rows])
+    for flags in (0, q4.Q4MM_FORCE_MMA):
+        y = q4.q4mm_forward_ex(W, xd, flags).cpu().numpy()
+        assert_within_bound(y[rows], y64, bound, "M=%d flags=%d" % (M, flags))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
