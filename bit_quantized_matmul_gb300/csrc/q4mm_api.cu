@@ -536,8 +536,9 @@ int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int
     sp = plan.splits;
   } else if (p == Q4MM_PATH_MMA) {
     const MmaPlan plan = mma_plan(&W->w, ds.num_sms);
-    l = mma_launch_count(M, (flags & Q4MM_BATCH_INVARIANT) != 0);
-    sp = plan.splits;
+    const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
+    l = mma_launch_count(M, inv);
+    sp = mma_row_groups(plan, W->w.K, inv, false) ? 1 : plan.splits;
   } else {
     const MmaPlan plan = simt_plan(&W->w, ds.num_sms);
     l = p == Q4MM_PATH_ROW_BY_ROW ? (int)M : simt_launch_count(M);

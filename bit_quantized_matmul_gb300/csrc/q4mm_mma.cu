@@ -31,6 +31,12 @@
 //                     (every wait bounded).  The fp32 rows arrive by cp.async
 //                     four or five chunks ahead.
 //
+// Short-K launches whose tiles x 4 fit on the SMs (the q/k/v group and o_proj
+// of a 7B layer) run as row-group CTAs instead: a CTA takes one row-group pair
+// (32 rows) of a tile over the whole K, and its 16 compute warps are 16 K
+// slices.  Its K reduction is then a shared-memory sum; no partial sums cross
+// CTAs, whose exchange costs 1-2 us in the tail of every split launch.
+//
 // Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
 // fp32 registers; the block's fp16 scale is applied on the CUDA cores,
 // acc = fma(d, D_b, acc), in ascending block order.  At the end the four K
@@ -73,6 +79,12 @@ constexpr int NSLOT = 4;                    // ring depth (a power of two)
 #ifndef Q4MM_CLUSTER_MAX
 #define Q4MM_CLUSTER_MAX 4
 #endif
+// row-group CTAs (one 32-row group pair over the whole K, no K split) for
+// launches whose tiles x 4 fit on the SMs and whose K is at most this
+#ifndef Q4MM_RG_MAX_K
+#define Q4MM_RG_MAX_K 4096
+#endif
+constexpr int RG_LD = 36;  // row stride of the row-group slice sums (32 rows + 4)
 // row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
 // the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
 // 32 different banks and the per-row reads stay consecutive
@@ -271,7 +283,7 @@ __device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_
 // reads its 512 contiguous bytes conflict-free in any slot order).  The slot
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
-template <int C, bool DENSE>
+template <int C, bool DENSE, bool RG>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
   using S = MmaCfg<C>;
   constexpr int MAXM = S::MAXM;
@@ -284,11 +296,16 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // RG: the CTA is row-group pair blockIdx.x & 3 of global tile blockIdx.x >> 2
+  // over the whole K, and its 16 compute warps are 16 K slices; otherwise the
+  // CTA is global tile blockIdx.x over K split blockIdx.y, its compute warps
+  // 4 row-group pairs x 4 K slices
+  const int gtile = RG ? (int)(blockIdx.x >> 2) : (int)blockIdx.x;
   int wi = 0;
 #pragma unroll
   for (int i = 1; i < MMA_GROUP_MAX; ++i)
-    if (i < a.nweights && (int)blockIdx.x >= a.w[i].tile_start) wi = i;
-  const int64_t tile = (int64_t)blockIdx.x - a.w[wi].tile_start;  // tile within its weight
+    if (i < a.nweights && gtile >= a.w[i].tile_start) wi = i;
+  const int64_t tile = (int64_t)gtile - a.w[wi].tile_start;  // tile within its weight
   const uint4* nib_w = a.w[wi].nib;
   const uint8_t* scl_w = a.w[wi].scl;
   const int split = blockIdx.y;
@@ -307,15 +324,17 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // compute warps: first weight loads before anything else (weights never
   // depend on an earlier kernel)
-  const int rgp = warp & 3, sl = (warp >> 2) & 3;
-  const int n_i = (compute && npairs > sl) ? (npairs - sl + SLICES - 1) / SLICES : 0;
+  constexpr int NSL = RG ? COMPUTE_WARPS : SLICES;  // K slices
+  const int rgp = RG ? (int)(blockIdx.x & 3) : (warp & 3);
+  const int sl = RG ? (warp & (COMPUTE_WARPS - 1)) : ((warp >> 2) & 3);
+  const int n_i = (compute && npairs > sl) ? (npairs - sl + NSL - 1) / NSL : 0;
   const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
-  constexpr int64_t WSTEP = SLICES * 8 * 32;  // uint4 between a slice's consecutive pairs
+  constexpr int64_t WSTEP = NSL * 8 * 32;  // uint4 between a slice's consecutive pairs
   // ring slot j of this warp: [row group 2rgp, 2rgp + 1][lane][16 B] of
   // nibbles, then the 128 scale bytes of the two row groups ([rg][g][4 x fp16])
   const uint32_t wring = smem_u32(smem + S::WR_OFF + warp * (WD * S::WSLOT));
   const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
-  constexpr int64_t SSTEP = SLICES * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
+  constexpr int64_t SSTEP = NSL * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
   auto fetch = [&](int i) {  // pair i of this warp's K slice into slot i % WD
     if (i < n_i) {
       const uint32_t d = wring + (uint32_t)(i % WD) * S::WSLOT;
@@ -352,7 +371,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   if (tid == 0) {
     for (int b = 0; b < NSLOT; ++b) {
       mbar_init(smem_u32(&bfull[b]), CONV_THREADS);
-      mbar_init(smem_u32(&bempty[b]), COMPUTE_WARPS);
+      // a chunk's 8 pairs go to all 16 compute warps (two each), or with
+      // row-group CTAs to the 8 warps whose slices hold them (one each)
+      mbar_init(smem_u32(&bempty[b]), RG ? COMPUTE_WARPS / 2 : COMPUTE_WARPS);
     }
     s_err = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -399,9 +420,10 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #pragma unroll 4
 #endif
       for (int i = 0; i < n_i; ++i) {
-        const int c = i >> 1;
+        // chunk of this pair: slice sl's pairs are sl + NSL i
+        const int c = RG ? 2 * i + (sl >> 3) : (i >> 1);
         const int slot = c & (NSLOT - 1);
-        if ((i & 1) == 0 &&
+        if ((RG || (i & 1) == 0) &&
             !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
           s_err = 1;
           goto compute_done;
@@ -409,7 +431,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         uint4 w0, w1;
         uint2 sv0, sv1;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
         load_pair(i, w0, w1, sv0, sv1);
-        const int pc = sl + 4 * (i & 1);  // pair within the chunk
+        const int pc = RG ? (sl & 7) : (sl + 4 * (i & 1));  // pair within the chunk
         const uint8_t* sb = smem + slot * S::SLOT;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -472,7 +494,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             }
           }
         }
-        if ((i & 1) && c + NSLOT < nchunks) {  // this warp is done with the slot
+        if ((RG || (i & 1)) && c + NSLOT < nchunks) {  // this warp is done with the slot
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bempty[slot]));
         }
@@ -587,6 +609,48 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // a CTA of a cluster stays for the cluster barriers below whatever happened
   if (failed && !a.cluster) {
     if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
+    return;
+  }
+
+  if constexpr (RG) {
+    // ---- row-group CTA: add the 16 K slices in shared memory and write y ----
+    float* red = reinterpret_cast<float*>(smem);  // [16 slices][C*8 columns][RG_LD]
+    constexpr int RS = C * 8 * RG_LD;
+    if (compute) {
+      const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int cg = 0; cg < C; ++cg)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v;
+            if constexpr (PACKED) {
+              const float2 pr = split2(acc[r][cg][e >> 1]);
+              v = (e & 1) ? pr.y : pr.x;
+            } else {
+              v = accf[r][cg][e];
+            }
+            red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RG_LD + r * 16 + g + 8 * (e >> 1)] = v;
+          }
+    }
+    __syncthreads();
+    // thread: row tid % 32 of the pair, token rows tid / 32 + 20k; fixed order
+    // of terms and slices, as on the split path
+    const int row = tid & 31;
+    const int64_t n = tile * TILE_N + rgp * 32 + row;
+    float* y = a.w[wi].y;
+    if (n < a.w[wi].N) {
+      for (int m = tid >> 5; m < mrows; m += KERNEL_THREADS / 32) {
+        const int c0 = DENSE ? 3 * m : 8 * m;
+        float v = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+#pragma unroll
+          for (int s = 0; s < NSL; ++s) v += red[s * RS + (c0 + t) * RG_LD + row];
+        y[(int64_t)m * a.w[wi].N + n] = v;
+      }
+    }
     return;
   }
 
@@ -707,7 +771,7 @@ int cluster_capacity(int device, int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -715,7 +779,7 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
-template <int C, bool DENSE>
+template <int C, bool DENSE, bool RG>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
@@ -744,7 +808,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.K = W0->K;
   a.KBP = W0->KBP;
   a.mrows = mrows;
-  a.kbp_per_split = plan.kbp_per_split;
+  a.kbp_per_split = RG ? W0->KBP : plan.kbp_per_split;
   a.status = ws.status;
   a.e.N = W0->N;
   a.e.N_pad = (int64_t)tiles * TILE_N;
@@ -752,7 +816,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.e.y = nullptr;
   a.e.idx = idx ? idx + mb : nullptr;
   a.e.maxval = (idx && maxval) ? maxval + mb : nullptr;
-  a.e.splits = plan.splits;
+  a.e.splits = RG ? 1 : plan.splits;
   a.e.partial = ws.partial;
   a.e.counters = ws.counters;
   a.e.status = ws.status;
@@ -761,7 +825,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.e.tiles = tiles;
   static bool attr_set[64] = {};
   if (!attr_set[W0->device & 63]) {
-    if (cudaFuncSetAttribute(mma_kernel<C, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, DENSE, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63] = true;
@@ -772,10 +836,10 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // memory.  Both add the splits in the same order.  (Measured on GB300 for
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
-  a.cluster = plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
+  a.cluster = !RG && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
               tiles <= cluster_capacity<C, DENSE>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles, (unsigned)plan.splits, 1);
+  cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1) : dim3((unsigned)tiles, (unsigned)plan.splits, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
@@ -788,7 +852,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE, RG>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 // Rows per launch: 8 with dense packing (3 column groups), 3 with one row per
@@ -831,6 +895,10 @@ int mma_launch_count(int64_t M, bool batch_invariant) {
   return (int)((M + rpl - 1) / rpl);
 }
 
+bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick) {
+  return !batch_invariant && !greedy_pick && plan.splits >= 4 && K <= Q4MM_RG_MAX_K;
+}
+
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
                      const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s,
                      const int32_t* xrows, int64_t x_rows) {
@@ -839,6 +907,10 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   if (plan.splits > 1 && tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   const int64_t K = L.W[0]->K;
   const int64_t rpl = rows_per_launch(batch_invariant);
+  // row-group CTAs: no K split and so no cross-CTA exchange, when four CTAs
+  // per tile fit on the SMs (the split plan has at least 4 splits) and K is
+  // short; the plan depends on the shapes only (y output, default mode)
+  const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr);
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     const float* xs = xrows ? x : x + mb * K;
@@ -846,15 +918,24 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
     int st;
     if (batch_invariant) {
       switch (mrows) {
-        case 1: st = launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        case 2: st = launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        default: st = launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        case 1: st = launch_c<1, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        case 2: st = launch_c<2, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        default: st = launch_c<3, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
       }
     } else {
-      switch ((3 * mrows + 7) / 8) {  // column groups of this launch
-        case 1: st = launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        case 2: st = launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        default: st = launch_c<3, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+      const int cgs = (3 * mrows + 7) / 8;  // column groups of this launch
+      if (rg) {
+        switch (cgs) {
+          case 1: st = launch_c<1, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          case 2: st = launch_c<2, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          default: st = launch_c<3, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        }
+      } else {
+        switch (cgs) {
+          case 1: st = launch_c<1, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          case 2: st = launch_c<2, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          default: st = launch_c<3, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        }
       }
     }
     if (st) return st;

@@ -285,7 +285,9 @@ Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
 
 /* Plan of a call with these arguments, without running it: *path receives
  * the Q4MM_PATH_* value, *launches the number of kernel launches the call
- * makes, *splits the K partition count.  Any output pointer may be NULL. */
+ * makes, *splits the K partition count of a q4mm_forward_ex call (1 when the
+ * streaming kernel gives each CTA one 32-row group pair over the whole K).
+ * Any output pointer may be NULL. */
 Q4_API int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int* launches,
                           int* splits);
 

@@ -41,23 +41,41 @@ def _setup(q4, N, config):
     return q4.q4_quantize(torch.from_numpy(w).to(DEV)), oracle.quantize(w)
 
 
-# N -> K splits of the streaming kernel on 152 SMs: 32 tiles -> 4, 40 -> 3,
-# 63 -> 2 (all three within the GPU's cluster capacity: cluster path); 28 -> 5
-# (global-memory path)
-STREAM_CASES = [(4000, 4), (5000, 3), (8000, 2), (3584, 5)]
+# (N, K) -> K splits of the streaming kernel on 152 SMs: 32 tiles -> 4, 40 ->
+# 3, 63 -> 2 (all three within the GPU's cluster capacity: cluster path); 28
+# -> 5 (global-memory path).  The 4- and 5-split shapes use K = 4608: at K up
+# to 4096 those tile counts run as row-group CTAs without a K split (below).
+STREAM_CASES = [(4000, 4608, 4), (5000, K, 3), (8000, K, 2), (3584, 4608, 5)]
 
 
-@pytest.mark.parametrize("N,splits", STREAM_CASES)
-def test_streaming_split_exchange_matches_oracle(q4, N, splits):
-    W, blocks = _setup(q4, N, 70)
+@pytest.mark.parametrize("N,KK,splits", STREAM_CASES)
+def test_streaming_split_exchange_matches_oracle(q4, N, KK, splits):
+    w = weights(70, N % 11, N, KK)
+    W, blocks = q4.q4_quantize(torch.from_numpy(w).to(DEV)), oracle.quantize(w)
     _, _, s = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
     if _sms() == 152:
         assert s == splits
     for M in (1, 3, 8, 11):  # one, two and three column groups; two launches
-        x = acts(70, M, K, salt=N)
+        x = acts(70, M, KK, salt=N)
         y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), q4.Q4MM_FORCE_MMA).cpu().numpy()
         _, y64, bound = oracle.matmul(blocks, x)
-        assert_within_bound(y, y64, bound, "mma N=%d M=%d" % (N, M))
+        assert_within_bound(y, y64, bound, "mma N=%d K=%d M=%d" % (N, KK, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
+
+
+@pytest.mark.parametrize("N", [4000, 3584, 640])
+def test_streaming_row_group_ctas_match_oracle(q4, N):
+    # K = 3584 with 32, 28 and 5 tiles: four CTAs per tile fit on the SMs, so
+    # each CTA takes one 32-row group pair over the whole K (no K split)
+    W, blocks = _setup(q4, N, 72)
+    _, _, s = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
+    assert s == 1
+    for M in (1, 2, 3, 5, 8, 9, 16):
+        x = acts(72, M, K, salt=N)
+        y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), q4.Q4MM_FORCE_MMA).cpu().numpy()
+        _, y64, bound = oracle.matmul(blocks, x)
+        assert_within_bound(y, y64, bound, "row groups N=%d M=%d" % (N, M))
     assert q4.q4_device_status() == q4.Q4_OK
     W.free()
 
@@ -98,9 +116,12 @@ def test_tensor_core_split_exchange_matches_oracle(q4, M, flags):
 
 def test_alternating_shapes_share_counter_slots(q4):
     # calls of different split counts and exchanges use the same counter slots
-    # and partial-sum words one after the other; every result stays right
-    cases = [(4000, 8, q4.Q4MM_FORCE_MMA), (300, 3, q4.Q4MM_FORCE_MMA), (3584, 5, q4.Q4MM_FORCE_MMA),
-             (3584, 32, q4.Q4MM_FORCE_TC), (8000, 1, q4.Q4MM_FORCE_MMA), (512, 20, q4.Q4MM_FORCE_TC)]
+    # and partial-sum words one after the other (row-group CTAs with none in
+    # between); every result stays right.  Batch-invariant mode keeps the K
+    # split: clusters of 4 for 4000 rows, global words for 3584.
+    mma, inv = q4.Q4MM_FORCE_MMA, q4.Q4MM_BATCH_INVARIANT
+    cases = [(4000, 8, mma), (4000, 3, mma | inv), (300, 3, mma), (3584, 5, mma | inv),
+             (3584, 32, q4.Q4MM_FORCE_TC), (3584, 5, mma), (8000, 1, mma), (512, 20, q4.Q4MM_FORCE_TC)]
     prepared = []
     for i, (N, M, f) in enumerate(cases):
         W, blocks = _setup(q4, N, 73 + i)
