@@ -507,27 +507,38 @@ def run_path_sweep(args):
             ys = [torch.empty((M, synthetic.QWEN7B_LINEARS[n][0]), dtype=torch.float32, device=dev)
                   for n in names]
 
-            def issue_group():
-                for li in range(layers):
-                    q4.q4mm_forward_group([stack[n][li] for n in names], xs[K], ys=ys,
-                                          flags=q4.Q4MM_FORCE_MMA, stream=stream)
-            with torch.cuda.stream(stream):
-                issue_group()
-            torch.cuda.synchronize(dev)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                issue_group()
-            with torch.cuda.stream(stream):
-                for _ in range(3):
-                    g.replay()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for _ in range(5):
-                    g.replay()
-                b.record(stream)
-            torch.cuda.synchronize(dev)
-            groups_out.setdefault(gname, {})[str(M)] = {"mma_group_us": a.elapsed_time(b) * 1e3 / (5 * layers)}
-            del g
+            def time_group(flags):
+                def issue_group():
+                    for li in range(layers):
+                        q4.q4mm_forward_group([stack[n][li] for n in names], xs[K], ys=ys,
+                                              flags=flags, stream=stream)
+                with torch.cuda.stream(stream):
+                    issue_group()
+                torch.cuda.synchronize(dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    issue_group()
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        g.replay()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(5):
+                        g.replay()
+                    b.record(stream)
+                torch.cuda.synchronize(dev)
+                return a.elapsed_time(b) * 1e3 / (5 * layers)
+
+            # streaming: one launch per 8 rows over the group; tensor cores:
+            # one launch pair over the group (the group threshold forced to 1)
+            rec = {"mma_group_us": time_group(q4.Q4MM_FORCE_MMA)}
+            old_thr = q4.q4mm_get_group_m_threshold()
+            q4.q4mm_set_group_m_threshold(1)
+            try:
+                rec["tc_group_us"] = time_group(0)
+            finally:
+                q4.q4mm_set_group_m_threshold(old_thr)
+            groups_out.setdefault(gname, {})[str(M)] = rec
     # threshold: smallest M of the sweep from which one decoder layer (q, o like
     # q_proj; k, v like k_proj; gate, up like gate_proj; down) takes no longer
     # on the tcgen05 path than on the streaming path, for every larger M too
@@ -547,11 +558,12 @@ def run_path_sweep(args):
             "up_proj": "gate_proj"}
     for gname, names in GROUPS:
         if gname in groups_out:
-            for M in sweep:
-                groups_out[gname][str(M)]["tc_us"] = sum(out[like[n]][str(M)]["tc"]["us"] for n in names)
+            for M in sweep:  # for reference: the group's weights as separate tcgen05 calls
+                groups_out[gname][str(M)]["tc_separate_us"] = sum(out[like[n]][str(M)]["tc"]["us"]
+                                                                  for n in names)
 
     def group_layer(M, path):
-        key = "tc_us" if path == "tc" else "mma_group_us"
+        key = "tc_group_us" if path == "tc" else "mma_group_us"
         return sum(groups_out[g][str(M)][key] for g in groups_out)
 
     gthr = None

@@ -43,12 +43,11 @@ DeviceScratch g_dev[MAX_DEVICES];
 // for the whole layer up to M = 8, the tensor-core kernel from M = 16.
 constexpr int64_t DEFAULT_M_THRESHOLD = 16;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
-// Grouped calls (q4mm_forward_group) stay on the streaming kernel longer: there
-// one launch covers the whole group, while the tensor-core path runs once per
-// weight.  Measured the same way over a layer's q/k/v and gate/up groups: the
-// one streaming launch per group is faster up to M = 16 (77.6 against 114.3 us
-// for the two groups), the per-weight tensor-core calls from M = 24 (114.6
-// against 115.9 us, nearly a tie).
+// Grouped calls (q4mm_forward_group) run one launch over the whole group on
+// either path.  Measured the same way over a layer's q/k/v and gate/up groups:
+// the streaming launches are faster up to M = 16 (77.4 against 83.7 us for
+// the two groups), the grouped tensor-core launches from M = 24 (84.3
+// against 115.4 us).
 constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 24;
 std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
@@ -396,27 +395,27 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
     const bool streaming = (flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 ||
                            !tc_supported(ds) || M < g_group_m_threshold.load();
+    MmaLaunch L;
+    L.count = count;
+    int64_t tiles = 0;
+    for (int i = 0; i < count; ++i) {
+      L.W[i] = &W[i]->w;
+      L.y[i] = y[i];
+      tiles += W[i]->w.tiles;
+    }
+    Workspace ws;
     if (streaming) {
-      MmaLaunch L;
-      L.count = count;
-      int64_t tiles = 0;
-      for (int i = 0; i < count; ++i) {
-        L.W[i] = &W[i]->w;
-        L.y[i] = y[i];
-        tiles += W[i]->w.tiles;
-      }
       const MmaPlan plan = mma_plan_tiles(tiles, W[0]->w.KBP, ds.num_sms);
-      Workspace ws;
       st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws);
       if (st) return st;
       return launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
     }
-  }
-  for (int i = 0; i < count; ++i) {  // tensor-core path: one call per weight
-    st = run(W[i], x, y[i], nullptr, nullptr, M, flags, stream);
+    // tensor-core path: one launch pair over the tiles of the whole group
+    const TcPlan plan = tc_plan_tiles(tiles, W[0]->w.KBP, M, ds.num_sms, false);
+    st = workspace_get(dev, tc_partial_bytes_tiles(tiles, plan, M), tc_xop_bytes_kbp(W[0]->w.KBP, plan, M), &ws);
     if (st) return st;
+    return launch_tc_group(L, x, M, nullptr, nullptr, plan, ws, stream);
   }
-  return Q4_OK;
 }
 
 int q4mm_argmax_rows(const q4_weight* Wh, const float* x, int64_t x_rows, const int32_t* rows,

@@ -147,6 +147,13 @@ struct TcPlan {
   int num_sms;            // SMs of the device (one CTA per SM)
 };
 TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant);
+TcPlan tc_plan_tiles(int64_t tiles, int64_t KBP, int64_t M, int num_sms, bool batch_invariant);
+size_t tc_partial_bytes_tiles(int64_t tiles, const TcPlan& p, int64_t M);
+size_t tc_xop_bytes_kbp(int64_t KBP, const TcPlan& p, int64_t M);
+// One tcgen05 launch (pair) over the tiles of up to MMA_GROUP_MAX weights that
+// share K and the activations.
+int launch_tc_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
+                    const TcPlan& plan, const Workspace& ws, cudaStream_t s);
 size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M);
 size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M);
 int tc_launch_count(const TcPlan& p, int64_t M);

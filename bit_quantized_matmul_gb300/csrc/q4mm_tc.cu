@@ -83,9 +83,20 @@ struct Cfg {
   static_assert(NST * STAGE_BYTES >= MTR * TILE_N * 4, "epilogue sums fit over the stages");
 };
 
-struct TcArgs {
+// One weight of a launch.  A launch covers the tiles of up to MMA_GROUP_MAX
+// weights that share K and the activations (the q, k and v projections, or
+// gate and up): global tile t belongs to the last weight whose tile_start <= t.
+struct TcWeight {
   const uint8_t* nib;  // fragment layout
   const uint8_t* scl;
+  float* y;            // [rows of this launch, N], or null (greedy pick)
+  int64_t N;
+  int tile_start;      // first global tile
+};
+
+struct TcArgs {
+  TcWeight w[MMA_GROUP_MAX];
+  int nweights;
   const uint8_t* xop;  // activation operand, [mtiles][KB2][64*NB] bytes
   int64_t KBP, KB2;    // block pairs, padded blocks (2 * KBP)
   int64_t kbp_per_split;
@@ -386,7 +397,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
+  const int mt = blockIdx.x, gtile = blockIdx.y, split = blockIdx.z;
+  int wi = 0;
+#pragma unroll
+  for (int i = 1; i < MMA_GROUP_MAX; ++i)
+    if (i < a.nweights && gtile >= a.w[i].tile_start) wi = i;
+  const int tile = gtile - a.w[wi].tile_start;  // tile within its weight
   const int64_t bp0 = (int64_t)split * a.kbp_per_split;
   const int64_t bp1 = min(a.KBP, bp0 + a.kbp_per_split);
   const int nblk = (int)(2 * (bp1 - bp0));  // includes the zero pad block of an odd count
@@ -417,8 +433,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
     // ---------------- producer ----------------
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");  // the activation operand of the pre-pass
-      const uint8_t* nib_base = a.nib + ((int64_t)tile * a.KBP + bp0) * PAIR_NIB_BYTES;
-      const uint8_t* scl_base = a.scl + ((int64_t)tile * a.KBP + bp0) * PAIR_SCL_BYTES;
+      const uint8_t* nib_base = a.w[wi].nib + ((int64_t)tile * a.KBP + bp0) * PAIR_NIB_BYTES;
+      const uint8_t* scl_base = a.w[wi].scl + ((int64_t)tile * a.KBP + bp0) * PAIR_SCL_BYTES;
       const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB2 + 2 * bp0) * (int64_t)C::BOP_BLOCK;
       int last = -1;
       for (int u = 0; u < nunits; ++u) {
@@ -576,7 +592,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         // last-CTA exchange: the arrival is drawn once the accumulator is
         // complete, so the CTA that draws last is the last to finish and its
         // peers' partial sums are already on their way
-        if (warp == 0 && lane == 0) s_arrival = split_arrive(&a.e.counters[tile * a.mtiles + mt]);
+        if (warp == 0 && lane == 0) s_arrival = split_arrive(&a.e.counters[gtile * a.mtiles + mt]);
         asm volatile("bar.sync 2, 256;" ::: "memory");
       }
       const unsigned arrival = s_arrival;
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         const int S = a.e.splits;
         const int r0 = split * TILE_N / S, r1 = (split + 1) * TILE_N / S;
         const int64_t sstride = a.e.M * a.e.N_pad;
-        unsigned long long* part = a.e.partial + m0 * a.e.N_pad + (int64_t)tile * TILE_N;
+        unsigned long long* part = a.e.partial + m0 * a.e.N_pad + (int64_t)gtile * TILE_N;
         const bool mine = row >= r0 && row < r1;
 #pragma unroll 1
         for (int c = quad; c < nchunk; c += 2) {
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         asm volatile("bar.sync 2, 256;" ::: "memory");
         const int et = warp * 32 + lane;  // 0..255
         if (et == 0) {
-          unsigned* ctr = &a.e.counters[tile * a.mtiles + mt];
+          unsigned* ctr = &a.e.counters[gtile * a.mtiles + mt];
           const unsigned w = split_arrive(ctr);
           if (arrival_last(w, S)) {
             __threadfence();  // every peer's stores are visible before the epoch moves on
@@ -680,10 +696,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
           for (int q = 0; q < OB; ++q) {
             const int o = ob + 256 * q;
             const int64_t n = (int64_t)tile * TILE_N + r0 + o % rows;
-            if (o < outs && n < a.e.N) a.e.y[(m0 + o / rows) * a.e.N + n] = acc[q];
+            if (o < outs && n < a.w[wi].N) a.w[wi].y[(m0 + o / rows) * a.w[wi].N + n] = acc[q];
           }
         }
       } else {
+        // this weight's outputs; partial sums and counters by the global tile
+        EpiArgs e = a.e;
+        e.y = a.w[wi].y;
+        e.N = a.w[wi].N;
+        e.partial = a.e.partial + (int64_t)a.w[wi].tile_start * TILE_N;
 #pragma unroll 1
         for (int c = quad; c < nchunk; c += 2) {
           const int c0 = c * EPI_ROWS;
@@ -695,8 +716,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
 #pragma unroll
           for (int j = 0; j < EPI_ROWS; ++j) val[j] = (t0[j] + t1[j]) + t2[j];
           finish_tile<EPI_ROWS, 1, EPI_ROWS>(
-              a.e, val, row, 0, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split, arrival,
-              c == 0 ? tile * a.mtiles + mt : -1, &s_last[quad], red[quad],
+              e, val, row, 0, tile, m0 + c0, min(EPI_ROWS, mcount - c0), split, arrival,
+              c == 0 ? gtile * a.mtiles + mt : -1, &s_last[quad], red[quad],
               [quad]() { asm volatile("bar.sync %0, 128;" ::"r"(3 + quad) : "memory"); });
         }
       }
@@ -728,12 +749,15 @@ int nb_for(int64_t ml, bool batch_invariant) {
 }
 
 template <int NB>
-int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* idx, float* maxval,
+int launch_nb(const MmaLaunch& L, const float* x, int64_t ml, int32_t* idx, float* maxval,
               const TcPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s) {
   using C = Cfg<NB>;
+  const Weight* W = L.W[0];  // K, KBP and the device are the group's
+  int64_t tiles = 0;
+  for (int i = 0; i < L.count; ++i) tiles += L.W[i]->tiles;
   const int mtiles = (int)((ml + C::MTR - 1) / C::MTR);
   const int64_t KB2 = 2 * W->KBP;
-  if (plan.splits > 1 && W->tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
+  if (plan.splits > 1 && tiles * mtiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   {
     const int64_t total = (int64_t)mtiles * KB2 * 4 * C::MTR;
     const int64_t want = (total + 255) / 256;
@@ -755,8 +779,24 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
     chunks += (rows + EPI_ROWS - 1) / EPI_ROWS;
   }
   TcArgs a;
-  a.nib = W->nib;
-  a.scl = reinterpret_cast<const uint8_t*>(W->d);
+  {
+    int t0 = 0;
+    for (int i = 0; i < MMA_GROUP_MAX; ++i) {
+      if (i < L.count) {
+        const Weight* Wi = L.W[i];
+        a.w[i].nib = Wi->nib;
+        a.w[i].scl = reinterpret_cast<const uint8_t*>(Wi->d);
+        a.w[i].y = L.y[i] ? L.y[i] + mb * Wi->N : nullptr;
+        a.w[i].N = Wi->N;
+        a.w[i].tile_start = t0;
+        t0 += (int)Wi->tiles;
+      } else {
+        a.w[i] = a.w[0];
+        a.w[i].tile_start = 1 << 30;
+      }
+    }
+  }
+  a.nweights = L.count;
   a.xop = static_cast<const uint8_t*>(ws.xop);
   a.KBP = W->KBP;
   a.KB2 = KB2;
@@ -764,9 +804,9 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.mtiles = mtiles;
   a.status = ws.status;
   a.e.N = W->N;
-  a.e.N_pad = W->N_pad;
+  a.e.N_pad = tiles * TILE_N;
   a.e.M = ml;
-  a.e.y = y ? y + mb * W->N : nullptr;
+  a.e.y = a.w[0].y;
   a.e.idx = idx ? idx + mb : nullptr;
   a.e.maxval = (idx && maxval) ? maxval + mb : nullptr;
   a.e.splits = plan.splits;
@@ -775,14 +815,14 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
   a.e.status = ws.status;
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
-  a.e.tiles = (int)(W->tiles * chunks);
+  a.e.tiles = (int)(tiles * chunks);
   // reduce-scatter exchange when every CTA of the launch is resident at once
   // (one CTA per SM), otherwise (and for the greedy pick) the last CTA of a
   // tile adds up all its splits
-  a.rs = plan.splits > 1 && idx == nullptr && mtiles * W->tiles * plan.splits <= plan.num_sms;
+  a.rs = plan.splits > 1 && idx == nullptr && mtiles * tiles * plan.splits <= plan.num_sms;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)mtiles, (unsigned)W->tiles, (unsigned)plan.splits);
+  cfg.gridDim = dim3((unsigned)mtiles, (unsigned)tiles, (unsigned)plan.splits);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
@@ -799,7 +839,7 @@ int launch_nb(const Weight* W, const float* x, int64_t ml, float* y, int32_t* id
 
 bool tc_kernel_built() { return true; }
 
-TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
+TcPlan tc_plan_tiles(int64_t wtiles, int64_t KBP, int64_t M, int num_sms, bool batch_invariant) {
   TcPlan p;
   p.num_sms = num_sms;
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
@@ -808,16 +848,16 @@ TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
   // K partition: fill the SMs, balancing waves against units per CTA (+ a
   // fixed per-CTA cost in unit terms).  It depends on M through the token
   // tiles, except in batch-invariant mode (one token tile of 32 rows assumed).
-  const int64_t tiles = W->tiles * (batch_invariant ? 1 : mtiles);
+  const int64_t tiles = wtiles * (batch_invariant ? 1 : mtiles);
   // at least 16 blocks (four units) per split: the split-K epilogue runs once
   // per 16 token rows of every CTA, so very short K ranges cost more than
   // they save
   int64_t best_s = 1, best_cost = -1;
-  int64_t smax = W->KBP / 8;
+  int64_t smax = KBP / 8;
   if (smax < 1) smax = 1;
   if (smax > 64) smax = 64;
   for (int64_t s = 1; s <= smax; ++s) {
-    const int64_t kbps = (W->KBP + s - 1) / s;  // block pairs per split
+    const int64_t kbps = (KBP + s - 1) / s;  // block pairs per split
     const int64_t waves = (tiles * s + num_sms - 1) / num_sms;
     const int64_t cost = waves * ((2 * kbps + U - 1) / U + 6);
     if (best_cost < 0 || cost < best_cost) {
@@ -825,43 +865,64 @@ TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
       best_s = s;
     }
   }
-  p.kbp_per_split = (W->KBP + best_s - 1) / best_s;
-  p.splits = (int)((W->KBP + p.kbp_per_split - 1) / p.kbp_per_split);
+  p.kbp_per_split = (KBP + best_s - 1) / best_s;
+  p.splits = (int)((KBP + p.kbp_per_split - 1) / p.kbp_per_split);
   return p;
 }
 
-size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M) {
-  if (p.splits <= 1) return 0;
-  const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
-  return (size_t)p.splits * (size_t)ml * (size_t)W->N_pad * sizeof(unsigned long long);
+TcPlan tc_plan(const Weight* W, int64_t M, int num_sms, bool batch_invariant) {
+  return tc_plan_tiles(W->tiles, W->KBP, M, num_sms, batch_invariant);
 }
 
-size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) {
+size_t tc_partial_bytes_tiles(int64_t tiles, const TcPlan& p, int64_t M) {
+  if (p.splits <= 1) return 0;
+  const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
+  return (size_t)p.splits * (size_t)ml * (size_t)(tiles * TILE_N) * sizeof(unsigned long long);
+}
+
+size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M) {
+  return tc_partial_bytes_tiles(W->tiles, p, M);
+}
+
+size_t tc_xop_bytes_kbp(int64_t KBP, const TcPlan& p, int64_t M) {
   const int64_t ml = M < TC_M_LAUNCH ? M : TC_M_LAUNCH;
   const int64_t mtr = p.m_tile / 3;
   const int64_t mtiles = (ml + mtr - 1) / mtr;
-  return (size_t)mtiles * (size_t)(2 * W->KBP) * 64u * (size_t)p.m_tile;
+  return (size_t)mtiles * (size_t)(2 * KBP) * 64u * (size_t)p.m_tile;
 }
+
+size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) { return tc_xop_bytes_kbp(W->KBP, p, M); }
 
 int tc_launch_count(const TcPlan&, int64_t M) {
   return 2 * (int)((M + TC_M_LAUNCH - 1) / TC_M_LAUNCH);
 }
 
-int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
-              const TcPlan& plan, const Workspace& ws, cudaStream_t s) {
+int launch_tc_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
+                    const TcPlan& plan, const Workspace& ws, cudaStream_t s) {
+  const int64_t K = L.W[0]->K;
   for (int64_t mb = 0; mb < M; mb += TC_M_LAUNCH) {
     const int64_t ml = (M - mb) < TC_M_LAUNCH ? (M - mb) : TC_M_LAUNCH;
+    const float* xs = x + mb * K;
     int st;
     switch (plan.m_tile) {
-      case 48: st = launch_nb<48>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      case 96: st = launch_nb<96>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      case 144: st = launch_nb<144>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      case 192: st = launch_nb<192>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
-      default: st = launch_nb<240>(W, x + mb * W->K, ml, y, idx, maxval, plan, ws, mb, s); break;
+      case 48: st = launch_nb<48>(L, xs, ml, idx, maxval, plan, ws, mb, s); break;
+      case 96: st = launch_nb<96>(L, xs, ml, idx, maxval, plan, ws, mb, s); break;
+      case 144: st = launch_nb<144>(L, xs, ml, idx, maxval, plan, ws, mb, s); break;
+      case 192: st = launch_nb<192>(L, xs, ml, idx, maxval, plan, ws, mb, s); break;
+      default: st = launch_nb<240>(L, xs, ml, idx, maxval, plan, ws, mb, s); break;
     }
     if (st) return st;
   }
   return Q4_OK;
+}
+
+int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
+              const TcPlan& plan, const Workspace& ws, cudaStream_t s) {
+  MmaLaunch L;
+  L.count = 1;
+  L.W[0] = W;
+  L.y[0] = y;
+  return launch_tc_group(L, x, M, idx, maxval, plan, ws, s);
 }
 
 }  // namespace q4

@@ -173,7 +173,8 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
  * is bit-identical whatever M is; it may differ in the last bits from a
  * single-weight call of the same W_i.  At or above the group M threshold
  * (q4mm_get_group_m_threshold; without flags) the call runs the tensor-core
- * kernel once per weight instead. */
+ * kernel instead, again as one launch (with its activation pre-pass) over the
+ * tiles of the whole group. */
 Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
                               int64_t M, uint32_t flags, cudaStream_t stream);
 
@@ -299,12 +300,10 @@ Q4_API int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* pa
 Q4_API int q4mm_set_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_m_threshold(void);
 
-/* The M threshold of q4mm_forward_group: at or above it the group runs the
- * tcgen05 kernel once per weight, below it one streaming launch per 8 token
- * rows covers the whole group.  It is higher than the single-call threshold
- * because the grouped streaming launch pays one kernel boundary for several
- * weights; the default is the crossover measured on GB300 over a 7B layer's
- * q/k/v and gate/up groups.  Same range and errors as set_m_threshold. */
+/* The M threshold of q4mm_forward_group: at or above it one tcgen05 launch
+ * covers the whole group, below it one streaming launch per 8 token rows.
+ * The default is the crossover measured on GB300 over a 7B layer's q/k/v and
+ * gate/up groups.  Same range and errors as set_m_threshold. */
 Q4_API int q4mm_set_group_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_group_m_threshold(void);
 
