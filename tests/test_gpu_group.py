@@ -64,14 +64,28 @@ def test_group_batch_invariant_rows():
         W.free()
 
 
-def test_group_above_threshold_uses_per_weight_calls():
-    Ws, blocks = _group([(300, 1024), (256, 1024)], 98)
-    M = q4.q4mm_get_group_m_threshold() + 3
-    x_np = acts(98, M, 1024)
-    ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x_np).cuda())
-    for y, b in zip(ys, blocks):
-        _, y64, bound = oracle.matmul(b, x_np)
-        assert_within_bound(y.cpu().numpy(), y64, bound, "group M=%d" % M)
+@pytest.mark.parametrize("shapes,Ms", [
+    ([(300, 1024), (256, 1024)], (3, 40)),                    # ragged first weight
+    ([(1000, 3584), (130, 3584), (130, 3584)], (1, 17, 64)),  # q/k/v-like: 8 + 2 + 2 tiles, ragged
+    ([(2000, 2048), (2000, 2048)], (33, 300)),                # gate/up-like; two launch pairs at 300
+])
+def test_group_above_threshold_one_tensor_core_launch(shapes, Ms):
+    # at or above the group threshold one tcgen05 launch covers every tile of
+    # the group: each tile's weight, output and partial-sum slots come from
+    # the global tile index
+    Ws, blocks = _group(shapes, 98)
+    thr = q4.q4mm_get_group_m_threshold()
+    try:
+        q4.q4mm_set_group_m_threshold(1)  # every M below on the grouped tensor-core path
+        for M in Ms:
+            x_np = acts(98, M, shapes[0][1])
+            ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x_np).cuda())
+            for i, (y, b) in enumerate(zip(ys, blocks)):
+                _, y64, bound = oracle.matmul(b, x_np)
+                assert_within_bound(y.cpu().numpy(), y64, bound, "group weight %d M=%d" % (i, M))
+    finally:
+        q4.q4mm_set_group_m_threshold(thr)
+    assert q4.q4_device_status() == q4.Q4_OK
     for W in Ws:
         W.free()
 
