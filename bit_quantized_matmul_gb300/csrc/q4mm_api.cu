@@ -39,9 +39,10 @@ DeviceScratch g_dev[MAX_DEVICES];
 
 // Below this M the streaming mma.sync kernel is used, at or above it the
 // tcgen05 kernel.  Measured on GB300 over one Qwen2.5-7B decoder layer's seven
-// linears (bench.py --path-sweep, M in 1..256): the streaming kernel is faster
-// for the whole layer up to M = 8, the tensor-core kernel from M = 16.
-constexpr int64_t DEFAULT_M_THRESHOLD = 16;
+// linears as single calls (bench.py --path-sweep, M in 1..256): the streaming
+// kernel is faster for the whole layer up to M = 16 (161.0 against 170.7 us),
+// the tensor-core kernel from M = 24 (172.6 against 240.1 us).
+constexpr int64_t DEFAULT_M_THRESHOLD = 24;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 // Grouped calls (q4mm_forward_group) run one launch over the whole group on
 // either path.  Measured the same way over a layer's q/k/v and gate/up groups:
