@@ -254,6 +254,7 @@ def run_gpu(args):
             N, _ = synthetic.QWEN7B_LINEARS[name]
             ys[(M, name)] = torch.empty((M, N), dtype=torch.float32, device=dev)
     groups = tuple((n, (n,)) for n in TYPES) if args.separate else GROUPS
+    flags = q4.Q4MM_BATCH_INVARIANT if args.batch_invariant else 0
 
     def issue(M, gname):
         names = dict(groups)[gname]
@@ -261,10 +262,10 @@ def run_gpu(args):
         x = xs[(M, K)]
         for layer in range(layers):
             if len(names) == 1:
-                q4.q4mm_forward(stack[names[0]][layer], x, y=ys[(M, names[0])], stream=stream)
+                q4.q4mm_forward_ex(stack[names[0]][layer], x, flags, y=ys[(M, names[0])], stream=stream)
             else:
                 q4.q4mm_forward_group([stack[n][layer] for n in names], x,
-                                      ys=[ys[(M, n)] for n in names], stream=stream)
+                                      ys=[ys[(M, n)] for n in names], flags=flags, stream=stream)
 
     # warm the library (scratch allocation) before capture
     with torch.cuda.stream(stream):
@@ -286,11 +287,12 @@ def run_gpu(args):
     launches_per_step = 0
     for M in msw:
         for gname, names in groups:
-            if len(names) > 1 and M < q4.q4mm_get_group_m_threshold():
-                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M, q4.Q4MM_FORCE_MMA)  # one launch for the group
+            if len(names) > 1:
+                # one launch (pair) covers the group on either path
+                grp = flags or (q4.Q4MM_FORCE_MMA if M < q4.q4mm_get_group_m_threshold() else 0)
+                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M, grp)
             else:
-                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M)
-                l *= len(names)  # single calls, or one call per weight of a group
+                _, l, _ = q4.q4mm_plan_info(stack[names[0]][0], M, flags)
             launches[(M, gname)] = l
             launches_per_step += l * layers
 
@@ -360,7 +362,7 @@ def run_gpu(args):
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     traffic = None
     if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash() and \
-            TRAFFIC.get("grouped") == (not args.separate) and \
+            TRAFFIC.get("grouped") == (not args.separate) and not args.batch_invariant and \
             TRAFFIC.get("m_sweep", list(M_SWEEP)) == list(msw):
         traffic = TRAFFIC.get("bytes_per_launch")
     per_m = {}
@@ -424,6 +426,7 @@ def run_gpu(args):
                              % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "calls_per_layer": [g for g, _ in groups],
+                       "mode": "batch-invariant" if args.batch_invariant else "default",
                        "m_threshold": q4.q4mm_get_m_threshold(),
                        "group_m_threshold": q4.q4mm_get_group_m_threshold()},
             "token_rows_per_s": sum(msw) * world / (ms_per_step * 1e-3),
@@ -580,6 +583,75 @@ def run_path_sweep(args):
     return 0
 
 
+def run_lm_head(args):
+    """Fused greedy pick (q4mm_argmax) on the Qwen2.5-7B LM head, 152064 x 3584
+    Q4_0 (N(0, 0.02^2) weights, fp32 N(0,1) activations), at M = 1, 4, 16.
+    Two weight copies (612 MB, far beyond L2) alternate between calls.  Prints
+    one JSON line; GB/s counts packed weight bytes."""
+    import numpy as np
+    import torch
+
+    import bit_quantized_matmul_gb300 as q4
+    import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, K = synthetic.LM_HEAD
+    Ws = []
+    for c in range(2):
+        w = torch.from_numpy(synthetic.normal(synthetic.weight_seed(3, 10 + c), (N, K), sigma=0.02)).to(dev)
+        Ws.append(q4.q4_quantize(w))
+        del w
+    wbytes = N * K * BLOCK_BYTES_PER_WEIGHT
+    stream = torch.cuda.Stream(dev)
+    peak, kind = _peaks()
+    cases = {}
+    for M in (1, 4, 16):
+        x = torch.from_numpy(synthetic.normal(synthetic.act_seed(3, M), (M, K))).to(dev)
+        idx = torch.empty((M,), dtype=torch.int32, device=dev)
+        mx = torch.empty((M,), dtype=torch.float32, device=dev)
+        lib = q4.raw_library()
+        reps = 20
+
+        def issue():
+            for r in range(reps):
+                st = lib.q4mm_argmax(Ws[r % 2].handle, x.data_ptr(), idx.data_ptr(), mx.data_ptr(), M,
+                                     stream.cuda_stream)
+                assert st == q4.Q4_OK, st
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                issue()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                issue()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(max(1, args.steps)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)
+        us = statistics.median(times)
+        path = q4.q4mm_plan_info(Ws[0], M)[0]
+        cases[str(M)] = {"us_per_call": us, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
+                         "frac_of_measured_hbm": wbytes / (us * 1e-6) / 1e9 / peak,
+                         "token_rows_per_s": M / (us * 1e-6), "path": int(path)}
+    assert q4.q4_device_status() == q4.Q4_OK
+    line = {"metric": "LM-head greedy pick (fused argmax) weight GB/s", "unit": "GB/s",
+            "value": cases["1"]["weight_gbs"], "n_gpus": 1, "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "qwen2.5-7b LM head 152064x3584 Q4_0, M = 1, 4, 16, fused argmax "
+                                   "(no logits written)", "l2": "two weight copies (612 MB) alternate"},
+            "cases": cases, "peak_gbs": peak, "peak_source": kind}
+    print(json.dumps(line), flush=True)
+    for W in Ws:
+        W.free()
+    return 0
+
+
 def run_kv_append(args):
     """KV-cache append of a Qwen2.5-0.5B-shaped cache (24 layers, 2 KV heads,
     head_dim 64, bf16): a 2,049-row prefill into one slot and a decode step of
@@ -658,11 +730,17 @@ def main():
                     help="one call per linear instead of grouping q/k/v and gate/up")
     ap.add_argument("--path-sweep", action="store_true",
                     help="time both kernel paths per M and print the measured M threshold")
+    ap.add_argument("--batch-invariant", action="store_true",
+                    help="run every call of the step in batch-invariant mode (Q4MM_BATCH_INVARIANT)")
+    ap.add_argument("--lm-head", action="store_true",
+                    help="time the fused greedy pick (q4mm_argmax) on the LM head instead of the step")
     ap.add_argument("--kv-append", action="store_true",
                     help="time the KV-cache append (q4_kv_append) instead of the matmul step")
     args = ap.parse_args()
     if args.kv_append:
         return run_kv_append(args)
+    if args.lm_head:
+        return run_lm_head(args)
     if args.path_sweep:
         return run_path_sweep(args)
     if args.impl == "reference":
