@@ -94,6 +94,7 @@ int quantize_flag_status(unsigned flag);
 struct MmaPlan {
   int splits;
   int64_t kbp_per_split;  // block pairs per split
+  int num_sms = 0;        // SMs the plan was made for (0: unknown)
 };
 
 // mma.sync streaming kernel (small and medium M).  One launch may cover up to

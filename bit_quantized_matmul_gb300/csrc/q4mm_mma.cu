@@ -31,6 +31,12 @@
 //                     (every wait bounded).  The fp32 rows arrive by cp.async
 //                     four or five chunks ahead.
 //
+// Launches of more tiles than SMs with one K split (the gate/up group of a 7B
+// layer: 296 tiles) and one or two column groups run as two-tile CTAs: a CTA
+// streams tiles 2b and 2b + 1 over the whole K, its warps covering the same
+// row groups of both and its converted activations serving both, so the
+// launch is one wave instead of two.
+//
 // Short-K launches whose tiles x 4 fit on the SMs (the q/k/v group and o_proj
 // of a 7B layer) run as row-group CTAs instead: a CTA takes one row-group pair
 // (32 rows) of a tile over the whole K, and its 16 compute warps are 16 K
@@ -84,7 +90,11 @@ constexpr int NSLOT = 4;                    // ring depth (a power of two)
 #ifndef Q4MM_RG_MAX_K
 #define Q4MM_RG_MAX_K 4096
 #endif
+#ifndef Q4MM_TWO_TILES
+#define Q4MM_TWO_TILES 1
+#endif
 constexpr int RG_LD = 36;  // row stride of the row-group slice sums (32 rows + 4)
+constexpr int T2_LD = 2 * TILE_N + 4;  // row stride of the two-tile slice sums (256 rows + 4)
 // row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
 // the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
 // 32 different banks and the per-row reads stay consecutive
@@ -115,7 +125,7 @@ struct MmaArgs {
   EpiArgs e;
 };
 
-template <int C>
+template <int C, int TPC = 1>
 struct MmaCfg {
   static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
   static constexpr int BF_PAIR = C * 1024;  // B fragments of a pair: [cg][h][32 slots] x 16 B
@@ -134,7 +144,7 @@ struct MmaCfg {
   static constexpr int WD = Q4MM_WD;
   static constexpr int WSLOT = 1024 + 128;
   static constexpr int WR_OFF = RING + XSTAGES * XSLOT;
-  static constexpr int WR = COMPUTE_WARPS * WD * WSLOT;
+  static constexpr int WR = COMPUTE_WARPS * WD * WSLOT * TPC;
   static constexpr int BAR_OFF = WR_OFF + WR > XCH_OFF + XCH ? WR_OFF + WR : XCH_OFF + XCH;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
@@ -283,9 +293,9 @@ __device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_
 // reads its 512 contiguous bytes conflict-free in any slot order).  The slot
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
-template <int C, bool DENSE, bool RG>
+template <int C, bool DENSE, bool RG, int TPC>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
-  using S = MmaCfg<C>;
+  using S = MmaCfg<C, TPC>;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -300,12 +310,21 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // over the whole K, and its 16 compute warps are 16 K slices; otherwise the
   // CTA is global tile blockIdx.x over K split blockIdx.y, its compute warps
   // 4 row-group pairs x 4 K slices
-  const int gtile = RG ? (int)(blockIdx.x >> 2) : (int)blockIdx.x;
+  // TPC = 2: the CTA takes global tiles 2 blockIdx.x and 2 blockIdx.x + 1 (the
+  // second when it exists) over the whole K; its warps cover the same row
+  // groups of both, and the converted activations serve both
+  const int gtile = RG ? (int)(blockIdx.x >> 2) : (int)blockIdx.x * TPC;
   int wi = 0;
 #pragma unroll
   for (int i = 1; i < MMA_GROUP_MAX; ++i)
     if (i < a.nweights && gtile >= a.w[i].tile_start) wi = i;
   const int64_t tile = (int64_t)gtile - a.w[wi].tile_start;  // tile within its weight
+  const bool has1 = TPC == 2 && (int64_t)gtile + 1 < a.e.N_pad / TILE_N;  // second tile
+  int wi1 = wi;
+#pragma unroll
+  for (int i = 1; i < MMA_GROUP_MAX; ++i)
+    if (i < a.nweights && gtile + 1 >= a.w[i].tile_start) wi1 = i;
+  const int64_t tile1 = (int64_t)gtile + 1 - a.w[wi1].tile_start;
   const uint4* nib_w = a.w[wi].nib;
   const uint8_t* scl_w = a.w[wi].scl;
   const int split = blockIdx.y;
@@ -329,18 +348,26 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   const int sl = RG ? (warp & (COMPUTE_WARPS - 1)) : ((warp >> 2) & 3);
   const int n_i = (compute && npairs > sl) ? (npairs - sl + NSL - 1) / NSL : 0;
   const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
+  const uint4* wp1 = a.w[wi1].nib + ((tile1 * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
   constexpr int64_t WSTEP = NSL * 8 * 32;  // uint4 between a slice's consecutive pairs
   // ring slot j of this warp: [row group 2rgp, 2rgp + 1][lane][16 B] of
   // nibbles, then the 128 scale bytes of the two row groups ([rg][g][4 x fp16])
-  const uint32_t wring = smem_u32(smem + S::WR_OFF + warp * (WD * S::WSLOT));
+  // (with two tiles per CTA a slot holds the first tile's 1152 bytes, then the second's)
+  const uint32_t wring = smem_u32(smem + S::WR_OFF + warp * (WD * S::WSLOT * TPC));
   const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
+  const uint8_t* sp1 = a.w[wi1].scl + (tile1 * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
   constexpr int64_t SSTEP = NSL * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
   auto fetch = [&](int i) {  // pair i of this warp's K slice into slot i % WD
     if (i < n_i) {
-      const uint32_t d = wring + (uint32_t)(i % WD) * S::WSLOT;
+      const uint32_t d = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC);
       cp_async16(d + lane * 16, wp + (int64_t)i * WSTEP);
       cp_async16(d + 512u + lane * 16, wp + (int64_t)i * WSTEP + 32);
       if (lane < 8) cp_async16(d + 1024u + lane * 16, sp + (int64_t)i * SSTEP);
+      if (TPC == 2 && has1) {
+        cp_async16(d + S::WSLOT + lane * 16, wp1 + (int64_t)i * WSTEP);
+        cp_async16(d + S::WSLOT + 512u + lane * 16, wp1 + (int64_t)i * WSTEP + 32);
+        if (lane < 8) cp_async16(d + S::WSLOT + 1024u + lane * 16, sp1 + (int64_t)i * SSTEP);
+      }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");  // one group per pair, empty or not
   };
@@ -384,16 +411,18 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // (packed fp32x2 updates) up to two column groups; as four floats [rg][cg][e]
   // for three, where the extra registers of the packed form would spill
   constexpr bool PACKED = C <= 2;
-  unsigned long long acc[2][C][2];
-  float accf[2][C][4];
+  unsigned long long acc[TPC][2][C][2];
+  float accf[TPC][2][C][4];
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
+  for (int tt = 0; tt < TPC; ++tt)
 #pragma unroll
-    for (int cg = 0; cg < C; ++cg) {
-      acc[r][cg][0] = acc[r][cg][1] = 0ull;
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) accf[r][cg][e] = 0.0f;
-    }
+      for (int cg = 0; cg < C; ++cg) {
+        acc[tt][r][cg][0] = acc[tt][r][cg][1] = 0ull;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accf[tt][r][cg][e] = 0.0f;
+      }
 
   if (compute) {
     const int g = lane >> 2;
@@ -402,10 +431,12 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     // the 16-byte words and scales of pair i of this warp, once they are in
     // (this lane's groups complete in order, WD - 1 may still fly; the warp
     // barrier makes lanes 0..7's scale copies visible to all lanes)
-    auto load_pair = [&](int i, uint4& a0, uint4& a1, uint2& s0, uint2& s1) {
-      asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
-      __syncwarp();
-      const uint32_t src = wring + (uint32_t)(i % WD) * S::WSLOT;
+    auto load_pair = [&](int i, int tt, uint4& a0, uint4& a1, uint2& s0, uint2& s1) {
+      if (tt == 0) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
+        __syncwarp();
+      }
+      const uint32_t src = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC) + (uint32_t)(tt * S::WSLOT);
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(a0.x), "=r"(a0.y), "=r"(a0.z), "=r"(a0.w) : "r"(src + lane * 16) : "memory");
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -428,11 +459,14 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           s_err = 1;
           goto compute_done;
         }
-        uint4 w0, w1;
-        uint2 sv0, sv1;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
-        load_pair(i, w0, w1, sv0, sv1);
         const int pc = RG ? (sl & 7) : (sl + 4 * (i & 1));  // pair within the chunk
         const uint8_t* sb = smem + slot * S::SLOT;
+#pragma unroll
+        for (int tt = 0; tt < TPC; ++tt) {
+        if (tt == 1 && !has1) break;  // the same for every thread of the CTA
+        uint4 w0, w1;
+        uint2 sv0, sv1;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
+        load_pair(i, tt, w0, w1, sv0, sv1);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t a00[4], a01[4], a10[4], a11[4];  // [rg][k-step]
@@ -446,8 +480,10 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             a11[p] = nib_pair(y1, p);
           }
           // refill the slot once every lane has unpacked both its words (the
-          // shared loads have completed, so the copy cannot overtake them)
-          if (h == 1) {
+          // shared loads have completed, so the copy cannot overtake them);
+          // with two tiles, after the second tile's words (or the first's
+          // when there is no second)
+          if (h == 1 && (TPC == 1 || tt == 1 || !has1)) {
             __syncwarp();
             fetch(i + WD);
           }
@@ -472,27 +508,28 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             mma_bf16_first(d, a00, bf.x, bf.y);
             mma_bf16_acc(d, a01, bf.z, bf.w);
             if constexpr (PACKED) {
-              ffma2(acc[0][cg][0], s00, d[0], d[1]);
-              ffma2(acc[0][cg][1], s01, d[2], d[3]);
+              ffma2(acc[tt][0][cg][0], s00, d[0], d[1]);
+              ffma2(acc[tt][0][cg][1], s01, d[2], d[3]);
             } else {
-              accf[0][cg][0] = fmaf(f00, d[0], accf[0][cg][0]);
-              accf[0][cg][1] = fmaf(f00, d[1], accf[0][cg][1]);
-              accf[0][cg][2] = fmaf(f01, d[2], accf[0][cg][2]);
-              accf[0][cg][3] = fmaf(f01, d[3], accf[0][cg][3]);
+              accf[tt][0][cg][0] = fmaf(f00, d[0], accf[tt][0][cg][0]);
+              accf[tt][0][cg][1] = fmaf(f00, d[1], accf[tt][0][cg][1]);
+              accf[tt][0][cg][2] = fmaf(f01, d[2], accf[tt][0][cg][2]);
+              accf[tt][0][cg][3] = fmaf(f01, d[3], accf[tt][0][cg][3]);
             }
             float e[4];
             mma_bf16_first(e, a10, bf.x, bf.y);
             mma_bf16_acc(e, a11, bf.z, bf.w);
             if constexpr (PACKED) {
-              ffma2(acc[1][cg][0], s10, e[0], e[1]);
-              ffma2(acc[1][cg][1], s11, e[2], e[3]);
+              ffma2(acc[tt][1][cg][0], s10, e[0], e[1]);
+              ffma2(acc[tt][1][cg][1], s11, e[2], e[3]);
             } else {
-              accf[1][cg][0] = fmaf(f10, e[0], accf[1][cg][0]);
-              accf[1][cg][1] = fmaf(f10, e[1], accf[1][cg][1]);
-              accf[1][cg][2] = fmaf(f11, e[2], accf[1][cg][2]);
-              accf[1][cg][3] = fmaf(f11, e[3], accf[1][cg][3]);
+              accf[tt][1][cg][0] = fmaf(f10, e[0], accf[tt][1][cg][0]);
+              accf[tt][1][cg][1] = fmaf(f10, e[1], accf[tt][1][cg][1]);
+              accf[tt][1][cg][2] = fmaf(f11, e[2], accf[tt][1][cg][2]);
+              accf[tt][1][cg][3] = fmaf(f11, e[3], accf[tt][1][cg][3]);
             }
           }
+        }
         }
         if ((RG || (i & 1)) && c + NSLOT < nchunks) {  // this warp is done with the slot
           __syncwarp();
@@ -612,6 +649,58 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     return;
   }
 
+  if constexpr (TPC == 2) {
+    // ---- two tiles, whole K: add the four K slices in shared memory, write y ----
+    float* red = reinterpret_cast<float*>(smem);  // [SLICES][C*8 columns][T2_LD]
+    constexpr int RS = C * 8 * T2_LD;
+    if (compute) {
+      const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int cg = 0; cg < C; ++cg)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v;
+              if constexpr (PACKED) {
+                const float2 pr = split2(acc[tt][r][cg][e >> 1]);
+                v = (e & 1) ? pr.y : pr.x;
+              } else {
+                v = accf[tt][r][cg][e];
+              }
+              red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * T2_LD + tt * TILE_N + (2 * rgp + r) * 16 + g +
+                  8 * (e >> 1)] = v;
+            }
+    }
+    __syncthreads();
+    // thread t < 512: row t % 256 of the two tiles, token rows t / 256 + 2k;
+    // fixed order of terms and slices, as on the other paths
+    if (tid < 2 * 2 * TILE_N) {
+      const int row = tid & (2 * TILE_N - 1);
+      const int tt = row >> 7;
+      if (tt == 0 || has1) {
+        const int ww = tt ? wi1 : wi;
+        const int64_t n = (tt ? tile1 : tile) * TILE_N + (row & (TILE_N - 1));
+        float* y = a.w[ww].y;
+        const int64_t N = a.w[ww].N;
+        if (n < N) {
+          for (int m = tid >> 8; m < mrows; m += 2) {
+            const int c0 = DENSE ? 3 * m : 8 * m;
+            float v = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * T2_LD + row];
+            y[(int64_t)m * N + n] = v;
+          }
+        }
+      }
+    }
+    return;
+  }
+
   if constexpr (RG) {
     // ---- row-group CTA: add the 16 K slices in shared memory and write y ----
     float* red = reinterpret_cast<float*>(smem);  // [16 slices][C*8 columns][RG_LD]
@@ -626,10 +715,10 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           for (int e = 0; e < 4; ++e) {
             float v;
             if constexpr (PACKED) {
-              const float2 pr = split2(acc[r][cg][e >> 1]);
+              const float2 pr = split2(acc[0][r][cg][e >> 1]);
               v = (e & 1) ? pr.y : pr.x;
             } else {
-              v = accf[r][cg][e];
+              v = accf[0][r][cg][e];
             }
             red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RG_LD + r * 16 + g + 8 * (e >> 1)] = v;
           }
@@ -667,10 +756,10 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         for (int e = 0; e < 4; ++e) {
           float v;
           if constexpr (PACKED) {
-            const float2 pr = split2(acc[r][cg][e >> 1]);
+            const float2 pr = split2(acc[0][r][cg][e >> 1]);
             v = (e & 1) ? pr.y : pr.x;
           } else {
-            v = accf[r][cg][e];
+            v = accf[0][r][cg][e];
           }
           red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RED_LD + (2 * rgp + r) * 16 + g +
               8 * (e >> 1)] = v;
@@ -762,7 +851,7 @@ int cluster_capacity(int device, int size) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
-  cfg.dynamicSmemBytes = MmaCfg<C>::BYTES;
+  cfg.dynamicSmemBytes = MmaCfg<C, 1>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -771,7 +860,7 @@ int cluster_capacity(int device, int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE, false, 1>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -779,11 +868,11 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
-template <int C, bool DENSE, bool RG>
+template <int C, bool DENSE, bool RG, int TPC = 1>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
-  using S = MmaCfg<C>;
+  using S = MmaCfg<C, TPC>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
   int tiles = 0;
@@ -825,7 +914,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.e.tiles = tiles;
   static bool attr_set[64] = {};
   if (!attr_set[W0->device & 63]) {
-    if (cudaFuncSetAttribute(mma_kernel<C, DENSE, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, DENSE, RG, TPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63] = true;
@@ -836,10 +925,11 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // memory.  Both add the splits in the same order.  (Measured on GB300 for
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
-  a.cluster = !RG && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
+  a.cluster = !RG && TPC == 1 && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
               tiles <= cluster_capacity<C, DENSE>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1) : dim3((unsigned)tiles, (unsigned)plan.splits, 1);
+  cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
+                   : dim3((unsigned)((tiles + TPC - 1) / TPC), (unsigned)plan.splits, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
@@ -852,7 +942,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE, RG>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE, RG, TPC>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 // Rows per launch: 8 with dense packing (3 column groups), 3 with one row per
@@ -866,6 +956,7 @@ MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms) {
   // floor(SMs / tiles) for a single wave, at least one, and small enough that
   // each CTA keeps at least two block pairs.
   MmaPlan p;
+  p.num_sms = num_sms;
   int64_t sp = (int64_t)num_sms / tiles;
   int64_t cap = KBP / 2;
   if (cap < 1) cap = 1;
@@ -911,6 +1002,11 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   // per tile fit on the SMs (the split plan has at least 4 splits) and K is
   // short; the plan depends on the shapes only (y output, default mode)
   const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr);
+  // two tiles per CTA (whole K, no split): launches of more tiles than SMs
+  // run as one wave of CTAs that stream two tiles each, for one or two column
+  // groups with y output in default mode
+  const bool two = Q4MM_TWO_TILES && !batch_invariant && idx == nullptr && xrows == nullptr &&
+                   plan.splits == 1 && plan.num_sms > 0 && tiles > plan.num_sms;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     const float* xs = xrows ? x : x + mb * K;
@@ -932,8 +1028,14 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
         }
       } else {
         switch (cgs) {
-          case 1: st = launch_c<1, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-          case 2: st = launch_c<2, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          case 1:
+            st = two ? launch_c<1, true, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                     : launch_c<1, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+            break;
+          case 2:
+            st = two ? launch_c<2, true, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                     : launch_c<2, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+            break;
           default: st = launch_c<3, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
         }
       }

@@ -135,3 +135,32 @@ def test_alternating_shapes_share_counter_slots(q4):
     assert q4.q4_device_status() == q4.Q4_OK
     for p in prepared:
         p[0].free()
+
+
+@pytest.mark.parametrize("shapes", [
+    [(155 * 128 - 37, 1024)],                 # 155 tiles (odd), ragged last tile
+    [(153 * 128 - 5, 1024), (300, 1024)],     # a CTA's two tiles in different weights
+])
+def test_two_tile_ctas_match_oracle(q4, shapes):
+    # more tiles than SMs and one K split: each CTA streams two tiles over the
+    # whole K (one or two column groups); three groups keep one tile per CTA
+    Ws, blocks = [], []
+    for i, (N, KK) in enumerate(shapes):
+        w = weights(74, i, N, KK)
+        Ws.append(q4.q4_quantize(torch.from_numpy(w).to(DEV)))
+        blocks.append(oracle.quantize(w))
+    _, _, s = q4.q4mm_plan_info(Ws[0], 1, q4.Q4MM_FORCE_MMA)
+    assert s == 1
+    for M in (1, 2, 3, 5, 8, 11):
+        x = acts(74, M, shapes[0][1], salt=len(shapes))
+        xd = torch.from_numpy(x).to(DEV)
+        if len(Ws) == 1:
+            ys = [q4.q4mm_forward_ex(Ws[0], xd, q4.Q4MM_FORCE_MMA)]
+        else:
+            ys = q4.q4mm_forward_group(Ws, xd, flags=q4.Q4MM_FORCE_MMA)
+        for i, (y, b) in enumerate(zip(ys, blocks)):
+            _, y64, bound = oracle.matmul(b, x)
+            assert_within_bound(y.cpu().numpy(), y64, bound, "two tiles weight %d M=%d" % (i, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    for W in Ws:
+        W.free()
