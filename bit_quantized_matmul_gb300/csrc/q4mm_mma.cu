@@ -675,6 +675,37 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             }
     }
     __syncthreads();
+    if (a.e.idx != nullptr) {
+      // greedy pick: per tile, thread tid owns row tid % 128 for token rows
+      // tid / 128 + 5k (as on the one-tile path), then the tile's maximum
+      constexpr int MG = KERNEL_THREADS / TILE_N;
+      constexpr int MT = (MAXM + MG - 1) / MG;
+      const int row = tid % TILE_N, mfirst = tid / TILE_N;
+#pragma unroll 1
+      for (int tt = 0; tt < 2; ++tt) {
+        if (tt == 1 && !has1) break;  // the same for every thread of the CTA
+        float val[MT];
+#pragma unroll
+        for (int k = 0; k < MT; ++k) {
+          const int m = mfirst + k * MG;
+          val[k] = 0.0f;
+          if (m < mrows) {
+            const int c0 = DENSE ? 3 * m : 8 * m;
+            float v = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * T2_LD + tt * TILE_N + row];
+            val[k] = v;
+          }
+        }
+        EpiArgs e = a.e;
+        e.N = a.w[tt ? wi1 : wi].N;
+        finish_tile<MT, MG, MAXM>(e, val, row, mfirst, tt ? tile1 : tile, 0, mrows, 0, 0u, -1, &s_flag,
+                                  kred, []() { __syncthreads(); });
+      }
+      return;
+    }
     // thread t < 512: row t % 256 of the two tiles, token rows t / 256 + 2k;
     // fixed order of terms and slices, as on the other paths
     if (tid < 2 * 2 * TILE_N) {
@@ -1003,10 +1034,10 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   // short; the plan depends on the shapes only (y output, default mode)
   const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr);
   // two tiles per CTA (whole K, no split): launches of more tiles than SMs
-  // run as one wave of CTAs that stream two tiles each, for one or two column
-  // groups with y output in default mode
-  const bool two = Q4MM_TWO_TILES && !batch_invariant && idx == nullptr && xrows == nullptr &&
-                   plan.splits == 1 && plan.num_sms > 0 && tiles > plan.num_sms;
+  // run as CTAs that stream two tiles each, for one or two column groups in
+  // default mode (y output or the greedy pick)
+  const bool two = Q4MM_TWO_TILES && !batch_invariant && plan.splits == 1 && plan.num_sms > 0 &&
+                   tiles > plan.num_sms;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     const float* xs = xrows ? x : x + mb * K;

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import acts, assert_within_bound, weights
+from gpu_helpers import acts, assert_within_bound, plant_near_ties, weights
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -164,3 +164,43 @@ def test_two_tile_ctas_match_oracle(q4, shapes):
     assert q4.q4_device_status() == q4.Q4_OK
     for W in Ws:
         W.free()
+
+
+def test_two_tile_ctas_greedy_pick_matches_oracle(q4):
+    # the greedy pick on two-tile CTAs: 155 tiles on 78 CTAs (the last with
+    # one tile), each tile folded into the per-row maximum on its own.  Rows
+    # 70 and 200 (two tiles of the first CTA) and 19750 (the lone last tile)
+    # hold the same weights, so an exact tie across tiles picks row 70.
+    N, KK = 155 * 128 - 37, 1024
+    w = weights(75, 0, N, KK)
+    w[200] = w[70]
+    w[19750] = w[70]
+    blocks = oracle.quantize(w)
+    W = q4.q4_quantize(torch.from_numpy(w).to(DEV))
+    _, _, s = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
+    assert s == 1
+    rng = np.random.default_rng(75)
+    for M in (1, 2, 5, 8, 11):
+        x = acts(75, M, KK)
+        x, planted = plant_near_ties(blocks, x, list(range(1, M, 2)), rng)
+        wd = oracle.dequantize(blocks[[70]]).astype(np.float64)[0]
+        x[0] = (wd / np.linalg.norm(wd) * 40).astype(np.float32)  # row 0: the exact tie
+        xd = torch.from_numpy(x).to(DEV)
+        idx, mx = q4.q4mm_argmax_ex(W, xd, q4.Q4MM_FORCE_MMA)
+        idx, mx = idx.cpu().numpy(), mx.cpu().numpy()
+        _, y64, bound = oracle.matmul(blocks, x)
+        assert idx[0] == 70, M
+        for m in range(M):
+            top = np.argsort(-y64[m], kind="stable")
+            margin = y64[m, top[0]] - y64[m, top[1]]
+            if m in planted:
+                assert margin > bound[m, top[0]] + bound[m, top[1]], "planted gap below the bound"
+            if margin > bound[m, top[0]] + bound[m, top[1]]:
+                assert idx[m] == top[0], (M, m)
+            assert abs(float(mx[m]) - y64[m, idx[m]]) <= bound[m, idx[m]]
+        # the same sums as the call that writes y (both on two-tile CTAs)
+        yf = q4.q4mm_forward_ex(W, xd, q4.Q4MM_FORCE_MMA).cpu().numpy()
+        assert np.array_equal(np.argmax(yf, axis=1), idx)
+        assert np.array_equal(yf.max(axis=1).view(np.uint32), mx.view(np.uint32))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
