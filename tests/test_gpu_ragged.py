@@ -42,6 +42,35 @@ def test_argmax_rows_matches_oracle_and_gathered_call():
     W.free()
 
 
+def test_argmax_rows_on_two_tile_ctas():
+    # a head of more tiles than SMs with one K split (155 tiles, K = 1024)
+    # runs the row-list pick on CTAs that stream two tiles each
+    N, K = 155 * 128 - 37, 1024
+    w = weights(123, 0, N, K)
+    blocks = oracle.quantize(w)
+    W = q4.q4_quantize(torch.from_numpy(w).cuda())
+    _, _, splits = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
+    assert splits == 1
+    x_np = acts(123, 30, K)
+    x = torch.from_numpy(x_np).cuda()
+    for sel in ([29], [3, 7, 7, 0, 12], list(range(29, 0, -3))):
+        rows = torch.tensor(sel, dtype=torch.int32, device="cuda")
+        idx, mx = q4.q4mm_argmax_rows(W, x, rows)
+        ref_idx, y64, bound = _oracle_argmax(blocks, x_np[sel])
+        got, gmx = idx.cpu().numpy(), mx.cpu().numpy()
+        for r in range(len(sel)):
+            top = np.sort(y64[r])[::-1]
+            if top[0] - top[1] > bound[r].max():
+                assert got[r] == ref_idx[r], (sel, r)
+            else:
+                assert y64[r, got[r]] >= top[0] - bound[r, got[r]]
+            assert abs(float(gmx[r]) - y64[r, got[r]]) <= bound[r, got[r]]
+        gi, gm = q4.q4mm_argmax(W, x[sel].contiguous())
+        assert torch.equal(gi, idx) and torch.equal(gm.view(torch.int32), mx.view(torch.int32))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()
+
+
 def test_argmax_rows_out_of_range_index_is_reported_not_read():
     N, K = 300, 256
     W = q4.q4_quantize(torch.from_numpy(weights(121, 0, N, K)).cuda())
