@@ -532,7 +532,7 @@ def run_path_sweep(args):
                 torch.cuda.synchronize(dev)
                 return a.elapsed_time(b) * 1e3 / (5 * layers)
 
-            # streaming: one launch per 8 rows over the group; tensor cores:
+            # streaming: one launch per 16 rows over the group; tensor cores:
             # one launch pair over the group (the group threshold forced to 1)
             rec = {"mma_group_us": time_group(q4.Q4MM_FORCE_MMA)}
             old_thr = q4.q4mm_get_group_m_threshold()

@@ -33,7 +33,7 @@ Q4MM_ROW_BY_ROW = 0x8
 Q4MM_FORCE_MMA = 0x10
 Q4MM_M_MAX = 4096
 Q4MM_GROUP_MAX = 4
-Q4MM_NOALLOC_PARTIAL_BYTES = 1228800
+Q4MM_NOALLOC_PARTIAL_BYTES = 2457600
 Q4MM_PATH_SIMT = 1
 Q4MM_PATH_TC = 2
 Q4MM_PATH_ROW_BY_ROW = 3
@@ -259,7 +259,7 @@ def q4mm_forward_noalloc(W: Q4Weight, x: torch.Tensor, y: torch.Tensor, stream=N
 
 
 def q4mm_forward_group(Ws, x: torch.Tensor, ys=None, flags: int = 0, stream=None):
-    """[x @ W_i^T for W_i in Ws] in one launch per 8 token rows (weights sharing K)."""
+    """[x @ W_i^T for W_i in Ws] in one launch per 16 token rows (weights sharing K)."""
     _dev_f32(x, "x")
     M = x.shape[0]
     if not 1 <= len(Ws) <= Q4MM_GROUP_MAX:

@@ -538,7 +538,8 @@ int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int
     const MmaPlan plan = mma_plan(&W->w, ds.num_sms);
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
     l = mma_launch_count(M, inv);
-    sp = mma_row_groups(plan, W->w.K, inv, false) ? 1 : plan.splits;
+    const int64_t rows0 = M < mma_rows_per_launch(inv) ? M : mma_rows_per_launch(inv);  // first launch
+    sp = mma_row_groups(plan, W->w.K, inv, false, rows0) ? 1 : plan.splits;
   } else {
     const MmaPlan plan = simt_plan(&W->w, ds.num_sms);
     l = p == Q4MM_PATH_ROW_BY_ROW ? (int)M : simt_launch_count(M);

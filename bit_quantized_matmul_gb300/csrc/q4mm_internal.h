@@ -107,10 +107,13 @@ struct MmaLaunch {
   float* y[MMA_GROUP_MAX] = {};
 };
 MmaPlan mma_plan(const Weight* W, int num_sms);
-// True when a launch with this plan uses row-group CTAs (one 32-row group pair
-// of a tile over the whole K, no K split) instead of the split plan: four
-// CTAs per tile fit on the SMs and K is short, for y output in default mode.
-bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick);
+// True when a launch of `launch_rows` token rows with this plan uses row-group
+// CTAs (one 32-row group pair of a tile over the whole K, no K split) instead
+// of the split plan: four CTAs per tile fit on the SMs, K is short and the
+// launch has at most 8 rows, for y output in default mode.
+bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick,
+                    int64_t launch_rows);
+int mma_rows_per_launch(bool batch_invariant);
 MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms);
 size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant);
 size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant);

@@ -1,6 +1,6 @@
 // q4mm_mma.cu — streaming tensor-core kernel for small M (the decode path).
 //
-// This is the linear layer of a decode step: M token rows (1 to 8 per launch)
+// This is the linear layer of a decode step: M token rows (1 to 16 per launch)
 // times a Q4_0 weight matrix read from HBM exactly once per call ("Why LLM
 // Decoding Is Slow, and Why Batching Is (Almost) Free", §3-§4: decode streams
 // every weight once per step, and the extra token rows of a batch ride along
@@ -8,12 +8,14 @@
 // kernels of "Why Continuous Batching Slowed Down My LLM Inference Engine"
 // (§"Two Rows of Input, Two Different Kernels") — a one-row GEMV and a tiled
 // GEMM — with one kernel whose cost per weight hardly changes between 1 and
-// 8 rows, so no row count needs a different kernel or a per-row relaunch.
+// 16 rows, so no row count needs a different kernel or a per-row relaunch.
 //
 // CTA = one 128-row tile over a K range (block pairs [bp0, bp1)); 640 threads:
 //
 //   16 compute warps  warp w takes row groups 2(w&3), 2(w&3)+1 (32 rows) and
-//                     K slice w>>2: block pairs bp0 + slice + 4i.  Its lanes
+//                     K slice w>>2: block pairs bp0 + slice + 4i (with four
+//                     to six column groups, 9 to 16 rows: row group w&7 and
+//                     K slice (w>>3)&1, block pairs bp0 + slice + 2i).  Its lanes
 //                     copy their 16-byte weight fragments (coalesced, 1 KB per
 //                     warp and pair) and lanes 0..7 the pair's 128 bytes of
 //                     fp16 scales from HBM into the warp's private cp.async
@@ -27,7 +29,8 @@
 //                     exact three-term bf16 B fragments (x = x0 + x1 + x2,
 //                     term t of row m in MMA column 3m + t, or column t of the
 //                     row's own column group in batch-invariant mode) into a
-//                     4-slot shared-memory ring with full/empty mbarriers
+//                     4-slot (2-slot from four column groups) shared-memory
+//                     ring with full/empty mbarriers
 //                     (every wait bounded).  The fp32 rows arrive by cp.async
 //                     four or five chunks ahead.
 //
@@ -59,7 +62,8 @@
 namespace q4 {
 namespace {
 
-constexpr int MAX_CG = 3;          // column groups per launch (24 MMA columns)
+constexpr int MAX_CG = 3;          // column groups per launch with one row per group
+constexpr int MAX_CG_DENSE = 6;    // column groups per launch with dense packing (48 MMA columns)
 constexpr int SLICES = 4;          // K slices per CTA
 constexpr int COMPUTE_WARPS = 16;  // 4 row-group pairs x 4 slices
 constexpr int CONV_WARPS = 4;
@@ -68,7 +72,6 @@ constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int KERNEL_THREADS = COMPUTE_THREADS + CONV_THREADS;
 constexpr int CHUNK_PAIRS = 8;              // block pairs per ring slot (512 k)
 constexpr int CHUNK_K = CHUNK_PAIRS * 64;
-constexpr int NSLOT = 4;                    // ring depth (a power of two)
 // Block pairs in flight per compute warp (its private cp.async ring) and the
 // unroll of its pair loop.  Measured on GB300 over the 7B decoder layers at
 // M = 1..8: a ring of two pairs with the loop unrolled twice (slot indices and
@@ -128,25 +131,35 @@ struct MmaArgs {
 template <int C, int TPC = 1>
 struct MmaCfg {
   static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
+  // four to six column groups (9 to 16 token rows, dense): one row group per
+  // compute warp, 8 row groups x 2 K slices, so that the accumulators of six
+  // groups fit; a two-slot B ring and three x stages, so that the larger
+  // fragments fit in shared memory
+  static constexpr bool R1 = C >= 4;
+  static constexpr int NSL = R1 ? 2 : SLICES;  // K slices of a tile's CTA
+  static constexpr int NRG = R1 ? 1 : 2;       // row groups per compute warp
+  static constexpr int NSLOT = R1 ? 2 : 4;     // B ring depth (a power of two)
   static constexpr int BF_PAIR = C * 1024;  // B fragments of a pair: [cg][h][32 slots] x 16 B
   static constexpr int SLOT = CHUNK_PAIRS * BF_PAIR;
   static constexpr int RING = NSLOT * SLOT;
   // converter staging: per slot the chunk's raw fp32 x rows
-  static constexpr int XSTAGES = C == 3 ? 5 : 6;  // chunks of x in flight + the one converted
+  static constexpr int XSTAGES = R1 ? 3 : (C == 3 ? 5 : 6);  // chunks of x in flight + the one converted
   static constexpr int XSLOT = MAXM * CHUNK_K * 4;
   static constexpr int XRAW_OFF = RING;
-  static constexpr int RED = SLICES * C * 8 * RED_LD * 4;  // per-slice sums for the gather
+  static constexpr int RED = NSL * C * 8 * RED_LD * 4;  // per-slice sums for the gather
   static constexpr int XCH_OFF = (RED + 15) / 16 * 16;  // cluster split-K: this CTA's sums
   static constexpr int XCH = MAXM * TILE_N * 4;           // [token row][tile row] fp32
   // weight pairs in flight per compute warp: a private ring of WD slots, each
   // the warp's 16-byte fragments of its two row groups (1 KB) and their fp16
-  // scales (128 B), filled by cp.async
+  // scales (128 B), filled by cp.async (half of that with one row group)
   static constexpr int WD = Q4MM_WD;
-  static constexpr int WSLOT = 1024 + 128;
+  static constexpr int WSLOT = NRG * (512 + 64);
+  static constexpr int WSCL = NRG * 512;  // offset of the scales in a slot
   static constexpr int WR_OFF = RING + XSTAGES * XSLOT;
   static constexpr int WR = COMPUTE_WARPS * WD * WSLOT * TPC;
   static constexpr int BAR_OFF = WR_OFF + WR > XCH_OFF + XCH ? WR_OFF + WR : XCH_OFF + XCH;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
+  static_assert(!R1 || TPC == 1, "one row group per warp: one tile per CTA");
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -309,7 +322,8 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // RG: the CTA is row-group pair blockIdx.x & 3 of global tile blockIdx.x >> 2
   // over the whole K, and its 16 compute warps are 16 K slices; otherwise the
   // CTA is global tile blockIdx.x over K split blockIdx.y, its compute warps
-  // 4 row-group pairs x 4 K slices
+  // 4 row-group pairs x 4 K slices (8 row groups x 2 K slices with four to
+  // six column groups)
   // TPC = 2: the CTA takes global tiles 2 blockIdx.x and 2 blockIdx.x + 1 (the
   // second when it exists) over the whole K; its warps cover the same row
   // groups of both, and the converted activations serve both
@@ -334,6 +348,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   const int nchunks = (npairs + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
   const int mrows = a.mrows;
   uint64_t* bfull = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  constexpr int NSLOT = S::NSLOT;
+  constexpr bool R1 = S::R1;
+  constexpr int NRG = S::NRG;
   uint64_t* bempty = bfull + NSLOT;
   const bool compute = warp < COMPUTE_WARPS;
 
@@ -343,26 +360,27 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // compute warps: first weight loads before anything else (weights never
   // depend on an earlier kernel)
-  constexpr int NSL = RG ? COMPUTE_WARPS : SLICES;  // K slices
+  constexpr int NSL = RG ? COMPUTE_WARPS : S::NSL;  // K slices
   const int rgp = RG ? (int)(blockIdx.x & 3) : (warp & 3);
-  const int sl = RG ? (warp & (COMPUTE_WARPS - 1)) : ((warp >> 2) & 3);
+  const int sl = RG ? (warp & (COMPUTE_WARPS - 1)) : (R1 ? ((warp >> 3) & 1) : ((warp >> 2) & 3));
+  const int rg0 = R1 ? (warp & 7) : 2 * rgp;  // first row group of this warp
   const int n_i = (compute && npairs > sl) ? (npairs - sl + NSL - 1) / NSL : 0;
-  const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
-  const uint4* wp1 = a.w[wi1].nib + ((tile1 * a.KBP + bp0 + sl) * 8 + 2 * rgp) * 32 + lane;
+  const uint4* wp = nib_w + ((tile * a.KBP + bp0 + sl) * 8 + rg0) * 32 + lane;
+  const uint4* wp1 = a.w[wi1].nib + ((tile1 * a.KBP + bp0 + sl) * 8 + rg0) * 32 + lane;
   constexpr int64_t WSTEP = NSL * 8 * 32;  // uint4 between a slice's consecutive pairs
-  // ring slot j of this warp: [row group 2rgp, 2rgp + 1][lane][16 B] of
-  // nibbles, then the 128 scale bytes of the two row groups ([rg][g][4 x fp16])
+  // ring slot j of this warp: [row groups rg0 .. rg0 + NRG - 1][lane][16 B] of
+  // nibbles, then the 64 scale bytes of each row group ([rg][g][4 x fp16])
   // (with two tiles per CTA a slot holds the first tile's 1152 bytes, then the second's)
   const uint32_t wring = smem_u32(smem + S::WR_OFF + warp * (WD * S::WSLOT * TPC));
-  const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
-  const uint8_t* sp1 = a.w[wi1].scl + (tile1 * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + (2 * rgp) * 64 + lane * 16;
+  const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + rg0 * 64 + lane * 16;
+  const uint8_t* sp1 = a.w[wi1].scl + (tile1 * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + rg0 * 64 + lane * 16;
   constexpr int64_t SSTEP = NSL * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
   auto fetch = [&](int i) {  // pair i of this warp's K slice into slot i % WD
     if (i < n_i) {
       const uint32_t d = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC);
       cp_async16(d + lane * 16, wp + (int64_t)i * WSTEP);
-      cp_async16(d + 512u + lane * 16, wp + (int64_t)i * WSTEP + 32);
-      if (lane < 8) cp_async16(d + 1024u + lane * 16, sp + (int64_t)i * SSTEP);
+      if (NRG == 2) cp_async16(d + 512u + lane * 16, wp + (int64_t)i * WSTEP + 32);
+      if (lane < 4 * NRG) cp_async16(d + S::WSCL + lane * 16, sp + (int64_t)i * SSTEP);
       if (TPC == 2 && has1) {
         cp_async16(d + S::WSLOT + lane * 16, wp1 + (int64_t)i * WSTEP);
         cp_async16(d + S::WSLOT + 512u + lane * 16, wp1 + (int64_t)i * WSTEP + 32);
@@ -398,8 +416,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   if (tid == 0) {
     for (int b = 0; b < NSLOT; ++b) {
       mbar_init(smem_u32(&bfull[b]), CONV_THREADS);
-      // a chunk's 8 pairs go to all 16 compute warps (two each), or with
-      // row-group CTAs to the 8 warps whose slices hold them (one each)
+      // a chunk's 8 pairs go to all 16 compute warps (two each, or four
+      // with one row group per warp), or with row-group CTAs to the 8 warps
+      // whose slices hold them (one each)
       mbar_init(smem_u32(&bempty[b]), RG ? COMPUTE_WARPS / 2 : COMPUTE_WARPS);
     }
     s_err = 0;
@@ -411,12 +430,13 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // (packed fp32x2 updates) up to two column groups; as four floats [rg][cg][e]
   // for three, where the extra registers of the packed form would spill
   constexpr bool PACKED = C <= 2;
-  unsigned long long acc[TPC][2][C][2];
-  float accf[TPC][2][C][4];
+  static_assert(!(R1 && RG), "row-group CTAs have two row groups per warp");
+  unsigned long long acc[TPC][NRG][C][2];
+  float accf[TPC][NRG][C][4];
 #pragma unroll
   for (int tt = 0; tt < TPC; ++tt)
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
+    for (int r = 0; r < NRG; ++r)
 #pragma unroll
       for (int cg = 0; cg < C; ++cg) {
         acc[tt][r][cg][0] = acc[tt][r][cg][1] = 0ull;
@@ -444,6 +464,15 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s0.x), "=r"(s0.y) : "r"(src + 1024u + g * 8) : "memory");
       asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s1.x), "=r"(s1.y) : "r"(src + 1088u + g * 8) : "memory");
     };
+    // the same with one row group per warp
+    auto load_pair1 = [&](int i, uint4& a0, uint2& s0) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
+      __syncwarp();
+      const uint32_t src = wring + (uint32_t)(i % WD) * S::WSLOT;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a0.x), "=r"(a0.y), "=r"(a0.z), "=r"(a0.w) : "r"(src + lane * 16) : "memory");
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s0.x), "=r"(s0.y) : "r"(src + S::WSCL + g * 8) : "memory");
+    };
     {
 #if Q4MM_UNROLL == 2
 #pragma unroll 2
@@ -452,15 +481,51 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #endif
       for (int i = 0; i < n_i; ++i) {
         // chunk of this pair: slice sl's pairs are sl + NSL i
-        const int c = RG ? 2 * i + (sl >> 3) : (i >> 1);
+        const int c = RG ? 2 * i + (sl >> 3) : (R1 ? (i >> 2) : (i >> 1));
         const int slot = c & (NSLOT - 1);
-        if ((RG || (i & 1) == 0) &&
+        if ((RG || (R1 ? (i & 3) == 0 : (i & 1) == 0)) &&
             !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
           s_err = 1;
           goto compute_done;
         }
-        const int pc = RG ? (sl & 7) : (sl + 4 * (i & 1));  // pair within the chunk
+        const int pc = RG ? (sl & 7) : (R1 ? sl + 2 * (i & 3) : sl + 4 * (i & 1));  // pair within the chunk
         const uint8_t* sb = smem + slot * S::SLOT;
+        if constexpr (R1) {
+          // one row group: A fragments of its two k-steps per block, C column
+          // groups of MMAs, the block scale on the CUDA cores as below
+          uint4 w0;
+          uint2 sv0;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
+          load_pair1(i, w0, sv0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a0[4], a1[4];  // [k-step]
+            const uint32_t x0 = h ? w0.z : w0.x, x1 = h ? w0.w : w0.y;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              a0[p] = nib_pair(x0, p);
+              a1[p] = nib_pair(x1, p);
+            }
+            if (h == 1) {  // every lane has unpacked both its words: refill the slot
+              __syncwarp();
+              fetch(i + WD);
+            }
+            const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
+            const float f0 = h ? __high2float(q0[0]) : __low2float(q0[0]);
+            const float f1 = h ? __high2float(q0[1]) : __low2float(q0[1]);
+            const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
+#pragma unroll
+            for (int cg = 0; cg < C; ++cg) {
+              const uint4 bf = *reinterpret_cast<const uint4*>(bb + cg * 1024);
+              float d[4];
+              mma_bf16_first(d, a0, bf.x, bf.y);
+              mma_bf16_acc(d, a1, bf.z, bf.w);
+              accf[0][0][cg][0] = fmaf(f0, d[0], accf[0][0][cg][0]);
+              accf[0][0][cg][1] = fmaf(f0, d[1], accf[0][0][cg][1]);
+              accf[0][0][cg][2] = fmaf(f1, d[2], accf[0][0][cg][2]);
+              accf[0][0][cg][3] = fmaf(f1, d[3], accf[0][0][cg][3]);
+            }
+          }
+        } else {
 #pragma unroll
         for (int tt = 0; tt < TPC; ++tt) {
         if (tt == 1 && !has1) break;  // the same for every thread of the CTA
@@ -531,7 +596,8 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           }
         }
         }
-        if ((RG || (i & 1)) && c + NSLOT < nchunks) {  // this warp is done with the slot
+        }
+        if ((RG || (R1 ? (i & 3) == 3 : (i & 1))) && c + NSLOT < nchunks) {  // this warp is done with the slot
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bempty[slot]));
         }
@@ -774,13 +840,13 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     return;
   }
 
-  // ---- gather: per tile row and MMA column, the four K slices ----
-  float* red = reinterpret_cast<float*>(smem);  // [SLICES][C*8][RED_LD]
+  // ---- gather: per tile row and MMA column, the four (two) K slices ----
+  float* red = reinterpret_cast<float*>(smem);  // [NSL][C*8][RED_LD]
   constexpr int RS = C * 8 * RED_LD;
   if (compute) {
     const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
+    for (int r = 0; r < NRG; ++r)
 #pragma unroll
       for (int cg = 0; cg < C; ++cg)
 #pragma unroll
@@ -792,7 +858,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           } else {
             v = accf[0][r][cg][e];
           }
-          red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RED_LD + (2 * rgp + r) * 16 + g +
+          red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RED_LD + ((R1 ? (warp & 7) : 2 * rgp) + r) * 16 + g +
               8 * (e >> 1)] = v;
         }
   }
@@ -816,7 +882,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 #pragma unroll
       for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each slice 0..3
 #pragma unroll
-        for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * RED_LD + row];
+        for (int s = 0; s < S::NSL; ++s) v += red[s * RS + (c0 + t) * RED_LD + row];
       val[k] = v;
     }
   }
@@ -976,9 +1042,9 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE, RG, TPC>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
-// Rows per launch: 8 with dense packing (3 column groups), 3 with one row per
-// column group (batch-invariant mode).
-int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (MAX_CG * 8) / 3; }
+// Rows per launch: 16 with dense packing (6 column groups), 3 with one row
+// per column group (batch-invariant mode).
+int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (MAX_CG_DENSE * 8) / 3; }
 
 }  // namespace
 
@@ -1012,13 +1078,17 @@ size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batc
   return mma_partial_bytes_tiles(W->tiles, p, M, batch_invariant);
 }
 
+int mma_rows_per_launch(bool batch_invariant) { return rows_per_launch(batch_invariant); }
+
 int mma_launch_count(int64_t M, bool batch_invariant) {
   const int64_t rpl = rows_per_launch(batch_invariant);
   return (int)((M + rpl - 1) / rpl);
 }
 
-bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick) {
-  return !batch_invariant && !greedy_pick && plan.splits >= 4 && K <= Q4MM_RG_MAX_K;
+bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick,
+                    int64_t launch_rows) {
+  return !batch_invariant && !greedy_pick && launch_rows <= 8 && plan.splits >= 4 &&
+         K <= Q4MM_RG_MAX_K;
 }
 
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
@@ -1029,10 +1099,10 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   if (plan.splits > 1 && tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   const int64_t K = L.W[0]->K;
   const int64_t rpl = rows_per_launch(batch_invariant);
-  // row-group CTAs: no K split and so no cross-CTA exchange, when four CTAs
-  // per tile fit on the SMs (the split plan has at least 4 splits) and K is
-  // short; the plan depends on the shapes only (y output, default mode)
-  const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr);
+  // row-group CTAs (per launch, below): no K split and so no cross-CTA
+  // exchange, when four CTAs per tile fit on the SMs (the split plan has at
+  // least 4 splits), K is short and the launch has at most 8 rows; the plan
+  // depends on the shapes and that row count only (y output, default mode)
   // two tiles per CTA (whole K, no split): launches of more tiles than SMs
   // run as CTAs that stream two tiles each, for one or two column groups in
   // default mode (y output or the greedy pick)
@@ -1040,6 +1110,7 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
                    tiles > plan.num_sms;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
+    const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr, mrows);
     const float* xs = xrows ? x : x + mb * K;
     const int32_t* xr = xrows ? xrows + mb : nullptr;
     int st;
@@ -1051,7 +1122,13 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
       }
     } else {
       const int cgs = (3 * mrows + 7) / 8;  // column groups of this launch
-      if (rg) {
+      if (cgs >= 4) {  // 9 to 16 rows: one row group per warp, K splits
+        switch (cgs) {
+          case 4: st = launch_c<4, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          case 5: st = launch_c<5, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+          default: st = launch_c<6, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
+        }
+      } else if (rg) {
         switch (cgs) {
           case 1: st = launch_c<1, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
           case 2: st = launch_c<2, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;

@@ -158,7 +158,7 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
 
 /* y_i = x @ W_i^T for up to Q4MM_GROUP_MAX weights that share K and the same
  * activations (the q, k and v projections, or the gate and up projections, of
- * one decoder layer), in one kernel launch per 8 token rows instead of one per
+ * one decoder layer), in one kernel launch per 16 token rows instead of one per
  * weight: the activations are staged once and the fixed cost of a launch is
  * paid once ("Why LLM Decoding Is Slow, and Why Batching Is (Almost) Free",
  * §4: every weight is still read exactly once per call).
@@ -178,8 +178,8 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
 Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
                               int64_t M, uint32_t flags, cudaStream_t stream);
 
-/* Capacity of the split-K partial sums of q4mm_forward_noalloc (1200 KiB). */
-#define Q4MM_NOALLOC_PARTIAL_BYTES 1228800
+/* Capacity of the split-K partial sums of q4mm_forward_noalloc (2400 KiB). */
+#define Q4MM_NOALLOC_PARTIAL_BYTES 2457600
 
 /* y = x @ W^T without allocating any device memory.  (The pages have no
  * counterpart: this is a library concern.)
@@ -189,7 +189,7 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * at that moment use this call instead: a serving process that gave all free
  * device memory to its own pool (the allocation would fail), or a step that
  * must not wait for the whole device, as cudaFree does.  Its scratch is one
- * fixed device array in the library (about 1.3 MB per device, created when the
+ * fixed device array in the library (about 2.5 MB per device, created when the
  * library's device code is loaded), so this call allocates nothing.  (As for
  * any CUDA library, the runtime may still load kernel code on first use.)
  *
@@ -197,7 +197,7 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * Always runs the streaming mma.sync kernel with its usual K partition: the
  * results are bit-identical to q4mm_forward_ex(W, x, y, M, Q4MM_FORCE_MMA).
  * Returns Q4_ERR_SHAPE, before any launch, if the call's split-K partial
- * sums (splits x min(M, 8) x N rounded up to 128 x 8 bytes) exceed
+ * sums (splits x min(M, 16) x N rounded up to 128 x 8 bytes) exceed
  * Q4MM_NOALLOC_PARTIAL_BYTES.  On a 152-SM GB300 every linear layer of a
  * 7B decoder (N, K up to 18944) fits at any M; q4mm_forward has no such limit.
  *
@@ -286,8 +286,9 @@ Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
 
 /* Plan of a call with these arguments, without running it: *path receives
  * the Q4MM_PATH_* value, *launches the number of kernel launches the call
- * makes, *splits the K partition count of a q4mm_forward_ex call (1 when the
- * streaming kernel gives each CTA one 32-row group pair over the whole K).
+ * makes, *splits the K partition count of the first launch of a
+ * q4mm_forward_ex call (1 when the streaming kernel gives each CTA one 32-row
+ * group pair over the whole K, which it does for launches of up to 8 rows).
  * Any output pointer may be NULL. */
 Q4_API int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int* launches,
                           int* splits);
@@ -301,7 +302,7 @@ Q4_API int q4mm_set_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_m_threshold(void);
 
 /* The M threshold of q4mm_forward_group: at or above it one tcgen05 launch
- * covers the whole group, below it one streaming launch per 8 token rows.
+ * covers the whole group, below it one streaming launch per 16 token rows.
  * The default is the crossover measured on GB300 over a 7B layer's q/k/v and
  * gate/up groups.  Same range and errors as set_m_threshold. */
 Q4_API int q4mm_set_group_m_threshold(int64_t m);

@@ -204,3 +204,35 @@ def test_two_tile_ctas_greedy_pick_matches_oracle(q4):
         assert np.array_equal(yf.max(axis=1).view(np.uint32), mx.view(np.uint32))
     assert q4.q4_device_status() == q4.Q4_OK
     W.free()
+
+
+SIXTEEN_ROW_CASES = [(4000, 4608), (3584, 3584), (155 * 128 - 37, 1024), (300, 1024)]
+
+
+@pytest.mark.parametrize("N,KK", SIXTEEN_ROW_CASES)
+def test_sixteen_row_launches_match_oracle(q4, N, KK):
+    # 9 to 16 token rows in one streaming launch (four to six column groups,
+    # one row group per warp, two K slices per CTA) over each exchange on a
+    # 152-SM device: clusters (32 tiles x 4 splits), flagged global words
+    # (28 tiles x 5 splits; a ragged 3-tile weight x 8) and one K split (155
+    # tiles); 20 and 23 rows add a launch of 4 or 7 rows
+    w = weights(76, 0, N, KK)
+    blocks = oracle.quantize(w)
+    W = q4.q4_quantize(torch.from_numpy(w).to(DEV))
+    if (N, KK) == (3584, 3584) and torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)[2] == 1    # row-group CTAs
+        assert q4.q4mm_plan_info(W, 16, q4.Q4MM_FORCE_MMA)[1:] == (1, 5)  # one launch, 5 splits
+    for M in (9, 12, 14, 16, 20, 23):
+        x = acts(76, M, KK)
+        y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), q4.Q4MM_FORCE_MMA).cpu().numpy()
+        _, y64, bound = oracle.matmul(blocks, x)
+        assert_within_bound(y, y64, bound, "N=%d K=%d M=%d" % (N, KK, M))
+    # the greedy pick at 16 rows adds the splits in the order of the call that
+    # writes y, so it picks the same indices and values
+    xd = torch.from_numpy(acts(77, 16, KK)).to(DEV)
+    idx, mx = q4.q4mm_argmax_ex(W, xd, q4.Q4MM_FORCE_MMA)
+    yf = q4.q4mm_forward_ex(W, xd, q4.Q4MM_FORCE_MMA).cpu().numpy()
+    assert np.array_equal(idx.cpu().numpy(), np.argmax(yf, axis=1))
+    assert np.array_equal(mx.cpu().numpy().view(np.uint32), yf.max(axis=1).view(np.uint32))
+    assert q4.q4_device_status() == q4.Q4_OK
+    W.free()

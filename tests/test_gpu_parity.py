@@ -241,7 +241,7 @@ def test_argmax_exact_ties_pick_lowest_index(q4):
 def test_forward_at_the_largest_m(q4):
     # M = Q4MM_M_MAX in one call (tensor-core path, several token tiles), every
     # output of a seeded sample of rows against the oracle; the streaming path
-    # (8 rows per launch) on the same rows
+    # (16 rows per launch) on the same rows
     N, K = 300, 1024
     w = weights(52, 3, N, K)
     blocks = oracle.quantize(w)

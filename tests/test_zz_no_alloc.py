@@ -42,11 +42,11 @@ def _setup(N, K, c, m):
 def _partial_need(W, M):
     _, _, splits = q4.q4mm_plan_info(W, M, q4.Q4MM_FORCE_MMA)
     n_pad = (W.N + 127) // 128 * 128
-    return 0 if splits <= 1 else splits * min(M, 8) * n_pad * 8
+    return 0 if splits <= 1 else splits * min(M, 16) * n_pad * 8
 
 
 # (N, K, token-row counts): ragged tiles, a many-way K split with launches
-# of 8 + ... rows, the largest scratch of a 7B layer (q_proj at M >= 8), and a
+# of 16 + ... rows, the largest scratch of a 7B layer (q_proj at M >= 16), and a
 # one-split shape.
 CASES = [
     (300, 1024, (1, 5, 17)),
@@ -101,8 +101,8 @@ def test_noalloc_allocates_no_device_memory():
 
 
 def test_noalloc_rejects_oversized_calls_before_launch():
-    # 1024 x 18944: 8 tiles, so a 152-SM device splits K 19 ways and 8 rows
-    # need 19 * 8 * 1024 * 8 bytes of partial sums, more than the capacity.
+    # 1024 x 18944: 8 tiles, so a 152-SM device splits K 19 ways and 16 rows
+    # need 19 * 16 * 1024 * 8 bytes of partial sums, more than the capacity.
     N, K = 1024, 18944
     W, blocks = _setup(N, K, 92, 0)
     checked_reject = False
