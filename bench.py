@@ -146,6 +146,25 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(ms, world, device=None):
+    """The timed region's duration (ms) of the slowest rank: one MAX
+    all-reduce over the process group when there are several ranks."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes, world, ms_per_step):
+    """Whole-job throughput: every rank (an independent replica) streams
+    step_bytes per step, in the slowest rank's time."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 def cpu_oracle_sample(layers=1, Ms=M_SWEEP):
@@ -340,13 +359,9 @@ def run_gpu(args):
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_per_step = ms / args.steps
-    value = step_wbytes * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_wbytes, world, ms_per_step)
 
     # per-(M, call) durations over the timed region: each graph replay is the
     # `layers` calls of one kind, bracketed by events on the launching stream
@@ -402,8 +417,8 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    e2e_value = step_wbytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    e2e_value = whole_job_gbs(step_wbytes, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
