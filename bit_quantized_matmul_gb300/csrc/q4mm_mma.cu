@@ -128,14 +128,16 @@ struct MmaArgs {
   EpiArgs e;
 };
 
-template <int C, int TPC = 1>
+template <int C, int TPC = 1, bool DENSE = true, bool RG = false>
 struct MmaCfg {
   static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
   // four to six column groups (9 to 16 token rows, dense): one row group per
   // compute warp, 8 row groups x 2 K slices, so that the accumulators of six
   // groups fit; a two-slot B ring and three x stages, so that the larger
   // fragments fit in shared memory
-  static constexpr bool R1 = C >= 4;
+  // (measured on GB300: three column groups are faster with two row groups
+  // per warp, and batch-invariant launches keep one layout for every C)
+  static constexpr bool R1 = DENSE && !RG && TPC == 1 && C >= 4;
   static constexpr int NSL = R1 ? 2 : SLICES;  // K slices of a tile's CTA
   static constexpr int NRG = R1 ? 1 : 2;       // row groups per compute warp
   static constexpr int NSLOT = R1 ? 2 : 4;     // B ring depth (a power of two)
@@ -308,7 +310,7 @@ __device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_
 // ----------------------------------------------------------------------------
 template <int C, bool DENSE, bool RG, int TPC>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
-  using S = MmaCfg<C, TPC>;
+  using S = MmaCfg<C, TPC, DENSE, RG>;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -429,7 +431,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // accumulators: [rg][cg][row R0 / R1] as {column 2tq, column 2tq + 1} pairs
   // (packed fp32x2 updates) up to two column groups; as four floats [rg][cg][e]
   // for three, where the extra registers of the packed form would spill
-  constexpr bool PACKED = C <= 2;
+  // (packed with one row group per warp for four and five groups; six spill,
+  // measured slower)
+  constexpr bool PACKED = C <= 2 || (R1 && C <= 5);
   static_assert(!(R1 && RG), "row-group CTAs have two row groups per warp");
   unsigned long long acc[TPC][NRG][C][2];
   float accf[TPC][NRG][C][4];
@@ -512,6 +516,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
             const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
             const float f0 = h ? __high2float(q0[0]) : __low2float(q0[0]);
             const float f1 = h ? __high2float(q0[1]) : __low2float(q0[1]);
+            unsigned long long s0 = 0, s1 = 0;
+            if constexpr (PACKED) {
+              s0 = dup2(f0);
+              s1 = dup2(f1);
+            }
             const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
 #pragma unroll
             for (int cg = 0; cg < C; ++cg) {
@@ -519,10 +528,15 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
               float d[4];
               mma_bf16_first(d, a0, bf.x, bf.y);
               mma_bf16_acc(d, a1, bf.z, bf.w);
-              accf[0][0][cg][0] = fmaf(f0, d[0], accf[0][0][cg][0]);
-              accf[0][0][cg][1] = fmaf(f0, d[1], accf[0][0][cg][1]);
-              accf[0][0][cg][2] = fmaf(f1, d[2], accf[0][0][cg][2]);
-              accf[0][0][cg][3] = fmaf(f1, d[3], accf[0][0][cg][3]);
+              if constexpr (PACKED) {
+                ffma2(acc[0][0][cg][0], s0, d[0], d[1]);
+                ffma2(acc[0][0][cg][1], s1, d[2], d[3]);
+              } else {
+                accf[0][0][cg][0] = fmaf(f0, d[0], accf[0][0][cg][0]);
+                accf[0][0][cg][1] = fmaf(f0, d[1], accf[0][0][cg][1]);
+                accf[0][0][cg][2] = fmaf(f1, d[2], accf[0][0][cg][2]);
+                accf[0][0][cg][3] = fmaf(f1, d[3], accf[0][0][cg][3]);
+              }
             }
           }
         } else {
@@ -948,7 +962,7 @@ int cluster_capacity(int device, int size) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
-  cfg.dynamicSmemBytes = MmaCfg<C, 1>::BYTES;
+  cfg.dynamicSmemBytes = MmaCfg<C, 1, DENSE>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -969,7 +983,7 @@ template <int C, bool DENSE, bool RG, int TPC = 1>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
-  using S = MmaCfg<C, TPC>;
+  using S = MmaCfg<C, TPC, DENSE, RG>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
   int tiles = 0;
