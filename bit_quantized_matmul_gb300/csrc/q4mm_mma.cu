@@ -18,7 +18,8 @@
 //                     K slice (w>>3)&1, block pairs bp0 + slice + 2i).  Its lanes
 //                     copy their 16-byte weight fragments (coalesced, 1 KB per
 //                     warp and pair) and lanes 0..7 the pair's 128 bytes of
-//                     fp16 scales from HBM into the warp's private cp.async
+//                     fp16 scales (512 and 64 bytes with one row group per
+//                     warp) from HBM into the warp's private cp.async
 //                     ring, two pairs ahead; each lane reads back its own
 //                     fragments, which in the fragment layout are exactly the
 //                     A registers of m16n8k16 MMAs once unpacked to exact bf16
@@ -32,7 +33,7 @@
 //                     4-slot (2-slot from four column groups) shared-memory
 //                     ring with full/empty mbarriers
 //                     (every wait bounded).  The fp32 rows arrive by cp.async
-//                     four or five chunks ahead.
+//                     four or five chunks ahead (two from four column groups).
 //
 // Launches of more tiles than SMs with one K split (the gate/up group of a 7B
 // layer: 296 tiles) and one or two column groups run as two-tile CTAs: a CTA
@@ -48,10 +49,13 @@
 //
 // Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
 // fp32 registers; the block's fp16 scale is applied on the CUDA cores,
-// acc = fma(d, D_b, acc), in ascending block order.  At the end the four K
-// slices and the three terms of each row are added in a fixed order, then the
-// K splits in ascending split order (q4mm_epilogue.cuh).  Nothing in that
-// order depends on M.
+// acc = fma(d, D_b, acc), in ascending block order.  At the end the four (or
+// two) K slices and the three terms of each row are added in a fixed order,
+// then the K splits in ascending split order (q4mm_epilogue.cuh).  In
+// batch-invariant mode nothing in that order depends on M; in the default
+// mode the launch's row count picks the CTA layout (row-group or two-tile CTAs
+// up to 8 rows, two K slices from 9), so a row's bits may differ with M
+// within the tolerance.
 #include <cuda_fp16.h>
 
 #include <atomic>
