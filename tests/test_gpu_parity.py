@@ -116,6 +116,8 @@ CASES = [
     (896, 896, (1, 2, 4)),                          # the 896 x 896 config
     (130, 3584, (1, 4, 33)),                        # 2 tiles, one of 2 rows
     (33, 18944, (1, 3)),                            # the long-K down_proj K, one ragged tile
+    (200, 224, (1, 3, 9, 16, 30)),                  # 7 blocks: the last pair half padding
+    (257, 1440, (2, 8, 12, 24)),                    # 45 blocks, 3 tiles, one of 1 row
 ]
 
 
