@@ -1027,12 +1027,14 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.e.keys = ws.keys + mb;
   a.e.argmax_done = ws.argmax_done;
   a.e.tiles = tiles;
-  static bool attr_set[64] = {};
-  if (!attr_set[W0->device & 63]) {
+  // per device, once (atomic: q4mm_forward and q4mm_forward_noalloc hold
+  // different locks; setting the attribute twice is harmless)
+  static std::atomic<bool> attr_set[64];
+  if (!attr_set[W0->device & 63].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(mma_kernel<C, DENSE, RG, TPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
-    attr_set[W0->device & 63] = true;
+    attr_set[W0->device & 63].store(true, std::memory_order_release);
   }
   // Split-K through distributed shared memory when the K splits of every tile
   // fit in one cluster of at most 4 CTAs and all the launch's clusters are

@@ -39,6 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "q4mm_epilogue.cuh"
 #include "q4mm_internal.h"
 
@@ -765,12 +767,12 @@ int launch_nb(const MmaLaunch& L, const float* x, int64_t ml, int32_t* idx, floa
     xop_kernel<NB><<<blocks, 256, 0, s>>>(x, ml, W->K, KB2, mtiles, static_cast<uint8_t*>(ws.xop));
     if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
   }
-  static bool attr_set[64] = {};
-  if (!attr_set[W->device & 63]) {
+  static std::atomic<bool> attr_set[64];  // per device, once (setting it twice is harmless)
+  if (!attr_set[W->device & 63].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
-    attr_set[W->device & 63] = true;
+    attr_set[W->device & 63].store(true, std::memory_order_release);
   }
   // greedy-pick completion count: one epilogue chunk per (tile, token chunk)
   int64_t chunks = 0;
