@@ -100,3 +100,14 @@ def test_kv_append_arguments_checked_on_host(q4):
     assert call(st=100) == q4.Q4_ERR_ALIGN          # 200-byte token stride
     assert call(p=a16 + 8) == q4.Q4_ERR_ALIGN
     assert call(total=2 ** 30) == q4.Q4_ERR_INVALID_ARG  # 8 vectors per row: past the 32-bit item index
+
+
+def test_binding_constants_match_the_header(q4):
+    # every numeric #define of the header (status codes, flags, limits, paths)
+    # has the same value in the Python binding
+    text = open(os.path.join(ROOT, "include", "q4mm.h")).read()
+    defs = dict(re.findall(r"^#define\s+(Q4\w*)\s+(0x[0-9A-Fa-f]+|\d+)u?\b", text, re.M))
+    assert len(defs) >= 20
+    for name, value in defs.items():
+        assert hasattr(q4, name), name
+        assert getattr(q4, name) == int(value, 0), (name, value, getattr(q4, name))
