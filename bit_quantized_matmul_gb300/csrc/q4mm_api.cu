@@ -38,18 +38,20 @@ struct DeviceScratch {
 DeviceScratch g_dev[MAX_DEVICES];
 
 // Below this M the streaming mma.sync kernel is used, at or above it the
-// tcgen05 kernel.  Measured on GB300 over one Qwen2.5-7B decoder layer's seven
-// linears as single calls (bench.py --path-sweep, M in 1..256): the streaming
-// kernel is faster for the whole layer up to M = 16 (161.0 against 170.7 us),
-// the tensor-core kernel from M = 24 (172.6 against 240.1 us).
-constexpr int64_t DEFAULT_M_THRESHOLD = 24;
+// tcgen05 kernel.  Measured on GB300 over one Qwen2.5-7B decoder layer (q/k/v
+// group, o, gate/up group, down; 8 layer copies in a CUDA graph), with the
+// streaming kernel taking up to 16 rows per launch: streaming is faster up to
+// M = 16 (o 13.7 against 16.9 us, down 33.2 against 40.3 us), the tensor-core
+// kernel from M = 17, where streaming needs a second launch (o 17.2 against
+// 17.9 us, down 40.5 against 44.5 us; the layer 142.4 against 148.7 us).
+constexpr int64_t DEFAULT_M_THRESHOLD = 17;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 // Grouped calls (q4mm_forward_group) run one launch over the whole group on
 // either path.  Measured the same way over a layer's q/k/v and gate/up groups:
-// the streaming launches are faster up to M = 16 (77.4 against 83.7 us for
-// the two groups), the grouped tensor-core launches from M = 24 (84.3
-// against 115.4 us).
-constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 24;
+// the streaming launches are faster up to M = 16 (66.3 against 84.4 us for
+// the two groups), the grouped tensor-core launches from M = 17 (84.6 against
+// 86.4 us).
+constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 17;
 std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
