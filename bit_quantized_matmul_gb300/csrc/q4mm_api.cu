@@ -575,18 +575,26 @@ int q4_device_status(void) {
   int st = current_device(&dev);
   if (st) return st;
   if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
-  DeviceScratch& ds = g_dev[dev];
-  std::lock_guard<std::mutex> lock(ds.mu);
-  if (!ds.init) return Q4_OK;
   unsigned v = 0;
-  if (cudaMemcpy(&v, ds.ws.status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return Q4_ERR_CUDA;
-  if (v) {
-    const unsigned zero = 0;
-    if (cudaMemcpy(ds.ws.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
-      return Q4_ERR_CUDA;
-    return (v & STATUS_TIMEOUT) ? Q4_ERR_TIMEOUT : Q4_ERR_INVALID_ARG;
+  {
+    DeviceScratch& ds = g_dev[dev];
+    std::lock_guard<std::mutex> lock(ds.mu);
+    if (ds.init) {
+      if (cudaMemcpy(&v, ds.ws.status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return Q4_ERR_CUDA;
+      if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(ds.ws.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
+          return Q4_ERR_CUDA;
+      }
+    }
   }
+  // the fixed scratch of q4mm_forward_noalloc keeps its own status word
+  unsigned na = 0;
+  st = noalloc_status_take(dev, &na);
+  if (st) return st;
+  v |= na;
+  if (v) return (v & STATUS_TIMEOUT) ? Q4_ERR_TIMEOUT : Q4_ERR_INVALID_ARG;
   return Q4_OK;
 }
 

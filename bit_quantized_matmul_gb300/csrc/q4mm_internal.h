@@ -165,6 +165,9 @@ int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx
               float* maxval, const TcPlan& plan, const Workspace& ws, cudaStream_t s);
 
 int device_num_sms(int device);
+// Read and clear the status word of q4mm_forward_noalloc's fixed scratch on
+// `device` (0 if that call never ran there).
+int noalloc_status_take(int device, unsigned* bits);
 bool tc_kernel_built();
 
 }  // namespace q4

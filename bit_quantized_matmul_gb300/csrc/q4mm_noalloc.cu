@@ -70,6 +70,26 @@ int setup_locked(int dev, NoAllocDevice& d) {
 }
 
 }  // namespace
+
+// The status word of the fixed array on `dev`: read and cleared (two 4-byte
+// copies, no allocation).  0 when no q4mm_forward_noalloc call has set the
+// array up on that device.
+int noalloc_status_take(int dev, unsigned* bits) {
+  *bits = 0;
+  if (dev < 0 || dev >= NA_MAX_DEVICES) return Q4_OK;
+  NoAllocDevice& d = g_na[dev];
+  std::lock_guard<std::mutex> lock(d.mu);
+  if (!d.ready) return Q4_OK;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, d.base, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return Q4_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(d.base, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess) return Q4_ERR_CUDA;
+  }
+  *bits = v;
+  return Q4_OK;
+}
+
 }  // namespace q4
 
 struct q4_weight {

@@ -207,8 +207,9 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * All calls on one device share the one array: calls whose kernels overlap on
  * the GPU (other streams, other host threads) race on it and give wrong
  * results.  Order them on one stream.  A bounded device-side wait that runs
- * out is recorded in this array's own status word, which q4_device_status
- * does not read; y is then unspecified. */
+ * out is recorded in this array's own status word (y is then unspecified);
+ * q4_device_status reads and clears that word together with the ordinary
+ * one, with two 4-byte copies and no allocation. */
 Q4_API int q4mm_forward_noalloc(const q4_weight* W, const float* x, float* y, int64_t M,
                                 cudaStream_t stream);
 
@@ -309,7 +310,8 @@ Q4_API int q4mm_set_group_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_group_m_threshold(void);
 
 /* Synchronize the current device and return (then clear) the device status
- * word: Q4_OK; Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out;
+ * words (the library's scratch and, once q4mm_forward_noalloc has run on the
+ * device, its fixed array): Q4_OK; Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out;
  * Q4_ERR_INVALID_ARG if q4mm_argmax_rows met a row index out of range; or
  * Q4_ERR_CUDA if the device reports an error. */
 Q4_API int q4_device_status(void);
