@@ -391,34 +391,13 @@ def run_gpu(args):
             "call_us": {g: per[(M, g)] * 1e3 for g, _ in groups},
         }
 
-    # ---- end to end through the public API: pinned host x in, host y out ----
-    pin_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    out_host = {M: torch.empty((M, 3584), dtype=torch.float32).pin_memory() for M in msw}
-    h2d = sum(v.numel() * 4 for v in pin_x.values())
-    d2h = sum(v.numel() * 4 for v in out_host.values())
+    # ---- end to end through the C ABI: pinned host x in, every output out ----
+    e2e = e2e_c_abi(q4, torch, dev, stack, msw, layers, args.steps, stream, world)
+    e2e_value = whole_job_gbs(step_wbytes, world, e2e["ms_per_step"])
 
-    def e2e_step():
-        for M in msw:
-            xs[(M, 3584)].copy_(pin_x[(M, 3584)], non_blocking=True)
-            xs[(M, 18944)].copy_(pin_x[(M, 18944)], non_blocking=True)
-            for gname, _ in groups:
-                graphs[(M, gname)].replay()
-            out_host[M].copy_(ys[(M, "down_proj")], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
-    e2e_value = whole_job_gbs(step_wbytes, world, e2e_ms)
+    configs = None
+    if not args.no_configs:
+        configs = extra_configs(q4, torch, dev, stack, stream, args, rank == 0 and world == 1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -454,11 +433,16 @@ def run_gpu(args):
                                    "from it), every launch of one step (%d launches)" % (n_launch * layers),
                          "algorithmic_bytes_per_launch": tot_bytes / n_launch,
                          "algorithmic_bytes_rule": "0.5625*sum(N_i*K) + 4*M*K + 4*M*sum(N_i) per call"},
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                    "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms_per_step"],
+                    "calls_per_step": e2e["calls"],
+                    "how": "every call of the step through the C ABI (q4mm_forward_group for q/k/v and "
+                           "gate/up, q4mm_forward for o and down), x copied in from pinned host memory per M, "
+                           "every output of every layer copied back to pinned host memory per M"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     for name in TYPES:
@@ -467,6 +451,246 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _graph_us(torch, stream, issue, reps, calls, warm=3):
+    """Median per-call time (us) of `issue` (which makes `calls` calls),
+    captured once in a CUDA graph and replayed `reps` times."""
+    with torch.cuda.stream(stream):
+        issue()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        issue()
+    times = []
+    with torch.cuda.stream(stream):
+        for r in range(warm + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            if r >= warm:
+                times.append(a.elapsed_time(b) * 1e3 / calls)
+    del g
+    return statistics.median(times)
+
+
+def e2e_c_abi(q4, torch, dev, stack, msw, layers, steps, stream, world):
+    """The step end to end through the library's C ABI: per M, x is copied in
+    from pinned host memory, every call is made through the C entry points
+    (argument checks, path choice and launches inside the timed region), and
+    the outputs of every layer and projection (one arena per M) are copied
+    back to pinned host memory.  Returns ms per step and the bytes moved."""
+    import ctypes
+
+    import synthetic
+
+    lib = q4.raw_library()
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    per_m = []
+    h2d = d2h = 0
+    calls = 0
+    for M in msw:
+        xh = {K: torch.from_numpy(synthetic.normal(synthetic.act_seed(1, M) + K, (M, K))).pin_memory()
+              for K in (3584, 18944)}
+        xd = {K: torch.empty((M, K), dtype=torch.float32, device=dev) for K in (3584, 18944)}
+        per_layer = sum(synthetic.QWEN7B_LINEARS[n][0] for n in TYPES) * M
+        arena = torch.empty(layers * per_layer, dtype=torch.float32, device=dev)
+        arena_h = torch.empty(layers * per_layer, dtype=torch.float32).pin_memory()
+        h2d += sum(v.numel() * 4 for v in xh.values())
+        d2h += arena.numel() * 4
+        ops = []
+        off = 0
+        for layer in range(layers):
+            yp = {}
+            for n in TYPES:
+                yp[n] = arena.data_ptr() + off * 4
+                off += synthetic.QWEN7B_LINEARS[n][0] * M
+            for gname, names in GROUPS:
+                K = synthetic.QWEN7B_LINEARS[names[0]][1]
+                if len(names) == 1:
+                    ops.append((lib.q4mm_forward, (stack[names[0]][layer].handle, ctypes.c_void_p(xd[K].data_ptr()),
+                                                   ctypes.c_void_p(yp[names[0]]), M, sh)))
+                else:
+                    hw = (ctypes.c_void_p * len(names))(*[stack[n][layer].handle.value for n in names])
+                    hy = (ctypes.c_void_p * len(names))(*[yp[n] for n in names])
+                    ops.append((lib.q4mm_forward_group, (hw, len(names), ctypes.c_void_p(xd[K].data_ptr()), hy, M,
+                                                         0, sh)))
+        calls += len(ops)
+        per_m.append((xh, xd, arena, arena_h, ops))
+
+    def step():
+        for xh, xd, arena, arena_h, ops in per_m:
+            for K in (3584, 18944):
+                xd[K].copy_(xh[K], non_blocking=True)
+            for fn, a in ops:
+                st = fn(*a)
+                if st != 0:
+                    raise RuntimeError("C ABI call failed with status %d" % st)
+            arena_h.copy_(arena, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h, "calls": calls}
+
+
+def _oracle_single_core():
+    """The oracle on one host core: the 896 x 896 call at M = 1, 2, 4 and the
+    gate projection (18944 x 3584) at M = 1, quantized beforehand."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+
+    out = {}
+    prev = oracle.set_threads(1)
+    try:
+        for (name, N, K, Ms) in (("896x896", 896, 896, (1, 2, 4)), ("gate_proj", 18944, 3584, (1,))):
+            blocks = oracle.quantize(synthetic.normal(synthetic.weight_seed(1, 0), (N, K), sigma=0.02))
+            for M in Ms:
+                x = synthetic.normal(synthetic.act_seed(1, M), (M, K))
+                t0 = time.perf_counter()
+                oracle.matmul(blocks, x)
+                dt = time.perf_counter() - t0
+                out["%s@M=%d" % (name, M)] = {"s": dt, "weight_gbs": N * K * BLOCK_BYTES_PER_WEIGHT / dt / 1e9,
+                                                "rows_per_s": M / dt}
+    finally:
+        oracle.set_threads(prev)
+    return {"cores": 1, "kind": "oracle", "cases": out}
+
+
+def extra_configs(q4, torch, dev, stack, stream, args, with_oracle):
+    """Every configuration of the metric besides the headline step: the
+    896 x 896 call, the M = 124 mixed step in default and batch-invariant mode,
+    the LM-head greedy pick, and the M sweep on gate_proj and on the stack
+    with the measured streaming / tensor-core crossover."""
+    import synthetic
+
+    peak, _ = _peaks()
+    reps = max(5, min(args.steps, 20))
+    out = {}
+
+    # ---- 896 x 896, M = 1, 2, 4: 400 weight copies (180 MB, beyond L2) in one graph
+    N = K = 896
+    copies = 400
+    Ws = [q4.q4_quantize(torch.from_numpy(synthetic.normal(synthetic.weight_seed(1, c), (N, K), sigma=0.02)).to(dev))
+          for c in range(copies)]
+    wb = N * K * BLOCK_BYTES_PER_WEIGHT
+    c1 = {}
+    for M in (1, 2, 4):
+        x = torch.from_numpy(synthetic.normal(synthetic.act_seed(1, M), (M, K))).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def issue():
+            for W in Ws:
+                q4.q4mm_forward(W, x, y=y, stream=stream)
+        us = _graph_us(torch, stream, issue, reps, copies)
+        singles = []
+        with torch.cuda.stream(stream):
+            for r in range(23):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                q4.q4mm_forward(Ws[(7 * r) % copies], x, y=y, stream=stream)
+                b.record(stream)
+                b.synchronize()
+                if r >= 3:
+                    singles.append(a.elapsed_time(b) * 1e3)
+        c1[str(M)] = {"us_per_call_graph": us, "us_single_launch": statistics.median(singles),
+                      "weight_gbs": wb / us / 1e3, "frac_of_measured_hbm": wb / us / 1e3 / peak,
+                      "token_rows_per_s": M / us * 1e6}
+    for W in Ws:
+        W.free()
+    out["c1_896x896"] = {"workload": "Q4_0 896x896, %d weight copies in one CUDA graph (beyond L2); the single "
+                                     "launch is one call between events" % copies, "per_M": c1}
+
+    # ---- M = 124 mixed step (120 prefill + 4 verify rows) through gate/up/down
+    L3 = min(8, len(stack["gate_proj"]))
+    M = 124
+    x1 = torch.from_numpy(synthetic.normal(synthetic.act_seed(3, M), (M, 3584))).to(dev)
+    x2 = torch.from_numpy(synthetic.normal(synthetic.act_seed(3, M) + 1, (M, 18944))).to(dev)
+    yg = torch.empty((M, 18944), device=dev)
+    yu = torch.empty((M, 18944), device=dev)
+    yd = torch.empty((M, 3584), device=dev)
+    wb3 = sum(synthetic.QWEN7B_LINEARS[n][0] * synthetic.QWEN7B_LINEARS[n][1]
+              for n in ("gate_proj", "up_proj", "down_proj")) * BLOCK_BYTES_PER_WEIGHT
+    c3 = {}
+    for mode, fl in (("default", 0), ("batch_invariant", q4.Q4MM_BATCH_INVARIANT)):
+        def issue():
+            for l in range(L3):
+                q4.q4mm_forward_group([stack["gate_proj"][l], stack["up_proj"][l]], x1, ys=[yg, yu], flags=fl,
+                                      stream=stream)
+                q4.q4mm_forward_ex(stack["down_proj"][l], x2, fl, y=yd, stream=stream)
+        us = _graph_us(torch, stream, issue, reps, L3)
+        _, lg, _ = q4.q4mm_plan_info(stack["gate_proj"][0], M, fl)
+        _, ld, _ = q4.q4mm_plan_info(stack["down_proj"][0], M, fl)
+        c3[mode] = {"us_per_layer": us, "weight_gbs": wb3 / us / 1e3, "token_rows_per_s": M / us * 1e6,
+                    "launches_gate_up_down": [lg, ld]}
+    c3["batch_invariant_over_default"] = c3["batch_invariant"]["us_per_layer"] / c3["default"]["us_per_layer"]
+    out["c3_mixed_m124"] = {"workload": "M = 124 (120 prefill + 4 verify rows) through gate/up (one grouped call) "
+                                        "and down, %d layers of the 7B stack in one CUDA graph" % L3, "modes": c3}
+
+    # ---- LM head, fused greedy pick
+    out["c4_lm_head"] = lm_head_cases(q4, torch, dev, stream, reps)
+
+    # ---- M sweep on gate_proj (28 copies) and on the stack (all layers), and the crossover
+    sweep = (1, 2, 3, 4, 5, 6, 8, 16, 32, 64, 128, 256)
+    Lg = len(stack["gate_proj"])
+    gb = 18944 * 3584 * BLOCK_BYTES_PER_WEIGHT
+    lb = sum(synthetic.QWEN7B_LINEARS[n][0] * synthetic.QWEN7B_LINEARS[n][1] for n in TYPES) * BLOCK_BYTES_PER_WEIGHT
+    gate, stk = {}, {}
+    for M in sweep:
+        xa = torch.from_numpy(synthetic.normal(synthetic.act_seed(5, M), (M, 3584))).to(dev)
+        xb = torch.from_numpy(synthetic.normal(synthetic.act_seed(5, M) + 1, (M, 18944))).to(dev)
+        ys = {n: torch.empty((M, synthetic.QWEN7B_LINEARS[n][0]), device=dev) for n in TYPES}
+
+        def issue_gate(fl=0):
+            for l in range(Lg):
+                q4.q4mm_forward_ex(stack["gate_proj"][l], xa, fl, y=ys["gate_proj"], stream=stream)
+        us = _graph_us(torch, stream, issue_gate, reps, Lg)
+        gate[str(M)] = {"us": us, "weight_gbs": gb / us / 1e3, "frac_of_measured_hbm": gb / us / 1e3 / peak,
+                        "token_rows_per_s": M / us * 1e6, "path": q4.q4mm_select_path(stack["gate_proj"][0], M)}
+        if M in (8, 16, 24, 32, 64):
+            gate[str(M)]["streaming_us"] = _graph_us(torch, stream, lambda: issue_gate(q4.Q4MM_FORCE_MMA), reps, Lg)
+            gate[str(M)]["tensor_core_us"] = _graph_us(torch, stream, lambda: issue_gate(q4.Q4MM_FORCE_TC), reps, Lg)
+
+        def issue_stack():
+            for l in range(Lg):
+                for gname, names in GROUPS:
+                    x = xb if names[0] == "down_proj" else xa
+                    if len(names) == 1:
+                        q4.q4mm_forward(stack[names[0]][l], x, y=ys[names[0]], stream=stream)
+                    else:
+                        q4.q4mm_forward_group([stack[n][l] for n in names], x, ys=[ys[n] for n in names],
+                                              stream=stream)
+        us = _graph_us(torch, stream, issue_stack, max(3, reps // 2), Lg)
+        stk[str(M)] = {"us_per_layer": us, "weight_gbs": lb / us / 1e3, "frac_of_measured_hbm": lb / us / 1e3 / peak,
+                       "token_rows_per_s": M / us * 1e6}
+    cross = None
+    for M in (8, 16, 24, 32, 64):
+        g = gate[str(M)]
+        if g["tensor_core_us"] <= g["streaming_us"]:
+            cross = M
+            break
+    out["c5_m_sweep"] = {"workload": "M sweep on gate_proj 18944x3584 (%d copies) and on the %d-layer stack "
+                                     "(grouped q/k/v and gate/up calls)" % (Lg, Lg),
+                         "gate_proj": gate, "stack": stk,
+                         "measured_crossover_gate": cross, "m_threshold": q4.q4mm_get_m_threshold(),
+                         "group_m_threshold": q4.q4mm_get_group_m_threshold()}
+    if with_oracle:
+        out["oracle_single_core"] = _oracle_single_core()
+    return out
+
 
 
 def run_path_sweep(args):
@@ -598,19 +822,13 @@ def run_path_sweep(args):
     return 0
 
 
-def run_lm_head(args):
-    """Fused greedy pick (q4mm_argmax) on the Qwen2.5-7B LM head, 152064 x 3584
-    Q4_0 (N(0, 0.02^2) weights, fp32 N(0,1) activations), at M = 1, 4, 16.
-    Two weight copies (612 MB, far beyond L2) alternate between calls.  Prints
-    one JSON line; GB/s counts packed weight bytes."""
-    import numpy as np
-    import torch
-
-    import bit_quantized_matmul_gb300 as q4
+def lm_head_cases(q4, torch, dev, stream, reps=10):
+    """Fused greedy pick (q4mm_argmax through the C ABI) on the Qwen2.5-7B LM
+    head, 152064 x 3584 Q4_0 (N(0, 0.02^2) weights, fp32 N(0,1) activations),
+    at M = 1, 4, 16.  Two weight copies (612 MB, far beyond L2) alternate
+    between the 20 calls of one CUDA graph; no logits are written."""
     import synthetic
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     N, K = synthetic.LM_HEAD
     Ws = []
     for c in range(2):
@@ -618,52 +836,48 @@ def run_lm_head(args):
         Ws.append(q4.q4_quantize(w))
         del w
     wbytes = N * K * BLOCK_BYTES_PER_WEIGHT
-    stream = torch.cuda.Stream(dev)
     peak, kind = _peaks()
+    lib = q4.raw_library()
     cases = {}
     for M in (1, 4, 16):
         x = torch.from_numpy(synthetic.normal(synthetic.act_seed(3, M), (M, K))).to(dev)
         idx = torch.empty((M,), dtype=torch.int32, device=dev)
         mx = torch.empty((M,), dtype=torch.float32, device=dev)
-        lib = q4.raw_library()
-        reps = 20
+        calls = 20
 
         def issue():
-            for r in range(reps):
+            for r in range(calls):
                 st = lib.q4mm_argmax(Ws[r % 2].handle, x.data_ptr(), idx.data_ptr(), mx.data_ptr(), M,
                                      stream.cuda_stream)
                 assert st == q4.Q4_OK, st
-        with torch.cuda.stream(stream):
-            for _ in range(max(3, args.warmup)):
-                issue()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                issue()
-        torch.cuda.synchronize(dev)
-        times = []
-        for _ in range(max(1, args.steps)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-            torch.cuda.synchronize(dev)
-            times.append(e0.elapsed_time(e1) * 1e3 / reps)
-        us = statistics.median(times)
+        us = _graph_us(torch, stream, issue, reps, calls)
         path = q4.q4mm_plan_info(Ws[0], M)[0]
         cases[str(M)] = {"us_per_call": us, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
                          "frac_of_measured_hbm": wbytes / (us * 1e-6) / 1e9 / peak,
                          "token_rows_per_s": M / (us * 1e-6), "path": int(path)}
     assert q4.q4_device_status() == q4.Q4_OK
-    line = {"metric": "LM-head greedy pick (fused argmax) weight GB/s", "unit": "GB/s",
-            "value": cases["1"]["weight_gbs"], "n_gpus": 1, "higher_is_better": True, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": "qwen2.5-7b LM head 152064x3584 Q4_0, M = 1, 4, 16, fused argmax "
-                                   "(no logits written)", "l2": "two weight copies (612 MB) alternate"},
-            "cases": cases, "peak_gbs": peak, "peak_source": kind}
-    print(json.dumps(line), flush=True)
     for W in Ws:
         W.free()
+    return {"workload": "qwen2.5-7b LM head 152064x3584 Q4_0, M = 1, 4, 16, fused argmax (no logits written)",
+            "l2": "two weight copies (612 MB) alternate", "per_M": cases, "peak_gbs": peak, "peak_source": kind}
+
+
+def run_lm_head(args):
+    """The LM-head greedy pick alone; prints one JSON line (GB/s of packed
+    weight bytes)."""
+    import torch
+
+    import bit_quantized_matmul_gb300 as q4
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    c = lm_head_cases(q4, torch, dev, stream, max(5, args.steps))
+    line = {"metric": "LM-head greedy pick (fused argmax) weight GB/s", "unit": "GB/s",
+            "value": c["per_M"]["1"]["weight_gbs"], "n_gpus": 1, "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": c["workload"], "l2": c["l2"]},
+            "cases": c["per_M"], "peak_gbs": c["peak_gbs"], "peak_source": c["peak_source"]}
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -739,6 +953,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config measurements (896x896, M=124 step, LM head, M sweep, "
+                         "single-core oracle)")
     ap.add_argument("--m-sweep", type=lambda v: [int(t) for t in v.split(",")], default=list(M_SWEEP),
                     help="token-row counts of the step (default 1,2,3,4,5,8)")
     ap.add_argument("--separate", action="store_true",

@@ -10,30 +10,48 @@
 // GEMM — with one kernel whose cost per weight hardly changes between 1 and
 // 16 rows, so no row count needs a different kernel or a per-row relaunch.
 //
+// Operands (every product exact, only fp32 accumulation rounds):
+//   weights  (q - 8) as binary16: one three-input LOP3 puts a nibble pair
+//            into the mantissas of 1024 + q (or 1024 + 16 q for the nibbles
+//            in bits 4..7 of a byte), one f16x2 subtraction leaves q - 8 (or
+//            16 (q - 8)), exact.  Rows R1 = R0 + 8 of a row group come from
+//            the high nibble positions and carry the factor 16, removed with
+//            the activation scale below.
+//   x        two binary16 terms per value, x * s = t0 + t1 to 2^-21, with s a
+//            power of two per (token row, 128 consecutive activations: two
+//            block pairs) chosen from their largest |x| so that x * s stays
+//            inside binary16's range; t0 keeps the top 11 significant bits of
+//            x * s, t1 the rest.
+// Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) t in fresh fp32
+// registers; the block's fp16 scale d is applied on the CUDA cores, per block
+// pair P = d_0 D_0 + d_1 D_1, then acc += P / s (1/s exact), in ascending
+// block-pair order.  At the end the K slices and the two terms of each row
+// are added in a fixed order, then the K splits in ascending split order
+// (q4mm_epilogue.cuh).
+//
 // CTA = one 128-row tile over a K range (block pairs [bp0, bp1)); 640 threads:
 //
 //   16 compute warps  warp w takes row groups 2(w&3), 2(w&3)+1 (32 rows) and
-//                     K slice w>>2: block pairs bp0 + slice + 4i (with four
-//                     to six column groups, 9 to 16 rows: row group w&7 and
-//                     K slice (w>>3)&1, block pairs bp0 + slice + 2i).  Its lanes
+//                     K slice w>>2: block pairs bp0 + slice + 4i (with three or
+//                     four column groups, 9 to 16 rows: row group w&7 and K
+//                     slice (w>>3)&1, block pairs bp0 + slice + 2i).  Its lanes
 //                     copy their 16-byte weight fragments (coalesced, 1 KB per
 //                     warp and pair) and lanes 0..7 the pair's 128 bytes of
 //                     fp16 scales (512 and 64 bytes with one row group per
-//                     warp) from HBM into the warp's private cp.async
-//                     ring, two pairs ahead; each lane reads back its own
-//                     fragments, which in the fragment layout are exactly the
-//                     A registers of m16n8k16 MMAs once unpacked to exact bf16
-//                     (q - 8).  The first pairs are on their way before the
-//                     kernel waits for the previous one on the stream (weights
-//                     never depend on it).  No CTA barrier in the loop.
+//                     warp) from HBM into the warp's private cp.async ring,
+//                     two pairs ahead; each lane reads back its own fragments,
+//                     which in the fragment layout are exactly the A registers
+//                     of m16n8k16 MMAs once unpacked.  The first pairs are on
+//                     their way before the kernel waits for the previous one
+//                     on the stream (weights never depend on it).  No CTA
+//                     barrier in the loop.
 //   4 converter warps stage, per chunk of 8 block pairs, the activations as
-//                     exact three-term bf16 B fragments (x = x0 + x1 + x2,
-//                     term t of row m in MMA column 3m + t, or column t of the
-//                     row's own column group in batch-invariant mode) into a
-//                     4-slot (2-slot from four column groups) shared-memory
-//                     ring with full/empty mbarriers
+//                     the two binary16 terms above in B-fragment order (term t
+//                     of token row m in MMA column 2m + t) together with each
+//                     row's 1/s, into a 4-slot (2-slot from three column
+//                     groups) shared-memory ring with full/empty mbarriers
 //                     (every wait bounded).  The fp32 rows arrive by cp.async
-//                     four or five chunks ahead (two from four column groups).
+//                     several chunks ahead.
 //
 // Launches of more tiles than SMs with one K split (the gate/up group of a 7B
 // layer: 296 tiles) and one or two column groups run as two-tile CTAs: a CTA
@@ -47,15 +65,13 @@
 // slices.  Its K reduction is then a shared-memory sum; no partial sums cross
 // CTAs, whose exchange costs 1-2 us in the tail of every split launch.
 //
-// Per block the two MMAs accumulate D_b = sum_{k in b} (q-8) x_t in fresh
-// fp32 registers; the block's fp16 scale is applied on the CUDA cores,
-// acc = fma(d, D_b, acc), in ascending block order.  At the end the four (or
-// two) K slices and the three terms of each row are added in a fixed order,
-// then the K splits in ascending split order (q4mm_epilogue.cuh).  In
-// batch-invariant mode nothing in that order depends on M; in the default
-// mode the launch's row count picks the CTA layout (row-group or two-tile CTAs
-// up to 8 rows, two K slices from 9), so a row's bits may differ with M
-// within the tolerance.
+// Batch-invariant mode runs every launch, whatever its row count, with the
+// same four-column-group kernel and the K partition of the shapes: a row goes
+// through the same operations in the same order wherever it sits in the
+// launch (an MMA output element depends only on its own row of A, column of
+// B and accumulator input) and whatever its neighbours hold (its scales come
+// from its own values).  In the default mode the launch's row count picks the
+// CTA layout, so a row's bits may differ with M within the tolerance.
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -66,8 +82,7 @@
 namespace q4 {
 namespace {
 
-constexpr int MAX_CG = 3;          // column groups per launch with one row per group
-constexpr int MAX_CG_DENSE = 6;    // column groups per launch with dense packing (48 MMA columns)
+constexpr int MAX_CG = 4;          // column groups per launch: two terms per token row, 16 rows
 constexpr int SLICES = 4;          // K slices per CTA
 constexpr int COMPUTE_WARPS = 16;  // 4 row-group pairs x 4 slices
 constexpr int CONV_WARPS = 4;
@@ -81,8 +96,11 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 // M = 1..8: a ring of two pairs with the loop unrolled twice (slot indices and
 // the once-per-chunk barrier steps become compile-time constants) beat rings
 // of 3, 4 and 8 pairs, four-fold unrolling and loading the next pair early.
-#ifndef Q4MM_WD
-#define Q4MM_WD 2
+#ifndef Q4MM_WD1
+#define Q4MM_WD1 2  // CTAs of one tile
+#endif
+#ifndef Q4MM_WD2
+#define Q4MM_WD2 2  // two-tile CTAs (twice the bytes per pair)
 #endif
 #ifndef Q4MM_UNROLL
 #define Q4MM_UNROLL 2
@@ -97,6 +115,15 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 #ifndef Q4MM_RG_MAX_K
 #define Q4MM_RG_MAX_K 4096
 #endif
+// B ring depth of row-group CTAs: every chunk of a K up to 4096
+#ifndef Q4MM_RG_NSLOT
+#define Q4MM_RG_NSLOT 4
+#endif
+// convert every chunk of a CTA's activations before its main loop (launches
+// of one or two column groups whose CTAs cover at most UP_CHUNKS chunks)
+#ifndef Q4MM_UPFRONT
+#define Q4MM_UPFRONT 1
+#endif
 #ifndef Q4MM_TWO_TILES
 #define Q4MM_TWO_TILES 1
 #endif
@@ -106,6 +133,7 @@ constexpr int T2_LD = 2 * TILE_N + 4;  // row stride of the two-tile slice sums 
 // the accumulator stores of a warp (lanes 4g + tq at column 2tq, row g) hit
 // 32 different banks and the per-row reads stay consecutive
 constexpr int RED_LD = TILE_N + 4;
+constexpr int TERMS = 2;  // binary16 terms per activation
 
 // One weight of a launch.  A launch covers the tiles of up to MMA_GROUP_MAX
 // weights that share K and the activations (e.g. the q, k and v projections):
@@ -132,24 +160,32 @@ struct MmaArgs {
   EpiArgs e;
 };
 
-template <int C, int TPC = 1, bool DENSE = true, bool RG = false>
+// Launches of one or two column groups whose CTAs cover at most this many
+// chunks convert all their activations before the main loop, with every
+// thread of the CTA, into one ring slot per chunk.
+constexpr int UP_CHUNKS = 8;
+
+template <int C, int TPC = 1, bool RG = false, bool UP = false>
 struct MmaCfg {
-  static constexpr int MAXM = (C * 8) / 3 > C ? (C * 8) / 3 : C;  // rows per launch
-  // four to six column groups (9 to 16 token rows, dense): one row group per
-  // compute warp, 8 row groups x 2 K slices, so that the accumulators of six
-  // groups fit; a two-slot B ring and three x stages, so that the larger
-  // fragments fit in shared memory
-  // (measured on GB300: three column groups are faster with two row groups
-  // per warp, and batch-invariant launches keep one layout for every C)
-  static constexpr bool R1 = DENSE && !RG && TPC == 1 && C >= 4;
+  static constexpr int MAXM = C * 8 / TERMS;  // token rows per launch
+  // three or four column groups (9 to 16 token rows): one row group per
+  // compute warp, 8 row groups x 2 K slices, so that the accumulators fit;
+  // a two-slot B ring and three x stages, so that the larger fragments fit in
+  // shared memory
+  static constexpr bool R1 = !RG && TPC == 1 && C >= 3;
   static constexpr int NSL = R1 ? 2 : SLICES;  // K slices of a tile's CTA
   static constexpr int NRG = R1 ? 1 : 2;       // row groups per compute warp
-  static constexpr int NSLOT = R1 ? 2 : 4;     // B ring depth (a power of two)
+  // B ring depth (a power of two); row-group CTAs hold every chunk of their
+  // K (at most 8) so that their converters never wait for a slot
+  static constexpr int NSLOT = UP ? UP_CHUNKS : (RG ? Q4MM_RG_NSLOT : (R1 ? 2 : 4));
   static constexpr int BF_PAIR = C * 1024;  // B fragments of a pair: [cg][h][32 slots] x 16 B
-  static constexpr int SLOT = CHUNK_PAIRS * BF_PAIR;
+  // per (pair, token row) {1/s, 1/s, 1/(16 s), 1/(16 s)}, after the fragments
+  static constexpr int SIG_OFF = CHUNK_PAIRS * BF_PAIR;
+  static constexpr int SLOT = SIG_OFF + CHUNK_PAIRS * MAXM * 16;
   static constexpr int RING = NSLOT * SLOT;
   // converter staging: per slot the chunk's raw fp32 x rows
-  static constexpr int XSTAGES = R1 ? 3 : (C == 3 ? 5 : 6);  // chunks of x in flight + the one converted
+  // chunks of x in flight + the one converted
+  static constexpr int XSTAGES = UP ? 0 : ((R1 || (RG && C == 2)) ? 3 : (C == 2 ? 4 : 6));
   static constexpr int XSLOT = MAXM * CHUNK_K * 4;
   static constexpr int XRAW_OFF = RING;
   static constexpr int RED = NSL * C * 8 * RED_LD * 4;  // per-slice sums for the gather
@@ -158,7 +194,7 @@ struct MmaCfg {
   // weight pairs in flight per compute warp: a private ring of WD slots, each
   // the warp's 16-byte fragments of its two row groups (1 KB) and their fp16
   // scales (128 B), filled by cp.async (half of that with one row group)
-  static constexpr int WD = Q4MM_WD;
+  static constexpr int WD = TPC == 2 ? Q4MM_WD2 : Q4MM_WD1;
   static constexpr int WSLOT = NRG * (512 + 64);
   static constexpr int WSCL = NRG * 512;  // offset of the scales in a slot
   static constexpr int WR_OFF = RING + XSTAGES * XSLOT;
@@ -166,42 +202,63 @@ struct MmaCfg {
   static constexpr int BAR_OFF = WR_OFF + WR > XCH_OFF + XCH ? WR_OFF + WR : XCH_OFF + XCH;
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static_assert(!R1 || TPC == 1, "one row group per warp: one tile per CTA");
-  static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
+  static_assert(!UP || C <= 2, "up-front conversion: one or two column groups");
+  static_assert(BYTES <= 227 * 1024 - 1024, "shared memory of one CTA");
+  static_assert(SLOT % 16 == 0 && XSLOT % 16 == 0, "16-byte aligned ring slots");
 };
 
-// bf16 pair (q - 8) for nibble pair p of word w: 0x4300 | q is bf16(128 + q),
-// and one bf16x2 subtraction of 136 is exact.
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int p) {
-  uint32_t t, r;
-  // (w >> 4p) & 0x000F000F | 0x43004300 as one three-input logic op
-  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(w >> (4 * p)));
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
-  return r;
+// The four A-fragment registers of one 32-bit fragment word (nibble pairs
+// p = 0..3 at bits 4p and 16 + 4p) as exact binary16 pairs: 0x6400 | q is
+// 1024 + q and 0x6400 | (q << 4) is 1024 + 16 q; one f16x2 subtraction of
+// 1032 (or 1152) leaves q - 8 (or 16 (q - 8)).  Pairs 0 and 2 are rows R0,
+// pairs 1 and 3 rows R1 (factor 16).
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  uint32_t t0, t1, t2, t3;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(t0) : "r"(w));
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(t1) : "r"(w));
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(t2) : "r"(w8));
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(t3) : "r"(w8));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(t0), "r"(0x64086408u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(a[1]) : "r"(t1), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(a[2]) : "r"(t2), "r"(0x64086408u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(a[3]) : "r"(t3), "r"(0x64806480u));
 }
 
 // D = A B + C with C = 0 (first k-step of a block) and with C = D (second).
-__device__ __forceinline__ void mma_bf16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+__device__ __forceinline__ void mma_f16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%10, %10, %10, %10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
-__device__ __forceinline__ void mma_bf16_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                             uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                            uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two fp32 accumulators in one 64-bit register pair: acc += s * (c0, c1), one
-// packed instruction, each half an ordinary fp32 fma.  `ss` holds {s, s}.
+// Two fp32 values in one 64-bit register pair; packed fp32x2 arithmetic, each
+// half an ordinary fp32 operation.  `ss` holds {s, s} (or two factors).
 __device__ __forceinline__ unsigned long long dup2(float s) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
   return r;
 }
+// r = ss * (c0, c1)
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long ss, float c0, float c1) {
+  unsigned long long r;
+  asm("{\n\t.reg .b64 rc;\n\t"
+      "mov.b64 rc, {%2, %3};\n\t"
+      "mul.rn.f32x2 %0, %1, rc;\n\t}"
+      : "=l"(r)
+      : "l"(ss), "f"(c0), "f"(c1));
+  return r;
+}
+// acc += ss * (c0, c1)
 __device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long long ss, float c0,
                                       float c1) {
   asm("{\n\t.reg .b64 rc;\n\t"
@@ -209,6 +266,11 @@ __device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long lon
       "fma.rn.f32x2 %0, %1, rc, %0;\n\t}"
       : "+l"(acc)
       : "l"(ss), "f"(c0), "f"(c1));
+}
+// acc += ss * v (both packed)
+__device__ __forceinline__ void ffma2p(unsigned long long& acc, unsigned long long ss,
+                                       unsigned long long v) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(ss), "l"(v));
 }
 __device__ __forceinline__ float2 split2(unsigned long long v) {
   float2 r;
@@ -287,22 +349,55 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// Exact three-term bf16 split of two consecutive activations: term 0 is the
-// top 16 bits of x (truncation), term 1 the top 16 bits of the exact
-// remainder, term 2 the rest (at most 8 significant bits, exact in bf16).
-// Each term packs (k, k + 1) as a bf16x2 word, k in the low half.
-__device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_t& t1,
-                                       uint32_t& t2) {
-  uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
-  t0 = __byte_perm(u0, u1, 0x7632);
-  float r0 = x0 - __uint_as_float(u0 & 0xFFFF0000u);
-  float r1 = x1 - __uint_as_float(u1 & 0xFFFF0000u);
-  u0 = __float_as_uint(r0);
-  u1 = __float_as_uint(r1);
-  t1 = __byte_perm(u0, u1, 0x7632);
-  r0 -= __uint_as_float(u0 & 0xFFFF0000u);
-  r1 -= __uint_as_float(u1 & 0xFFFF0000u);
-  t2 = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+// the same copy, issued only where `on` is nonzero (a predicate, no branch)
+__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void* src, uint32_t on) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}"
+               ::"r"(dst), "l"(src), "r"(on) : "memory");
+}
+
+// binary16 pair (lo, hi) rounded to nearest
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two-term binary16 split of four activations (k .. k + 3) scaled by s:
+// y = x s (exact, s a power of two), t0 keeps the top 11 significant bits of
+// y (exact in binary16 whenever |y| >= 2^-14), t1 = y - t0 rounded to
+// binary16, so y - t0 - t1 is at most 2^-21 |y| (plus 2^-24 where the terms
+// fall below binary16's normal range).  Each term packs (k, k + 1) or
+// (k + 2, k + 3) as an f16x2 word, the lower k in the low half.
+__device__ __forceinline__ void split4(const float4& v, float s, uint32_t (&ta)[2], uint32_t (&tb)[2]) {
+  float y0, y1, y2, y3, r0, r1, r2, r3;
+  asm("{\n\t.reg .b64 xa, xb, ss, ya, yb;\n\t"
+      "mov.b64 xa, {%8, %9};\n\t"
+      "mov.b64 xb, {%10, %11};\n\t"
+      "mov.b64 ss, {%12, %12};\n\t"
+      "mul.rn.f32x2 ya, xa, ss;\n\t"
+      "mul.rn.f32x2 yb, xb, ss;\n\t"
+      "mov.b64 {%0, %1}, ya;\n\t"
+      "mov.b64 {%2, %3}, yb;\n\t}"
+      : "=f"(y0), "=f"(y1), "=f"(y2), "=f"(y3), "=f"(r0), "=f"(r1), "=f"(r2), "=f"(r3)
+      : "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "f"(s));
+  const float h0 = __uint_as_float(__float_as_uint(y0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(y1) & 0xFFFFE000u);
+  const float h2 = __uint_as_float(__float_as_uint(y2) & 0xFFFFE000u);
+  const float h3 = __uint_as_float(__float_as_uint(y3) & 0xFFFFE000u);
+  asm("{\n\t.reg .b64 ya, yb, ha, hb, ra, rb;\n\t"
+      "mov.b64 ya, {%4, %5};\n\t"
+      "mov.b64 yb, {%6, %7};\n\t"
+      "mov.b64 ha, {%8, %9};\n\t"
+      "mov.b64 hb, {%10, %11};\n\t"
+      "sub.rn.f32x2 ra, ya, ha;\n\t"
+      "sub.rn.f32x2 rb, yb, hb;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t"
+      "mov.b64 {%2, %3}, rb;\n\t}"
+      : "=f"(r0), "=f"(r1), "=f"(r2), "=f"(r3)
+      : "f"(y0), "f"(y1), "f"(y2), "f"(y3), "f"(h0), "f"(h1), "f"(h2), "f"(h3));
+  ta[0] = pack_f16x2(h0, h1);
+  ta[1] = pack_f16x2(r0, r1);
+  tb[0] = pack_f16x2(h2, h3);
+  tb[1] = pack_f16x2(r2, r3);
 }
 
 // ----------------------------------------------------------------------------
@@ -312,9 +407,9 @@ __device__ __forceinline__ void split3(float x0, float x1, uint32_t& t0, uint32_
 // reads its 512 contiguous bytes conflict-free in any slot order).  The slot
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
-template <int C, bool DENSE, bool RG, int TPC>
+template <int C, bool RG, int TPC, bool UP>
 __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
-  using S = MmaCfg<C, TPC, DENSE, RG>;
+  using S = MmaCfg<C, TPC, RG, UP>;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -328,8 +423,8 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // RG: the CTA is row-group pair blockIdx.x & 3 of global tile blockIdx.x >> 2
   // over the whole K, and its 16 compute warps are 16 K slices; otherwise the
   // CTA is global tile blockIdx.x over K split blockIdx.y, its compute warps
-  // 4 row-group pairs x 4 K slices (8 row groups x 2 K slices with four to
-  // six column groups)
+  // 4 row-group pairs x 4 K slices (8 row groups x 2 K slices with three or
+  // four column groups)
   // TPC = 2: the CTA takes global tiles 2 blockIdx.x and 2 blockIdx.x + 1 (the
   // second when it exists) over the whole K; its warps cover the same row
   // groups of both, and the converted activations serve both
@@ -381,43 +476,46 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   const uint8_t* sp = scl_w + (tile * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + rg0 * 64 + lane * 16;
   const uint8_t* sp1 = a.w[wi1].scl + (tile1 * a.KBP + bp0 + sl) * PAIR_SCL_BYTES + rg0 * 64 + lane * 16;
   constexpr int64_t SSTEP = NSL * PAIR_SCL_BYTES;  // scale bytes between a slice's pairs
-  auto fetch = [&](int i) {  // pair i of this warp's K slice into slot i % WD
-    if (i < n_i) {
-      const uint32_t d = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC);
-      cp_async16(d + lane * 16, wp + (int64_t)i * WSTEP);
-      if (NRG == 2) cp_async16(d + 512u + lane * 16, wp + (int64_t)i * WSTEP + 32);
-      if (lane < 4 * NRG) cp_async16(d + S::WSCL + lane * 16, sp + (int64_t)i * SSTEP);
-      if (TPC == 2 && has1) {
-        cp_async16(d + S::WSLOT + lane * 16, wp1 + (int64_t)i * WSTEP);
-        cp_async16(d + S::WSLOT + 512u + lane * 16, wp1 + (int64_t)i * WSTEP + 32);
-        if (lane < 8) cp_async16(d + S::WSLOT + 1024u + lane * 16, sp1 + (int64_t)i * SSTEP);
-      }
+  // the next pair of this warp's K slice to fetch, and its sources (running
+  // pointers; past the end nothing is dereferenced: every copy is predicated)
+  int fnext = 0;
+  const uint4* wsrc = wp;
+  const uint4* wsrc1 = wp1;
+  const uint8_t* ssrc = sp;
+  const uint8_t* ssrc1 = sp1;
+  auto fetch = [&]() {  // pair fnext into slot fnext % WD
+    const uint32_t ok = fnext < n_i;
+    const uint32_t d = wring + (uint32_t)(fnext % WD) * (S::WSLOT * TPC);
+    cp_async16_if(d + lane * 16, wsrc, ok);
+    if (NRG == 2) cp_async16_if(d + 512u + lane * 16, wsrc + 32, ok);
+    cp_async16_if(d + S::WSCL + lane * 16, ssrc, ok & (uint32_t)(lane < 4 * NRG));
+    if (TPC == 2) {
+      const uint32_t ok1 = ok & (uint32_t)has1;
+      cp_async16_if(d + S::WSLOT + lane * 16, wsrc1, ok1);
+      cp_async16_if(d + S::WSLOT + 512u + lane * 16, wsrc1 + 32, ok1);
+      cp_async16_if(d + S::WSLOT + 1024u + lane * 16, ssrc1, ok1 & (uint32_t)(lane < 8));
+      wsrc1 += WSTEP;
+      ssrc1 += SSTEP;
     }
     asm volatile("cp.async.commit_group;" ::: "memory");  // one group per pair, empty or not
+    wsrc += WSTEP;
+    ssrc += SSTEP;
+    ++fnext;
   };
   if (compute) {
 #pragma unroll
-    for (int u = 0; u < WD; ++u) fetch(u);
+    for (int u = 0; u < WD; ++u) fetch();
   }
 
-  // zero the B-fragment columns no converter writes: the last column group
-  // (dense packing with 3 * mrows < 8C) or every group (one row per group)
-  {
-    const bool part = DENSE ? (3 * mrows < 8 * C) : true;
-    if (part) {
-      constexpr int PER_SLOT = DENSE ? CHUNK_PAIRS * 2 * 32 : CHUNK_PAIRS * C * 2 * 32;  // uint4
-      for (int j = tid; j < NSLOT * PER_SLOT; j += KERNEL_THREADS) {
-        const int slot = j / PER_SLOT, r = j % PER_SLOT;
-        int off;
-        if (DENSE) {
-          const int pc = r >> 6, h = (r >> 5) & 1, q = r & 31;
-          off = ((pc * C + (C - 1)) * 2 + h) * 512 + q * 16;
-        } else {
-          off = r * 16;
-        }
-        *reinterpret_cast<uint4*>(smem + slot * S::SLOT + off) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+  // zero the B fragments of every slot when some columns are not written by
+  // a converter (fewer rows than the launch's column groups hold); the
+  // converters then overwrite the columns of the real rows
+  if (TERMS * mrows < 8 * C) {
+    constexpr int PER_SLOT = S::SIG_OFF / 16;  // uint4 of B fragments per slot
+    const int zslots = UP ? nchunks : NSLOT;
+    for (int j = tid; j < zslots * PER_SLOT; j += KERNEL_THREADS)
+      *reinterpret_cast<uint4*>(smem + (j / PER_SLOT) * S::SLOT + (j % PER_SLOT) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
   }
   if (tid == 0) {
     for (int b = 0; b < NSLOT; ++b) {
@@ -432,198 +530,210 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   }
   __syncthreads();
 
-  // accumulators: [rg][cg][row R0 / R1] as {column 2tq, column 2tq + 1} pairs
-  // (packed fp32x2 updates) up to two column groups; as four floats [rg][cg][e]
-  // for three, where the extra registers of the packed form would spill
-  // (packed with one row group per warp for four and five groups; six spill,
-  // measured slower)
-  constexpr bool PACKED = C <= 2 || (R1 && C <= 5);
+  if constexpr (UP) {
+    // ---- every thread: the activations of all chunks, straight from x ----
+    // 128 threads per chunk (k = 4ct .. 4ct + 3), five chunk sets; every load
+    // is issued before any is used
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+    constexpr int CSETS = KERNEL_THREADS / 128;
+    constexpr int PER = (UP_CHUNKS + CSETS - 1) / CSETS;
+    const int ct = tid & 127, cset = tid >> 7;
+    const int pc = ct >> 4, h = (ct >> 3) & 1, j = (ct >> 1) & 3, tql = 2 * (ct & 1);
+    const int kbase = (pc * C * 2 + h) * 512 + j * 4;
+    const int s2 = pc & 1;
+    const int oa = ((tql) ^ h) * 16, ob = ((tql + 1) ^ h) * 16;
+    // row m of this launch: x row xrows[m] when a row list is given (checked:
+    // an index outside [0, x_rows) reads zeros and sets STATUS_BAD_ROW)
+    auto row_off = [&](int m) -> int64_t {
+      if (a.xrows == nullptr) return (int64_t)m * a.K;
+      const int32_t r = __ldg(a.xrows + m);
+      if (r >= 0 && (int64_t)r < a.x_rows) return (int64_t)r * a.K;
+      if (tid == 0 && split == 0) atomicOr(a.status, STATUS_BAD_ROW);
+      return -1;
+    };
+    const float* xr = a.x + bp0 * 64 + 4 * ct;
+    float4 v[PER][MAXM];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int c = cset + q * CSETS;
+      const bool k_ok = c < nchunks && c * CHUNK_PAIRS + pc < npairs &&
+                        (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m) {
+        v[q][m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (k_ok && m < mrows) {
+          const int64_t off = row_off(m);
+          if (off >= 0) v[q][m] = __ldg(reinterpret_cast<const float4*>(xr + off + (int64_t)c * CHUNK_K));
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int c = cset + q * CSETS;
+      if (c >= nchunks) break;  // the same for the whole warp
+      uint8_t* sb = smem + c * S::SLOT;
+      const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m) {
+        if (m >= mrows) break;  // the same for every thread of the CTA
+        // largest |x| of row m over the warp's 128 elements (two block pairs)
+        uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(v[q][m].x), fabsf(v[q][m].y)),
+                                           fmaxf(fabsf(v[q][m].z), fabsf(v[q][m].w))));
+        asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u));
+        int e = 14 - ((int)(u >> 23) - 127);
+        e = max(-120, min(120, e));
+        const float sc = __int_as_float((e + 127) << 23);
+        if (pair_ok) {
+          uint32_t ta[TERMS], tb[TERMS];
+          split4(v[q][m], sc, ta, tb);
+#pragma unroll
+          for (int t = 0; t < TERMS; ++t) {
+            const int col = TERMS * m + t;
+            const int cg = col >> 3, gl = col & 7;
+            uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
+            *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
+            *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
+          }
+          if ((ct & 15) == 0) {
+            const float r1 = __int_as_float((127 - e) << 23);
+            const float r16 = __int_as_float((123 - e) << 23);
+            *reinterpret_cast<float4*>(sb + S::SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // accumulators [tile][rg][cg][row R0 / R1] as {column 2tq, column 2tq + 1}
+  // pairs (packed fp32x2 updates)
   static_assert(!(R1 && RG), "row-group CTAs have two row groups per warp");
   unsigned long long acc[TPC][NRG][C][2];
-  float accf[TPC][NRG][C][4];
 #pragma unroll
   for (int tt = 0; tt < TPC; ++tt)
 #pragma unroll
     for (int r = 0; r < NRG; ++r)
 #pragma unroll
-      for (int cg = 0; cg < C; ++cg) {
-        acc[tt][r][cg][0] = acc[tt][r][cg][1] = 0ull;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) accf[tt][r][cg][e] = 0.0f;
-      }
+      for (int cg = 0; cg < C; ++cg) acc[tt][r][cg][0] = acc[tt][r][cg][1] = 0ull;
 
   if (compute) {
-    const int g = lane >> 2;
+    const int g = lane >> 2, tq = lane & 3;
     const int lsw0 = (lane ^ ((sl & 1) * 4)) * 16;        // slot of this lane, h = 0
     const int lsw1 = (lane ^ ((sl & 1) * 4 + 1)) * 16;    // h = 1
     // the 16-byte words and scales of pair i of this warp, once they are in
     // (this lane's groups complete in order, WD - 1 may still fly; the warp
     // barrier makes lanes 0..7's scale copies visible to all lanes)
-    auto load_pair = [&](int i, int tt, uint4& a0, uint4& a1, uint2& s0, uint2& s1) {
+    auto load_pair = [&](int i, int tt, uint4 (&w)[2], uint2 (&sv)[2]) {
       if (tt == 0) {
         asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
         __syncwarp();
       }
       const uint32_t src = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC) + (uint32_t)(tt * S::WSLOT);
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(a0.x), "=r"(a0.y), "=r"(a0.z), "=r"(a0.w) : "r"(src + lane * 16) : "memory");
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(a1.x), "=r"(a1.y), "=r"(a1.z), "=r"(a1.w) : "r"(src + 512u + lane * 16) : "memory");
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s0.x), "=r"(s0.y) : "r"(src + 1024u + g * 8) : "memory");
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s1.x), "=r"(s1.y) : "r"(src + 1088u + g * 8) : "memory");
+#pragma unroll
+      for (int r = 0; r < NRG; ++r) {
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[r].x), "=r"(w[r].y), "=r"(w[r].z), "=r"(w[r].w)
+                     : "r"(src + r * 512u + lane * 16)
+                     : "memory");
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(sv[r].x), "=r"(sv[r].y)
+                     : "r"(src + S::WSCL + r * 64u + g * 8)
+                     : "memory");
+      }
     };
-    // the same with one row group per warp
-    auto load_pair1 = [&](int i, uint4& a0, uint2& s0) {
-      asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
-      __syncwarp();
-      const uint32_t src = wring + (uint32_t)(i % WD) * S::WSLOT;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(a0.x), "=r"(a0.y), "=r"(a0.z), "=r"(a0.w) : "r"(src + lane * 16) : "memory");
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(s0.x), "=r"(s0.y) : "r"(src + S::WSCL + g * 8) : "memory");
-    };
-    {
 #if Q4MM_UNROLL == 2
 #pragma unroll 2
 #elif Q4MM_UNROLL == 4
 #pragma unroll 4
 #endif
-      for (int i = 0; i < n_i; ++i) {
-        // chunk of this pair: slice sl's pairs are sl + NSL i
-        const int c = RG ? 2 * i + (sl >> 3) : (R1 ? (i >> 2) : (i >> 1));
-        const int slot = c & (NSLOT - 1);
-        if ((RG || (R1 ? (i & 3) == 0 : (i & 1) == 0)) &&
-            !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
-          s_err = 1;
-          goto compute_done;
-        }
-        const int pc = RG ? (sl & 7) : (R1 ? sl + 2 * (i & 3) : sl + 4 * (i & 1));  // pair within the chunk
-        const uint8_t* sb = smem + slot * S::SLOT;
-        if constexpr (R1) {
-          // one row group: A fragments of its two k-steps per block, C column
-          // groups of MMAs, the block scale on the CUDA cores as below
-          uint4 w0;
-          uint2 sv0;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
-          load_pair1(i, w0, sv0);
+    for (int i = 0; i < n_i; ++i) {
+      // chunk of this pair: slice sl's pairs are sl + NSL i
+      const int c = RG ? 2 * i + (sl >> 3) : (R1 ? (i >> 2) : (i >> 1));
+      const int slot = UP ? c : (c & (NSLOT - 1));
+      if (!UP && (RG || (R1 ? (i & 3) == 0 : (i & 1) == 0)) &&
+          !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
+        s_err = 1;
+        break;
+      }
+      const int pc = RG ? (sl & 7) : (R1 ? sl + 2 * (i & 3) : sl + 4 * (i & 1));  // pair within the chunk
+      const uint8_t* sb = smem + slot * S::SLOT;
+      // {1/s, 1/s} and {1/(16 s), 1/(16 s)} of token row 4 cg + tq (the
+      // lane's two columns are that row's two terms; rows beyond the launch's
+      // are not written: their columns are never read back)
+      const uint32_t sig = smem_u32(sb + S::SIG_OFF + (pc * MAXM + tq) * 16);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t a0[4], a1[4];  // [k-step]
-            const uint32_t x0 = h ? w0.z : w0.x, x1 = h ? w0.w : w0.y;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              a0[p] = nib_pair(x0, p);
-              a1[p] = nib_pair(x1, p);
-            }
-            if (h == 1) {  // every lane has unpacked both its words: refill the slot
-              __syncwarp();
-              fetch(i + WD);
-            }
-            const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
-            const float f0 = h ? __high2float(q0[0]) : __low2float(q0[0]);
-            const float f1 = h ? __high2float(q0[1]) : __low2float(q0[1]);
-            unsigned long long s0 = 0, s1 = 0;
-            if constexpr (PACKED) {
-              s0 = dup2(f0);
-              s1 = dup2(f1);
-            }
-            const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
-#pragma unroll
-            for (int cg = 0; cg < C; ++cg) {
-              const uint4 bf = *reinterpret_cast<const uint4*>(bb + cg * 1024);
-              float d[4];
-              mma_bf16_first(d, a0, bf.x, bf.y);
-              mma_bf16_acc(d, a1, bf.z, bf.w);
-              if constexpr (PACKED) {
-                ffma2(acc[0][0][cg][0], s0, d[0], d[1]);
-                ffma2(acc[0][0][cg][1], s1, d[2], d[3]);
-              } else {
-                accf[0][0][cg][0] = fmaf(f0, d[0], accf[0][0][cg][0]);
-                accf[0][0][cg][1] = fmaf(f0, d[1], accf[0][0][cg][1]);
-                accf[0][0][cg][2] = fmaf(f1, d[2], accf[0][0][cg][2]);
-                accf[0][0][cg][3] = fmaf(f1, d[3], accf[0][0][cg][3]);
-              }
-            }
-          }
-        } else {
-#pragma unroll
-        for (int tt = 0; tt < TPC; ++tt) {
+      for (int tt = 0; tt < TPC; ++tt) {
         if (tt == 1 && !has1) break;  // the same for every thread of the CTA
-        uint4 w0, w1;
-        uint2 sv0, sv1;  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
-        load_pair(i, tt, w0, w1, sv0, sv1);
+        uint4 w[2];
+        uint2 sv[2];  // .x = d(R0, b0), d(R0, b1); .y = d(R1, b0), d(R1, b1)
+        load_pair(i, tt, w, sv);
+        // this pair's sum d_0 D_0 + d_1 D_1 per [rg][cg][R0 / R1]
+        unsigned long long pp[NRG][C][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t a00[4], a01[4], a10[4], a11[4];  // [rg][k-step]
-          const uint32_t x0 = h ? w0.z : w0.x, x1 = h ? w0.w : w0.y;
-          const uint32_t y0 = h ? w1.z : w1.x, y1 = h ? w1.w : w1.y;
+          uint32_t af[NRG][2][4];  // [rg][k-step][register]
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            a00[p] = nib_pair(x0, p);
-            a01[p] = nib_pair(x1, p);
-            a10[p] = nib_pair(y0, p);
-            a11[p] = nib_pair(y1, p);
+          for (int r = 0; r < NRG; ++r) {
+            unpack_word(h ? w[r].z : w[r].x, af[r][0]);
+            unpack_word(h ? w[r].w : w[r].y, af[r][1]);
           }
-          // refill the slot once every lane has unpacked both its words (the
+          // refill the slot once every lane has unpacked its words (the
           // shared loads have completed, so the copy cannot overtake them);
           // with two tiles, after the second tile's words (or the first's
           // when there is no second)
           if (h == 1 && (TPC == 1 || tt == 1 || !has1)) {
             __syncwarp();
-            fetch(i + WD);
+            fetch();  // pair i + WD
           }
-          const __half2* q0 = reinterpret_cast<const __half2*>(&sv0);
-          const __half2* q1 = reinterpret_cast<const __half2*>(&sv1);
-          const float f00 = h ? __high2float(q0[0]) : __low2float(q0[0]);
-          const float f01 = h ? __high2float(q0[1]) : __low2float(q0[1]);
-          const float f10 = h ? __high2float(q1[0]) : __low2float(q1[0]);
-          const float f11 = h ? __high2float(q1[1]) : __low2float(q1[1]);
-          unsigned long long s00 = 0, s01 = 0, s10 = 0, s11 = 0;
-          if constexpr (PACKED) {
-            s00 = dup2(f00);
-            s01 = dup2(f01);
-            s10 = dup2(f10);
-            s11 = dup2(f11);
+          unsigned long long dd[NRG][2];
+#pragma unroll
+          for (int r = 0; r < NRG; ++r) {
+            const __half2* q = reinterpret_cast<const __half2*>(&sv[r]);
+            dd[r][0] = dup2(h ? __high2float(q[0]) : __low2float(q[0]));
+            dd[r][1] = dup2(h ? __high2float(q[1]) : __low2float(q[1]));
           }
           const uint8_t* bb = sb + (pc * C * 2 + h) * 512 + (h ? lsw1 : lsw0);
 #pragma unroll
           for (int cg = 0; cg < C; ++cg) {
             const uint4 bf = *reinterpret_cast<const uint4*>(bb + cg * 1024);
-            float d[4];
-            mma_bf16_first(d, a00, bf.x, bf.y);
-            mma_bf16_acc(d, a01, bf.z, bf.w);
-            if constexpr (PACKED) {
-              ffma2(acc[tt][0][cg][0], s00, d[0], d[1]);
-              ffma2(acc[tt][0][cg][1], s01, d[2], d[3]);
-            } else {
-              accf[tt][0][cg][0] = fmaf(f00, d[0], accf[tt][0][cg][0]);
-              accf[tt][0][cg][1] = fmaf(f00, d[1], accf[tt][0][cg][1]);
-              accf[tt][0][cg][2] = fmaf(f01, d[2], accf[tt][0][cg][2]);
-              accf[tt][0][cg][3] = fmaf(f01, d[3], accf[tt][0][cg][3]);
-            }
-            float e[4];
-            mma_bf16_first(e, a10, bf.x, bf.y);
-            mma_bf16_acc(e, a11, bf.z, bf.w);
-            if constexpr (PACKED) {
-              ffma2(acc[tt][1][cg][0], s10, e[0], e[1]);
-              ffma2(acc[tt][1][cg][1], s11, e[2], e[3]);
-            } else {
-              accf[tt][1][cg][0] = fmaf(f10, e[0], accf[tt][1][cg][0]);
-              accf[tt][1][cg][1] = fmaf(f10, e[1], accf[tt][1][cg][1]);
-              accf[tt][1][cg][2] = fmaf(f11, e[2], accf[tt][1][cg][2]);
-              accf[tt][1][cg][3] = fmaf(f11, e[3], accf[tt][1][cg][3]);
+#pragma unroll
+            for (int r = 0; r < NRG; ++r) {
+              float d[4];
+              mma_f16_first(d, af[r][0], bf.x, bf.y);
+              mma_f16_acc(d, af[r][1], bf.z, bf.w);
+              if (h == 0) {
+                pp[r][cg][0] = fmul2(dd[r][0], d[0], d[1]);
+                pp[r][cg][1] = fmul2(dd[r][1], d[2], d[3]);
+              } else {
+                ffma2(pp[r][cg][0], dd[r][0], d[0], d[1]);
+                ffma2(pp[r][cg][1], dd[r][1], d[2], d[3]);
+              }
             }
           }
         }
-        }
-        }
-        if ((RG || (R1 ? (i & 3) == 3 : (i & 1))) && c + NSLOT < nchunks) {  // this warp is done with the slot
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bempty[slot]));
+        // acc += P / s (rows R1 also / 16)
+#pragma unroll
+        for (int cg = 0; cg < C; ++cg) {
+          unsigned long long s0, s1;
+          asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(s0), "=l"(s1) : "r"(sig + cg * 64u) : "memory");
+#pragma unroll
+          for (int r = 0; r < NRG; ++r) {
+            ffma2p(acc[tt][r][cg][0], s0, pp[r][cg][0]);
+            ffma2p(acc[tt][r][cg][1], s1, pp[r][cg][1]);
+          }
         }
       }
+      if (!UP && (RG || (R1 ? (i & 3) == 3 : (i & 1))) && c + NSLOT < nchunks) {  // this warp is done with the slot
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bempty[slot]));
+      }
     }
-  compute_done:;
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy into the ring outlives the loop
-  } else {
+    // arrival number for the split-K epilogue (up-front conversion: drawn by
+    // the first compute warp at the end of its loop, so CTAs draw in about
+    // the order they finish)
+    if (UP && tid == 0 && a.e.splits > 1 && !a.cluster) s_arrival = split_arrive(&a.e.counters[blockIdx.x]);
+  } else if constexpr (!UP) {
     // ---- converter warps ----
     const int ct = tid - COMPUTE_THREADS;  // k = 4ct .. 4ct + 3 of each chunk
     const int pc = ct >> 4, h = (ct >> 3) & 1, j = (ct >> 1) & 3, tql = 2 * (ct & 1);
@@ -683,32 +793,50 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         s_err = 1;
         break;
       }
-      if (pair_ok) {
-        constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows read back together
+      constexpr int MG = MAXM < 4 ? MAXM : 4;  // rows read back together
 #pragma unroll
-        for (int m0 = 0; m0 < MAXM; m0 += MG) {
-          float4 v[MG];
+      for (int m0 = 0; m0 < MAXM; m0 += MG) {
+        if (m0 >= mrows) break;  // the same for every thread of the CTA
+        float4 v[MG];
+        uint32_t u[MG];
 #pragma unroll
-          for (int mm = 0; mm < MG; ++mm) {
-            v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (m0 + mm < mrows && k_ok && xoff[m0 + mm] >= 0)
-              v[mm] = *reinterpret_cast<const float4*>(xs + (m0 + mm) * (CHUNK_K * 4) + ct * 16);
-          }
+        for (int mm = 0; mm < MG; ++mm) {
+          v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (m0 + mm < mrows && k_ok && xoff[m0 + mm] >= 0)
+            v[mm] = *reinterpret_cast<const float4*>(xs + (m0 + mm) * (CHUNK_K * 4) + ct * 16);
+          // largest |x| of the four (as bits: non-negative floats order like integers)
+          u[mm] = __float_as_uint(fmaxf(fmaxf(fabsf(v[mm].x), fabsf(v[mm].y)), fmaxf(fabsf(v[mm].z), fabsf(v[mm].w))));
+        }
+        // the largest |x| per row over the warp's 128 elements (two block
+        // pairs), one warp-wide reduction per row
 #pragma unroll
-          for (int mm = 0; mm < MG; ++mm) {
-            const int m = m0 + mm;
-            if (m < mrows) {
-              uint32_t ta[3], tb[3];
-              split3(v[mm].x, v[mm].y, ta[0], ta[1], ta[2]);
-              split3(v[mm].z, v[mm].w, tb[0], tb[1], tb[2]);
+        for (int mm = 0; mm < MG; ++mm)
+          if (m0 + mm < mrows) asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u[mm]));
 #pragma unroll
-              for (int t = 0; t < 3; ++t) {
-                const int col = DENSE ? 3 * m + t : 8 * m + t;
-                const int cg = col >> 3, gl = col & 7;
-                uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
-                *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
-                *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
-              }
+        for (int mm = 0; mm < MG; ++mm) {
+          const int m = m0 + mm;
+          if (m >= mrows) break;
+          // s = 2^e with e = 14 - floor(log2 max|x|), kept within [-120, 120]:
+          // |x s| < 2^15 for every finite x
+          int e = 14 - ((int)(u[mm] >> 23) - 127);
+          e = max(-120, min(120, e));
+          const float s = __int_as_float((e + 127) << 23);
+          if (pair_ok) {
+            uint32_t ta[TERMS], tb[TERMS];
+            split4(v[mm], s, ta, tb);
+#pragma unroll
+            for (int t = 0; t < TERMS; ++t) {
+              const int col = TERMS * m + t;
+              const int cg = col >> 3, gl = col & 7;
+              uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
+              *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
+              *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
+            }
+            if ((ct & 15) == 0) {
+              // 1/s, and 1/(16 s) for rows R1 (exact powers of two)
+              const float r1 = __int_as_float((127 - e) << 23);
+              const float r16 = __int_as_float((123 - e) << 23);
+              *reinterpret_cast<float4*>(sb + S::SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
             }
           }
         }
@@ -747,15 +875,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           for (int cg = 0; cg < C; ++cg)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float v;
-              if constexpr (PACKED) {
-                const float2 pr = split2(acc[tt][r][cg][e >> 1]);
-                v = (e & 1) ? pr.y : pr.x;
-              } else {
-                v = accf[tt][r][cg][e];
-              }
+              const float2 pr = split2(acc[tt][r][cg][e >> 1]);
               red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * T2_LD + tt * TILE_N + (2 * rgp + r) * 16 + g +
-                  8 * (e >> 1)] = v;
+                  8 * (e >> 1)] = (e & 1) ? pr.y : pr.x;
             }
     }
     __syncthreads();
@@ -774,12 +896,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
           const int m = mfirst + k * MG;
           val[k] = 0.0f;
           if (m < mrows) {
-            const int c0 = DENSE ? 3 * m : 8 * m;
             float v = 0.0f;
 #pragma unroll
-            for (int t = 0; t < 3; ++t)
+            for (int t = 0; t < TERMS; ++t)
 #pragma unroll
-              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * T2_LD + tt * TILE_N + row];
+              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (TERMS * m + t) * T2_LD + tt * TILE_N + row];
             val[k] = v;
           }
         }
@@ -802,12 +923,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         const int64_t N = a.w[ww].N;
         if (n < N) {
           for (int m = tid >> 8; m < mrows; m += 2) {
-            const int c0 = DENSE ? 3 * m : 8 * m;
             float v = 0.0f;
 #pragma unroll
-            for (int t = 0; t < 3; ++t)
+            for (int t = 0; t < TERMS; ++t)
 #pragma unroll
-              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (c0 + t) * T2_LD + row];
+              for (int s = 0; s < SLICES; ++s) v += red[s * RS + (TERMS * m + t) * T2_LD + row];
             y[(int64_t)m * N + n] = v;
           }
         }
@@ -828,14 +948,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
         for (int cg = 0; cg < C; ++cg)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v;
-            if constexpr (PACKED) {
-              const float2 pr = split2(acc[0][r][cg][e >> 1]);
-              v = (e & 1) ? pr.y : pr.x;
-            } else {
-              v = accf[0][r][cg][e];
-            }
-            red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RG_LD + r * 16 + g + 8 * (e >> 1)] = v;
+            const float2 pr = split2(acc[0][r][cg][e >> 1]);
+            red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RG_LD + r * 16 + g + 8 * (e >> 1)] =
+                (e & 1) ? pr.y : pr.x;
           }
     }
     __syncthreads();
@@ -846,12 +961,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     float* y = a.w[wi].y;
     if (n < a.w[wi].N) {
       for (int m = tid >> 5; m < mrows; m += KERNEL_THREADS / 32) {
-        const int c0 = DENSE ? 3 * m : 8 * m;
         float v = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 3; ++t)
+        for (int t = 0; t < TERMS; ++t)
 #pragma unroll
-          for (int s = 0; s < NSL; ++s) v += red[s * RS + (c0 + t) * RG_LD + row];
+          for (int s = 0; s < NSL; ++s) v += red[s * RS + (TERMS * m + t) * RG_LD + row];
         y[(int64_t)m * a.w[wi].N + n] = v;
       }
     }
@@ -869,15 +983,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       for (int cg = 0; cg < C; ++cg)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float v;
-          if constexpr (PACKED) {
-            const float2 pr = split2(acc[0][r][cg][e >> 1]);
-            v = (e & 1) ? pr.y : pr.x;
-          } else {
-            v = accf[0][r][cg][e];
-          }
+          const float2 pr = split2(acc[0][r][cg][e >> 1]);
           red[sl * RS + (cg * 8 + 2 * tq + (e & 1)) * RED_LD + ((R1 ? (warp & 7) : 2 * rgp) + r) * 16 + g +
-              8 * (e >> 1)] = v;
+              8 * (e >> 1)] = (e & 1) ? pr.y : pr.x;
         }
   }
   __syncthreads();
@@ -895,12 +1003,11 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     const int m = mfirst + k * MGROUPS;
     val[k] = 0.0f;
     if (m < mrows) {
-      const int c0 = DENSE ? 3 * m : 8 * m;
       float v = 0.0f;
 #pragma unroll
-      for (int t = 0; t < 3; ++t)  // fixed order: term 0..2, each slice 0..3
+      for (int t = 0; t < TERMS; ++t)  // fixed order: term 0, 1, each slice 0..3
 #pragma unroll
-        for (int s = 0; s < S::NSL; ++s) v += red[s * RS + (c0 + t) * RED_LD + row];
+        for (int s = 0; s < S::NSL; ++s) v += red[s * RS + (TERMS * m + t) * RED_LD + row];
       val[k] = v;
     }
   }
@@ -956,7 +1063,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
 
 // Clusters of `size` CTAs of this kernel that the device holds at once (0 if
 // none or unknown), per device, cached.
-template <int C, bool DENSE>
+template <int C, bool UP>
 int cluster_capacity(int device, int size) {
   static std::atomic<int> cache[64][9];  // value + 1; 0 = not yet asked
   if (size < 2 || size > 8) return 0;
@@ -966,7 +1073,7 @@ int cluster_capacity(int device, int size) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
   cfg.blockDim = dim3(KERNEL_THREADS);
-  cfg.dynamicSmemBytes = MmaCfg<C, 1, DENSE>::BYTES;
+  cfg.dynamicSmemBytes = MmaCfg<C, 1, false, UP>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -975,7 +1082,7 @@ int cluster_capacity(int device, int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, DENSE, false, 1>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, false, 1, UP>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -983,11 +1090,11 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
-template <int C, bool DENSE, bool RG, int TPC = 1>
+template <int C, bool RG, int TPC = 1, bool UP = false>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
-  using S = MmaCfg<C, TPC, DENSE, RG>;
+  using S = MmaCfg<C, TPC, RG, UP>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
   int tiles = 0;
@@ -1031,7 +1138,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // different locks; setting the attribute twice is harmless)
   static std::atomic<bool> attr_set[64];
   if (!attr_set[W0->device & 63].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(mma_kernel<C, DENSE, RG, TPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, RG, TPC, UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63].store(true, std::memory_order_release);
@@ -1043,7 +1150,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
   a.cluster = !RG && TPC == 1 && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
-              tiles <= cluster_capacity<C, DENSE>(W0->device, plan.splits);
+              tiles <= cluster_capacity<C, UP>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
                    : dim3((unsigned)((tiles + TPC - 1) / TPC), (unsigned)plan.splits, 1);
@@ -1059,12 +1166,12 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C, DENSE, RG, TPC>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, RG, TPC, UP>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
-// Rows per launch: 16 with dense packing (6 column groups), 3 with one row
-// per column group (batch-invariant mode).
-int rows_per_launch(bool batch_invariant) { return batch_invariant ? MAX_CG : (MAX_CG_DENSE * 8) / 3; }
+// Rows per launch: 16 (four column groups of two terms per row), in both
+// modes.
+int rows_per_launch(bool) { return MAX_CG * 8 / TERMS; }
 
 }  // namespace
 
@@ -1124,10 +1231,19 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   // least 4 splits), K is short and the launch has at most 8 rows; the plan
   // depends on the shapes and that row count only (y output, default mode)
   // two tiles per CTA (whole K, no split): launches of more tiles than SMs
-  // run as CTAs that stream two tiles each, for one or two column groups in
-  // default mode (y output or the greedy pick)
+  // run as CTAs that stream two tiles each, for one or two column groups (up
+  // to 8 rows) in default mode (y output or the greedy pick)
   const bool two = Q4MM_TWO_TILES && !batch_invariant && plan.splits == 1 && plan.num_sms > 0 &&
                    tiles > plan.num_sms;
+  // up-front conversion when every CTA's K range is at most UP_CHUNKS chunks
+  // (row-group CTAs cover the whole K).  Measured on GB300 over the 7B layer
+  // (8 layer copies per graph, us per call, up-front / converter warps):
+  // q/k/v 4.79 / 5.68 at M = 1 and 7.68 / 9.76 at M = 8; down 17.13 / 18.90
+  // at M = 8.
+  const int64_t chunks_split = (plan.kbp_per_split + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
+  const int64_t chunks_all = (L.W[0]->KBP + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
+  const bool up_rg = Q4MM_UPFRONT && chunks_all <= UP_CHUNKS;
+  const bool up_split = Q4MM_UPFRONT && chunks_split <= UP_CHUNKS;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr, mrows);
@@ -1135,37 +1251,31 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
     const int32_t* xr = xrows ? xrows + mb : nullptr;
     int st;
     if (batch_invariant) {
-      switch (mrows) {
-        case 1: st = launch_c<1, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        case 2: st = launch_c<2, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        default: st = launch_c<3, false, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-      }
+      // one kernel for every row count: a row's operations and their order
+      // never depend on how many rows share its launch
+      st = launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     } else {
-      const int cgs = (3 * mrows + 7) / 8;  // column groups of this launch
-      if (cgs >= 4) {  // 9 to 16 rows: one row group per warp, K splits
-        switch (cgs) {
-          case 4: st = launch_c<4, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-          case 5: st = launch_c<5, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-          default: st = launch_c<6, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        }
+      const int cgs = (TERMS * mrows + 7) / 8;  // column groups of this launch
+      if (cgs >= 3) {  // 9 to 16 rows: one row group per warp, K splits
+        st = cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       } else if (rg) {
-        switch (cgs) {
-          case 1: st = launch_c<1, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-          case 2: st = launch_c<2, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-          default: st = launch_c<3, true, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        }
+        if (up_rg) st = cgs == 1 ? launch_c<1, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                                 : launch_c<2, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                           : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      } else if (two) {
+        // (two-tile CTAs keep the converter warps: with every chunk converted
+        // up front their accumulators spill; measured slower at 5-8 rows)
+        st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       } else {
-        switch (cgs) {
-          case 1:
-            st = two ? launch_c<1, true, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                     : launch_c<1, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-            break;
-          case 2:
-            st = two ? launch_c<2, true, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                     : launch_c<2, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-            break;
-          default: st = launch_c<3, true, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows); break;
-        }
+        if (up_split)
+          st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                        : launch_c<2, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        else
+          st = cgs == 1 ? launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                        : launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       }
     }
     if (st) return st;

@@ -68,8 +68,9 @@ def _load():
         lib.q4o_matmul_pairs.argtypes = [p, i64, i64, p, i64, p, i64, p, p, p]
         lib.q4o_argmax.argtypes = [p, i64, i64, p]
         lib.q4o_num_threads.argtypes = []
+        lib.q4o_set_threads.argtypes = [ctypes.c_int]
         for f in ("q4o_quantize", "q4o_dequantize", "q4o_matmul", "q4o_matmul_pairs",
-                  "q4o_argmax", "q4o_num_threads"):
+                  "q4o_argmax", "q4o_num_threads", "q4o_set_threads"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -162,3 +163,8 @@ def argmax(y: np.ndarray) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().q4o_num_threads())
+
+
+def set_threads(n: int) -> int:
+    """Use n threads in the oracle's loops from now on; returns the previous count."""
+    return int(_load().q4o_set_threads(int(n)))

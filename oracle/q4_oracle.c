@@ -283,6 +283,19 @@ int q4o_argmax(const float* y, int64_t M, int64_t N, int32_t* idx) {
   return Q4O_OK;
 }
 
+/* Threads the oracle's loops use from now on (n >= 1); returns the previous
+ * count.  Only the benchmark's single-core timing calls it. */
+int q4o_set_threads(int n) {
+#ifdef _OPENMP
+  const int prev = omp_get_max_threads();
+  if (n >= 1) omp_set_num_threads(n);
+  return prev;
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
 int q4o_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
