@@ -660,9 +660,6 @@ def extra_configs(q4, torch, dev, stack, stream, args, with_oracle):
         us = _graph_us(torch, stream, issue_gate, reps, Lg)
         gate[str(M)] = {"us": us, "weight_gbs": gb / us / 1e3, "frac_of_measured_hbm": gb / us / 1e3 / peak,
                         "token_rows_per_s": M / us * 1e6, "path": q4.q4mm_select_path(stack["gate_proj"][0], M)}
-        if M in (8, 16, 24, 32, 64):
-            gate[str(M)]["streaming_us"] = _graph_us(torch, stream, lambda: issue_gate(q4.Q4MM_FORCE_MMA), reps, Lg)
-            gate[str(M)]["tensor_core_us"] = _graph_us(torch, stream, lambda: issue_gate(q4.Q4MM_FORCE_TC), reps, Lg)
 
         def issue_stack():
             for l in range(Lg):
@@ -676,15 +673,26 @@ def extra_configs(q4, torch, dev, stack, stream, args, with_oracle):
         us = _graph_us(torch, stream, issue_stack, max(3, reps // 2), Lg)
         stk[str(M)] = {"us_per_layer": us, "weight_gbs": lb / us / 1e3, "frac_of_measured_hbm": lb / us / 1e3 / peak,
                        "token_rows_per_s": M / us * 1e6}
+    # both paths forced around the threshold, on gate_proj
+    paths = {}
+    for M in (8, 12, 16, 17, 20, 24, 32, 64):
+        xa = torch.from_numpy(synthetic.normal(synthetic.act_seed(6, M), (M, 3584))).to(dev)
+        yg = torch.empty((M, 18944), device=dev)
+
+        def issue_forced(fl):
+            for l in range(Lg):
+                q4.q4mm_forward_ex(stack["gate_proj"][l], xa, fl, y=yg, stream=stream)
+        paths[str(M)] = {"streaming_us": _graph_us(torch, stream, lambda: issue_forced(q4.Q4MM_FORCE_MMA), reps, Lg),
+                         "tensor_core_us": _graph_us(torch, stream, lambda: issue_forced(q4.Q4MM_FORCE_TC), reps, Lg)}
     cross = None
-    for M in (8, 16, 24, 32, 64):
-        g = gate[str(M)]
-        if g["tensor_core_us"] <= g["streaming_us"]:
+    for M in (8, 12, 16, 17, 20, 24, 32, 64):
+        if all(paths[str(m)]["tensor_core_us"] <= paths[str(m)]["streaming_us"]
+               for m in (8, 12, 16, 17, 20, 24, 32, 64) if m >= M):
             cross = M
             break
     out["c5_m_sweep"] = {"workload": "M sweep on gate_proj 18944x3584 (%d copies) and on the %d-layer stack "
                                      "(grouped q/k/v and gate/up calls)" % (Lg, Lg),
-                         "gate_proj": gate, "stack": stk,
+                         "gate_proj": gate, "stack": stk, "gate_proj_both_paths": paths,
                          "measured_crossover_gate": cross, "m_threshold": q4.q4mm_get_m_threshold(),
                          "group_m_threshold": q4.q4mm_get_group_m_threshold()}
     if with_oracle:

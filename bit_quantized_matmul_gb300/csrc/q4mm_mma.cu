@@ -120,9 +120,16 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 #define Q4MM_RG_NSLOT 4
 #endif
 // convert every chunk of a CTA's activations before its main loop (launches
-// of one or two column groups whose CTAs cover at most UP_CHUNKS chunks)
+// of one or two column groups whose CTAs cover at most UP_CHUNKS chunks);
+// for two-tile CTAs too, which then run without converter warps.  Measured
+// on GB300 (gate/up group of a 7B layer, us per call, up front / converter
+// warps): 14.79 / 15.64 at M = 1, 15.83 / 16.82 at M = 4, 22.73 / 23.76 at
+// M = 8
 #ifndef Q4MM_UPFRONT
 #define Q4MM_UPFRONT 1
+#endif
+#ifndef Q4MM_UP_TWO
+#define Q4MM_UP_TWO 1
 #endif
 #ifndef Q4MM_TWO_TILES
 #define Q4MM_TWO_TILES 1
@@ -203,6 +210,9 @@ struct MmaCfg {
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static_assert(!R1 || TPC == 1, "one row group per warp: one tile per CTA");
   static_assert(!UP || C <= 2, "up-front conversion: one or two column groups");
+  // threads: two-tile CTAs that convert up front need no converter warps
+  // (and get the register file of 512 threads: 128 registers each)
+  static constexpr int THREADS = (UP && TPC == 2) ? COMPUTE_THREADS : KERNEL_THREADS;
   static_assert(BYTES <= 227 * 1024 - 1024, "shared memory of one CTA");
   static_assert(SLOT % 16 == 0 && XSLOT % 16 == 0, "16-byte aligned ring slots");
 };
@@ -408,8 +418,9 @@ __device__ __forceinline__ void split4(const float4& v, float s, uint32_t (&ta)[
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
 template <int C, bool RG, int TPC, bool UP>
-__global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a) {
+__global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel(const MmaArgs a) {
   using S = MmaCfg<C, TPC, RG, UP>;
+  constexpr int NT = S::THREADS;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -513,7 +524,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   if (TERMS * mrows < 8 * C) {
     constexpr int PER_SLOT = S::SIG_OFF / 16;  // uint4 of B fragments per slot
     const int zslots = UP ? nchunks : NSLOT;
-    for (int j = tid; j < zslots * PER_SLOT; j += KERNEL_THREADS)
+    for (int j = tid; j < zslots * PER_SLOT; j += NT)
       *reinterpret_cast<uint4*>(smem + (j / PER_SLOT) * S::SLOT + (j % PER_SLOT) * 16) =
           make_uint4(0u, 0u, 0u, 0u);
   }
@@ -535,7 +546,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     // 128 threads per chunk (k = 4ct .. 4ct + 3), five chunk sets; every load
     // is issued before any is used
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
-    constexpr int CSETS = KERNEL_THREADS / 128;
+    constexpr int CSETS = NT / 128;
     constexpr int PER = (UP_CHUNKS + CSETS - 1) / CSETS;
     const int ct = tid & 127, cset = tid >> 7;
     const int pc = ct >> 4, h = (ct >> 3) & 1, j = (ct >> 1) & 3, tql = 2 * (ct & 1);
@@ -552,54 +563,67 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       return -1;
     };
     const float* xr = a.x + bp0 * 64 + 4 * ct;
-    float4 v[PER][MAXM];
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
+    // batches of (chunk, up to 4 rows); the next batch's loads are issued
+    // before the current one is converted
+    constexpr int MG = MAXM < 4 ? MAXM : 4;
+    constexpr int NB = PER * (MAXM / MG);
+    auto load_batch = [&](int b, float4 (&v)[MG]) {
+      const int q = b / (MAXM / MG), m0 = (b % (MAXM / MG)) * MG;
       const int c = cset + q * CSETS;
       const bool k_ok = c < nchunks && c * CHUNK_PAIRS + pc < npairs &&
                         (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
 #pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        v[q][m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (k_ok && m < mrows) {
-          const int64_t off = row_off(m);
-          if (off >= 0) v[q][m] = __ldg(reinterpret_cast<const float4*>(xr + off + (int64_t)c * CHUNK_K));
+      for (int mm = 0; mm < MG; ++mm) {
+        v[mm] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (k_ok && m0 + mm < mrows) {
+          const int64_t off = row_off(m0 + mm);
+          if (off >= 0) v[mm] = __ldg(reinterpret_cast<const float4*>(xr + off + (int64_t)c * CHUNK_K));
         }
       }
-    }
+    };
+    float4 vc[MG], vn[MG];
+    load_batch(0, vc);
 #pragma unroll
-    for (int q = 0; q < PER; ++q) {
+    for (int b = 0; b < NB; ++b) {
+      if (b + 1 < NB) load_batch(b + 1, vn);
+      const int q = b / (MAXM / MG), m0 = (b % (MAXM / MG)) * MG;
       const int c = cset + q * CSETS;
-      if (c >= nchunks) break;  // the same for the whole warp
-      uint8_t* sb = smem + c * S::SLOT;
-      const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
+      if (c < nchunks && m0 < mrows) {  // the same for the whole warp
+        uint8_t* sb = smem + c * S::SLOT;
+        const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
 #pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        if (m >= mrows) break;  // the same for every thread of the CTA
-        // largest |x| of row m over the warp's 128 elements (two block pairs)
-        uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(v[q][m].x), fabsf(v[q][m].y)),
-                                           fmaxf(fabsf(v[q][m].z), fabsf(v[q][m].w))));
-        asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u));
-        int e = 14 - ((int)(u >> 23) - 127);
-        e = max(-120, min(120, e));
-        const float sc = __int_as_float((e + 127) << 23);
-        if (pair_ok) {
-          uint32_t ta[TERMS], tb[TERMS];
-          split4(v[q][m], sc, ta, tb);
+        for (int mm = 0; mm < MG; ++mm) {
+          const int m = m0 + mm;
+          if (m >= mrows) break;  // the same for every thread of the CTA
+          // largest |x| of row m over the warp's 128 elements (two block pairs)
+          uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(vc[mm].x), fabsf(vc[mm].y)),
+                                             fmaxf(fabsf(vc[mm].z), fabsf(vc[mm].w))));
+          asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u));
+          int e = 14 - ((int)(u >> 23) - 127);
+          e = max(-120, min(120, e));
+          const float sc = __int_as_float((e + 127) << 23);
+          if (pair_ok) {
+            uint32_t ta[TERMS], tb[TERMS];
+            split4(vc[mm], sc, ta, tb);
 #pragma unroll
-          for (int t = 0; t < TERMS; ++t) {
-            const int col = TERMS * m + t;
-            const int cg = col >> 3, gl = col & 7;
-            uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
-            *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
-            *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
-          }
-          if ((ct & 15) == 0) {
-            const float r1 = __int_as_float((127 - e) << 23);
-            const float r16 = __int_as_float((123 - e) << 23);
-            *reinterpret_cast<float4*>(sb + S::SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
+            for (int t = 0; t < TERMS; ++t) {
+              const int col = TERMS * m + t;
+              const int cg = col >> 3, gl = col & 7;
+              uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
+              *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
+              *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
+            }
+            if ((ct & 15) == 0) {
+              const float r1 = __int_as_float((127 - e) << 23);
+              const float r16 = __int_as_float((123 - e) << 23);
+              *reinterpret_cast<float4*>(sb + S::SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
+            }
           }
         }
+      }
+      if (b + 1 < NB) {
+#pragma unroll
+        for (int mm = 0; mm < MG; ++mm) vc[mm] = vn[mm];
       }
     }
     __syncthreads();
@@ -884,7 +908,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     if (a.e.idx != nullptr) {
       // greedy pick: per tile, thread tid owns row tid % 128 for token rows
       // tid / 128 + 5k (as on the one-tile path), then the tile's maximum
-      constexpr int MG = KERNEL_THREADS / TILE_N;
+      constexpr int MG = NT / TILE_N;
       constexpr int MT = (MAXM + MG - 1) / MG;
       const int row = tid % TILE_N, mfirst = tid / TILE_N;
 #pragma unroll 1
@@ -960,7 +984,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
     const int64_t n = tile * TILE_N + rgp * 32 + row;
     float* y = a.w[wi].y;
     if (n < a.w[wi].N) {
-      for (int m = tid >> 5; m < mrows; m += KERNEL_THREADS / 32) {
+      for (int m = tid >> 5; m < mrows; m += NT / 32) {
         float v = 0.0f;
 #pragma unroll
         for (int t = 0; t < TERMS; ++t)
@@ -993,9 +1017,9 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
   // all threads take part from here: thread tid owns tile row tid % 128 for
   // the token rows tid / 128 + 5k, so the split-K reads of the last CTA are
   // spread over the whole CTA and issued in a single round
-  constexpr int MGROUPS = KERNEL_THREADS / TILE_N;
+  constexpr int MGROUPS = NT / TILE_N;
   constexpr int MT = (MAXM + MGROUPS - 1) / MGROUPS;
-  static_assert(KERNEL_THREADS % TILE_N == 0, "whole groups of tile rows");
+  static_assert(NT % TILE_N == 0, "whole groups of tile rows");
   const int row = tid % TILE_N, mfirst = tid / TILE_N;
   float val[MT];
 #pragma unroll
@@ -1034,7 +1058,7 @@ __global__ void __launch_bounds__(KERNEL_THREADS, 1) mma_kernel(const MmaArgs a)
       const int per = (outs + (int)nsplit - 1) / (int)nsplit;
       const int o_end = min(outs, (split + 1) * per);
       const uint32_t xa = smem_u32(xch);
-      for (int o = split * per + tid; o < o_end; o += KERNEL_THREADS) {
+      for (int o = split * per + tid; o < o_end; o += NT) {
         float t[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s)
@@ -1072,7 +1096,7 @@ int cluster_capacity(int device, int size) {
   if (c > 0) return c - 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
-  cfg.blockDim = dim3(KERNEL_THREADS);
+  cfg.blockDim = dim3(MmaCfg<C, 1, false, UP>::THREADS);
   cfg.dynamicSmemBytes = MmaCfg<C, 1, false, UP>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1154,7 +1178,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
                    : dim3((unsigned)((tiles + TPC - 1) / TPC), (unsigned)plan.splits, 1);
-  cfg.blockDim = dim3(KERNEL_THREADS);
+  cfg.blockDim = dim3(S::THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1244,6 +1268,7 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   const int64_t chunks_all = (L.W[0]->KBP + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
   const bool up_rg = Q4MM_UPFRONT && chunks_all <= UP_CHUNKS;
   const bool up_split = Q4MM_UPFRONT && chunks_split <= UP_CHUNKS;
+  const bool up_two = Q4MM_UPFRONT && chunks_all <= UP_CHUNKS;
   for (int64_t mb = 0; mb < M; mb += rpl) {
     const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
     const bool rg = mma_row_groups(plan, K, batch_invariant, idx != nullptr || xrows != nullptr, mrows);
@@ -1265,10 +1290,12 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
         else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
                            : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       } else if (two) {
-        // (two-tile CTAs keep the converter warps: with every chunk converted
-        // up front their accumulators spill; measured slower at 5-8 rows)
-        st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                      : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        if (Q4MM_UP_TWO && up_two)
+          st = cgs == 1 ? launch_c<1, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                        : launch_c<2, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        else
+          st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                        : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       } else {
         if (up_split)
           st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
