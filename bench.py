@@ -821,8 +821,32 @@ def run_path_sweep(args):
         if all(group_layer(m, "tc") <= group_layer(m, "mma") for m in sweep[i:]):
             gthr = M
             break
+    # The crossover of "Row-by-Row GEMV to the Rescue": one decoder layer (the
+    # seven linears as separate calls) at M = 1..8 under each path; ratio =
+    # throughput of a path / throughput of the tensor-core GEMM path (the
+    # pages' 134.3% / 109.2% / 90.7% at 3 / 4 / 5 requests compare their
+    # row-by-row GEMV with their GEMM the same way, on Metal).
+    cross = {}
+    pflags = {"row_by_row": q4.Q4MM_ROW_BY_ROW, "simt_single_launch": q4.Q4MM_FORCE_SIMT,
+              "mma_single_launch": q4.Q4MM_FORCE_MMA, "tensor_core_gemm": q4.Q4MM_FORCE_TC, "default": 0}
+    for M in range(1, 9):
+        xs = {K: torch.from_numpy(synthetic.normal(synthetic.act_seed(7, M) + K, (M, K))).to(dev)
+              for K in (3584, 18944)}
+        ys = {n: torch.empty((M, synthetic.QWEN7B_LINEARS[n][0]), device=dev) for n in TYPES}
+        rec = {}
+        for pname, fl in pflags.items():
+            def issue_layer():
+                for li in range(layers):
+                    for n in TYPES:
+                        K = synthetic.QWEN7B_LINEARS[n][1]
+                        q4.q4mm_forward_ex(stack[n][li], xs[K], fl, y=ys[n], stream=stream)
+            rec[pname + "_us_per_layer"] = _graph_us(torch, stream, issue_layer, 5, layers)
+        for pname in pflags:
+            rec[pname + "_vs_gemm"] = rec["tensor_core_gemm_us_per_layer"] / rec[pname + "_us_per_layer"]
+        cross[str(M)] = rec
     print(json.dumps({"path_sweep": out, "measured_threshold": thr, "groups": groups_out,
-                      "measured_group_threshold": gthr, "layers": layers, "sweep": list(sweep)}),
+                      "measured_group_threshold": gthr, "layers": layers, "sweep": list(sweep),
+                      "row_by_row_crossover": cross}),
           flush=True)
     for name in TYPES:
         for W in stack[name]:

@@ -46,7 +46,7 @@ BLOCK_BYTES = 18
 EXPORTS = (
     "q4_quantize", "q4_import_blocks", "q4_export_blocks", "q4_weight_free", "q4_weight_shape",
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
-    "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_argmax_rows", "q4_verify_greedy",
+    "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_forward_gated", "q4mm_argmax_rows", "q4_verify_greedy",
     "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4mm_set_group_m_threshold",
     "q4mm_get_group_m_threshold", "q4_device_status",
     "q4_status_string",
@@ -74,6 +74,7 @@ _sig = {
     "q4mm_argmax_ex": [_p, _p, _p, _p, _i64, _u32, _p],
     "q4mm_forward_noalloc": [_p, _p, _p, _i64, _p],
     "q4mm_forward_group": [_p, ctypes.c_int, _p, _p, _i64, _u32, _p],
+    "q4mm_forward_gated": [_p, _p, _p, _p, _i64, _u32, _p],
     "q4mm_argmax_rows": [_p, _p, _i64, _p, _i64, _p, _p, _p],
     "q4_verify_greedy": [_p, _p, _i64, _p, _i64, _p, _p],
     "q4_kv_append": [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(_i64),
@@ -280,6 +281,26 @@ def q4mm_forward_group(Ws, x: torch.Tensor, ys=None, flags: int = 0, stream=None
         _check(_lib.q4mm_forward_group(hw, len(Ws), x.data_ptr(), hy, M, int(flags), _stream(stream)),
                "q4mm_forward_group")
     return ys
+
+
+def q4mm_forward_gated(Wg: Q4Weight, Wu: Q4Weight, x: torch.Tensor, h: torch.Tensor | None = None,
+                       flags: int = 0, stream=None) -> torch.Tensor:
+    """h = SiLU(x @ Wg^T) * (x @ Wu^T) (the gated MLP step; q4mm_forward_gated)."""
+    _dev_f32(x, "x")
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != Wg.K:
+        raise ValueError("x must be [M, %d]" % Wg.K)
+    if (Wu.N, Wu.K) != (Wg.N, Wg.K):
+        raise ValueError("gate and up projections must have one shape")
+    if h is None:
+        h = torch.empty((M, Wg.N), dtype=torch.float32, device=x.device)
+    _dev_f32(h, "h")
+    if tuple(h.shape) != (M, Wg.N):
+        raise ValueError("h must be [M, %d]" % Wg.N)
+    with torch.cuda.device(x.device):
+        _check(_lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr(), h.data_ptr(), M, int(flags),
+                                       _stream(stream)), "q4mm_forward_gated")
+    return h
 
 
 def q4mm_argmax_rows(W: Q4Weight, x: torch.Tensor, rows: torch.Tensor, want_max: bool = True,

@@ -190,8 +190,19 @@ int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxv
 }  // namespace
 
 // Caller holds g_dev[device].mu.
-int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* out) {
+int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* out, size_t gu_bytes) {
   DeviceScratch& ds = g_dev[device];
+  if (gu_bytes > ds.ws.gu_bytes) {
+    size_t want = gu_bytes + gu_bytes / 2;
+    if (ds.ws.gu) cudaFree(ds.ws.gu);
+    ds.ws.gu = nullptr;
+    ds.ws.gu_bytes = 0;
+    if (cudaMalloc(&ds.ws.gu, want) != cudaSuccess) {
+      cudaGetLastError();
+      return Q4_ERR_NOMEM;
+    }
+    ds.ws.gu_bytes = want;
+  }
   if (partial_bytes > ds.ws.partial_bytes) {
     size_t want = partial_bytes + partial_bytes / 2;
     if (ds.ws.partial) cudaFree(ds.ws.partial);  // cudaFree waits for work in flight
@@ -419,6 +430,60 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
     if (st) return st;
     return launch_tc_group(L, x, M, nullptr, nullptr, plan, ws, stream);
   }
+}
+
+int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x, float* h, int64_t M,
+                       uint32_t flags, cudaStream_t stream) {
+  if (!Wg || !Wu || !x || !h) return Q4_ERR_INVALID_ARG;
+  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA)) return Q4_ERR_INVALID_ARG;
+  if (Wg->w.N != Wu->w.N || Wg->w.K != Wu->w.K || Wg->w.device != Wu->w.device) return Q4_ERR_INVALID_ARG;
+  if (M < 0) return Q4_ERR_INVALID_ARG;
+  if (M > Q4MM_M_MAX) return Q4_ERR_SHAPE;
+  if (M == 0) return Q4_OK;
+  if (!aligned16(x) || !aligned16(h)) return Q4_ERR_ALIGN;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  if (dev != Wg->w.device) return Q4_ERR_INVALID_ARG;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  st = init_device_locked(dev, ds);
+  if (st) return st;
+  const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
+  const bool streaming = (flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 || !tc_supported(ds) ||
+                         M < g_group_m_threshold.load();
+  Workspace ws;
+  if (streaming && !inv) {
+    // fused: the gate and up tiles of a row range in one CTA, h written directly
+    st = workspace_get(dev, 0, 0, &ws);
+    if (st) return st;
+    return launch_mma_gated(&Wg->w, &Wu->w, x, M, h, ws, stream);
+  }
+  // grouped call into scratch, then the elementwise step
+  const size_t out_bytes = (size_t)M * (size_t)Wg->w.N * sizeof(float);
+  MmaLaunch L;
+  L.count = 2;
+  L.W[0] = &Wg->w;
+  L.W[1] = &Wu->w;
+  const int64_t tiles = Wg->w.tiles + Wu->w.tiles;
+  if (streaming) {
+    const MmaPlan plan = mma_plan_tiles(tiles, Wg->w.KBP, ds.num_sms);
+    st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws, 2 * out_bytes);
+    if (st) return st;
+    L.y[0] = ws.gu;
+    L.y[1] = ws.gu + M * Wg->w.N;
+    st = launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
+  } else {
+    const TcPlan plan = tc_plan_tiles(tiles, Wg->w.KBP, M, ds.num_sms, false);
+    st = workspace_get(dev, tc_partial_bytes_tiles(tiles, plan, M), tc_xop_bytes_kbp(Wg->w.KBP, plan, M), &ws,
+                       2 * out_bytes);
+    if (st) return st;
+    L.y[0] = ws.gu;
+    L.y[1] = ws.gu + M * Wg->w.N;
+    st = launch_tc_group(L, x, M, nullptr, nullptr, plan, ws, stream);
+  }
+  if (st) return st;
+  return launch_silu_mul(ws.gu, ws.gu + M * Wg->w.N, h, M * Wg->w.N, stream);
 }
 
 int q4mm_argmax_rows(const q4_weight* Wh, const float* x, int64_t x_rows, const int32_t* rows,

@@ -71,6 +71,8 @@ struct Workspace {
   size_t partial_bytes = 0;
   void* xop = nullptr;                 // tensor-core activation operand
   size_t xop_bytes = 0;
+  float* gu = nullptr;                 // gate and up outputs of an unfused gated call
+  size_t gu_bytes = 0;
 };
 constexpr int MAX_COUNTERS = 1 << 16;
 
@@ -80,7 +82,7 @@ constexpr unsigned STATUS_BAD_ROW = 2u;   // a row index of q4mm_argmax_rows was
 constexpr unsigned STATUS_KV_RANGE = 4u;  // a q4_kv_append request was out of range (not written)
 
 // Returns Q4_OK and fills *ws with at least the requested capacities.
-int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws);
+int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws, size_t gu_bytes = 0);
 
 // ---- launchers (return a Q4 status; launch errors map to Q4_ERR_CUDA) ----
 // Quantize fp32 W (device) into canonical blocks in canon_dev, then repack.
@@ -105,6 +107,7 @@ struct MmaLaunch {
   int count = 0;
   const Weight* W[MMA_GROUP_MAX] = {};
   float* y[MMA_GROUP_MAX] = {};
+  bool gated = false;  // W[0], W[1] = gate, up: y[0] = SiLU(x W0^T) * (x W1^T)
 };
 MmaPlan mma_plan(const Weight* W, int num_sms);
 // True when a launch of `launch_rows` token rows with this plan uses row-group
@@ -123,6 +126,14 @@ int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* id
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
                      const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s,
                      const int32_t* xrows = nullptr, int64_t x_rows = 0);
+
+// h = SiLU(x Wg^T) * (x Wu^T) on the streaming kernel: two-tile CTAs that
+// pair tile b of Wg with tile b of Wu over the whole K, up to 8 token rows per
+// launch (Wg and Wu of one shape).
+int launch_mma_gated(const Weight* Wg, const Weight* Wu, const float* x, int64_t M, float* h,
+                     const Workspace& ws, cudaStream_t s);
+// h[i] = SiLU(g[i]) * u[i] for i < n (the gated step after a grouped call).
+int launch_silu_mul(const float* g, const float* u, float* h, int64_t n, cudaStream_t s);
 
 // KV-cache append of one step (see q4_kv_append); sizes in elements except
 // row_bytes and the source strides (bytes: K layer, token, head, then V's).

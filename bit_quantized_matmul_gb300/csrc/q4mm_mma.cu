@@ -112,6 +112,10 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 #endif
 // row-group CTAs (one 32-row group pair over the whole K, no K split) for
 // launches whose tiles x 4 fit on the SMs and whose K is at most this
+// row-group CTAs for launches of at most this many token rows
+#ifndef Q4MM_RG_MAX_ROWS
+#define Q4MM_RG_MAX_ROWS 8
+#endif
 #ifndef Q4MM_RG_MAX_K
 #define Q4MM_RG_MAX_K 4096
 #endif
@@ -162,6 +166,10 @@ struct MmaArgs {
   int64_t K, KBP;       // K, block pairs
   int mrows;            // token rows in this launch
   int64_t kbp_per_split;
+  // 0, or the tile count of the first weight when two-tile CTAs pair tile b
+  // of weight 0 with tile b of weight 1 and write h = SiLU(y0) * y1 into
+  // weight 0's output (gate and up projections of a gated MLP)
+  int gated;
   unsigned int* status; // device status word (bounded-wait expiry)
   int cluster;          // 1: the K splits of a tile are one thread-block cluster
   EpiArgs e;
@@ -438,19 +446,22 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
   // four column groups)
   // TPC = 2: the CTA takes global tiles 2 blockIdx.x and 2 blockIdx.x + 1 (the
   // second when it exists) over the whole K; its warps cover the same row
-  // groups of both, and the converted activations serve both
-  const int gtile = RG ? (int)(blockIdx.x >> 2) : (int)blockIdx.x * TPC;
+  // groups of both, and the converted activations serve both.  Gated
+  // launches pair tile blockIdx.x of the gate weight with the same tile of
+  // the up weight instead.
+  const int gtile = RG ? (int)(blockIdx.x >> 2) : (a.gated ? (int)blockIdx.x : (int)blockIdx.x * TPC);
+  const int gtile_b = a.gated ? (int)blockIdx.x + a.gated : gtile + 1;  // the second tile
   int wi = 0;
 #pragma unroll
   for (int i = 1; i < MMA_GROUP_MAX; ++i)
     if (i < a.nweights && gtile >= a.w[i].tile_start) wi = i;
   const int64_t tile = (int64_t)gtile - a.w[wi].tile_start;  // tile within its weight
-  const bool has1 = TPC == 2 && (int64_t)gtile + 1 < a.e.N_pad / TILE_N;  // second tile
+  const bool has1 = TPC == 2 && (int64_t)gtile_b < a.e.N_pad / TILE_N;  // second tile
   int wi1 = wi;
 #pragma unroll
   for (int i = 1; i < MMA_GROUP_MAX; ++i)
-    if (i < a.nweights && gtile + 1 >= a.w[i].tile_start) wi1 = i;
-  const int64_t tile1 = (int64_t)gtile + 1 - a.w[wi1].tile_start;
+    if (i < a.nweights && gtile_b >= a.w[i].tile_start) wi1 = i;
+  const int64_t tile1 = (int64_t)gtile_b - a.w[wi1].tile_start;
   const uint4* nib_w = a.w[wi].nib;
   const uint8_t* scl_w = a.w[wi].scl;
   const int split = blockIdx.y;
@@ -935,6 +946,32 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
       }
       return;
     }
+    if (a.gated) {
+      // h = SiLU(g) * u for the tile's 128 rows: thread t < 512 takes row
+      // t % 128 and token rows t / 128 + 4k; g and u are added up in the
+      // same order as on the ungated path, so they carry the same bits
+      if (tid < 4 * TILE_N) {
+        const int row = tid & (TILE_N - 1);
+        const int64_t n = tile * TILE_N + row;
+        float* h = a.w[0].y;
+        const int64_t N = a.w[0].N;
+        if (n < N) {
+          for (int m = tid >> 7; m < mrows; m += 4) {
+            float g = 0.0f, u = 0.0f;
+#pragma unroll
+            for (int t = 0; t < TERMS; ++t)
+#pragma unroll
+              for (int s = 0; s < SLICES; ++s) g += red[s * RS + (TERMS * m + t) * T2_LD + row];
+#pragma unroll
+            for (int t = 0; t < TERMS; ++t)
+#pragma unroll
+              for (int s = 0; s < SLICES; ++s) u += red[s * RS + (TERMS * m + t) * T2_LD + TILE_N + row];
+            h[(int64_t)m * N + n] = g / (1.0f + expf(-g)) * u;
+          }
+        }
+      }
+      return;
+    }
     // thread t < 512: row t % 256 of the two tiles, token rows t / 256 + 2k;
     // fixed order of terms and slices, as on the other paths
     if (tid < 2 * 2 * TILE_N) {
@@ -1144,6 +1181,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.KBP = W0->KBP;
   a.mrows = mrows;
   a.kbp_per_split = RG ? W0->KBP : plan.kbp_per_split;
+  a.gated = L.gated ? (int)L.W[0]->tiles : 0;
   a.status = ws.status;
   a.e.N = W0->N;
   a.e.N_pad = (int64_t)tiles * TILE_N;
@@ -1177,7 +1215,8 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
               tiles <= cluster_capacity<C, UP>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
-                   : dim3((unsigned)((tiles + TPC - 1) / TPC), (unsigned)plan.splits, 1);
+                   : L.gated ? dim3((unsigned)L.W[0]->tiles, 1, 1)
+                             : dim3((unsigned)((tiles + TPC - 1) / TPC), (unsigned)plan.splits, 1);
   cfg.blockDim = dim3(S::THREADS);
   cfg.dynamicSmemBytes = S::BYTES;
   cfg.stream = s;
@@ -1238,7 +1277,7 @@ int mma_launch_count(int64_t M, bool batch_invariant) {
 
 bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick,
                     int64_t launch_rows) {
-  return !batch_invariant && !greedy_pick && launch_rows <= 8 && plan.splits >= 4 &&
+  return !batch_invariant && !greedy_pick && launch_rows <= Q4MM_RG_MAX_ROWS && plan.splits >= 4 &&
          K <= Q4MM_RG_MAX_K;
 }
 
@@ -1305,6 +1344,31 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
                         : launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
       }
     }
+    if (st) return st;
+  }
+  return Q4_OK;
+}
+
+int launch_mma_gated(const Weight* Wg, const Weight* Wu, const float* x, int64_t M, float* h,
+                     const Workspace& ws, cudaStream_t s) {
+  // two-tile CTAs over the pair (gate tile b, up tile b), whole K, up to 8
+  // token rows per launch
+  MmaLaunch L;
+  L.count = 2;
+  L.W[0] = Wg;
+  L.W[1] = Wu;
+  L.y[0] = h;
+  L.y[1] = nullptr;
+  L.gated = true;
+  MmaPlan plan;
+  plan.splits = 1;
+  plan.kbp_per_split = Wg->KBP;
+  plan.num_sms = 0;
+  for (int64_t mb = 0; mb < M; mb += 8) {
+    const int mrows = (int)((M - mb) < 8 ? (M - mb) : 8);
+    const float* xs = x + mb * Wg->K;
+    const int st = mrows <= 4 ? launch_c<1, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0)
+                              : launch_c<2, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0);
     if (st) return st;
   }
   return Q4_OK;

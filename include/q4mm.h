@@ -178,6 +178,29 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
 Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
                               int64_t M, uint32_t flags, cudaStream_t stream);
 
+/* The hidden state of a gated MLP in one call:
+ *   h[M,N] = SiLU(x Wg^T) * (x Wu^T),  SiLU(z) = z / (1 + exp(-z)),
+ * with Wg, Wu the gate and up projections (same N and K, same device) and x
+ * fp32 [M,K] as for q4mm_forward; h fp32 [M,N] row-major, device, 16-byte
+ * aligned, caller-owned, fully overwritten.  The pages name the gate/up/down
+ * projections of Qwen2.5-7B but not the step between them; this is that
+ * model's gated MLP.  Fusing it into the matmul follows "Why LLM Decoding Is
+ * Slow, and Why Batching Is (Almost) Free" (§3 "The Real Constraint: Two
+ * Ceilings": small elementwise ops around the matmuls cost time of their
+ * own): on the streaming path (M below the group M threshold) each CTA
+ * computes the gate and up rows of the same row range and writes only h; g
+ * and u never reach memory.  On the tensor-core path and in batch-invariant
+ * mode the grouped call writes g and u to library scratch and one elementwise
+ * pass forms h.
+ *   flags   0, Q4MM_FORCE_MMA or Q4MM_BATCH_INVARIANT (others: INVALID_ARG).
+ * Each element is within the gate and up tolerances propagated through SiLU
+ * (SiLU is 1.1-Lipschitz) plus fp32 rounding; in batch-invariant mode row r
+ * of h is bit-identical whatever M is.  The streaming path takes up to 8
+ * token rows per launch.  Errors as for q4mm_forward_group; mismatched shapes
+ * or devices: INVALID_ARG. */
+Q4_API int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x, float* h,
+                              int64_t M, uint32_t flags, cudaStream_t stream);
+
 /* Capacity of the split-K partial sums of q4mm_forward_noalloc (2400 KiB). */
 #define Q4MM_NOALLOC_PARTIAL_BYTES 2457600
 

@@ -55,7 +55,7 @@ def test_streaming_split_exchange_matches_oracle(q4, N, KK, splits):
     _, _, s = q4.q4mm_plan_info(W, 1, q4.Q4MM_FORCE_MMA)
     if _sms() == 152:
         assert s == splits
-    for M in (1, 3, 8, 11):  # one, two and three column groups; two launches
+    for M in (1, 3, 8, 11):  # one, one, two and three column groups
         x = acts(70, M, KK, salt=N)
         y = q4.q4mm_forward_ex(W, torch.from_numpy(x).to(DEV), q4.Q4MM_FORCE_MMA).cpu().numpy()
         _, y64, bound = oracle.matmul(blocks, x)
@@ -92,7 +92,7 @@ def test_streaming_cluster_greedy_pick_matches_oracle(q4):
     idx = idx.cpu().numpy()
     for m in range(M):
         order = np.argsort(-y64[m], kind="stable")
-        if y64[m, order[0]] - y64[m, order[1]] > 2 * bound[m].max():
+        if y64[m, order[0]] - y64[m, order[1]] > bound[m, order[0]]:
             assert idx[m] == order[0], m
         assert abs(float(mx.cpu().numpy()[m]) - y64[m, idx[m]]) <= bound[m, idx[m]]
     W.free()
@@ -195,7 +195,8 @@ def test_two_tile_ctas_greedy_pick_matches_oracle(q4):
             margin = y64[m, top[0]] - y64[m, top[1]]
             if m in planted:
                 assert margin > bound[m, top[0]] + bound[m, top[1]], "planted gap below the bound"
-            if margin > bound[m, top[0]] + bound[m, top[1]]:
+            # exact wherever the oracle's top-2 margin exceeds the bound at the top index
+            if margin > bound[m, top[0]]:
                 assert idx[m] == top[0], (M, m)
             assert abs(float(mx[m]) - y64[m, idx[m]]) <= bound[m, idx[m]]
         # the same sums as the call that writes y (both on two-tile CTAs)
@@ -211,7 +212,7 @@ SIXTEEN_ROW_CASES = [(4000, 4608), (3584, 3584), (155 * 128 - 37, 1024), (300, 1
 
 @pytest.mark.parametrize("N,KK", SIXTEEN_ROW_CASES)
 def test_sixteen_row_launches_match_oracle(q4, N, KK):
-    # 9 to 16 token rows in one streaming launch (four to six column groups,
+    # 9 to 16 token rows in one streaming launch (three or four column groups,
     # one row group per warp, two K slices per CTA) over each exchange on a
     # 152-SM device: clusters (32 tiles x 4 splits), flagged global words
     # (28 tiles x 5 splits; a ragged 3-tile weight x 8) and one K split (155

@@ -213,7 +213,8 @@ def test_argmax_matches_oracle(q4, mode):
         for m in range(M):
             top = np.argsort(-y64[m], kind="stable")
             margin = y64[m, top[0]] - y64[m, top[1]]
-            if margin > bound[m, top[0]] + bound[m, top[1]]:
+            # exact wherever the oracle's top-2 margin exceeds the bound at the top index
+            if margin > bound[m, top[0]]:
                 assert idx[m] == ref[m], (mode, M, m, planted.get(m))
             else:
                 assert y64[m, ref[m]] - y64[m, idx[m]] <= bound[m, ref[m]] + bound[m, idx[m]]
