@@ -293,8 +293,26 @@ def run_gpu(args):
                 issue(M, gname)
     torch.cuda.synchronize(dev)
 
+    def issue_stack(M):
+        # the whole stack in layer order: q/k/v, o, gate/up, down of layer 0, then layer 1, ...
+        for layer in range(layers):
+            for gname, names in groups:
+                K = synthetic.QWEN7B_LINEARS[names[0]][1]
+                x = xs[(M, K)]
+                if len(names) == 1:
+                    q4.q4mm_forward_ex(stack[names[0]][layer], x, flags, y=ys[(M, names[0])], stream=stream)
+                else:
+                    q4.q4mm_forward_group([stack[n][layer] for n in names], x,
+                                          ys=[ys[(M, n)] for n in names], flags=flags, stream=stream)
+
+    # one CUDA graph per M holds the whole stack; per-call graphs (the
+    # `layers` calls of one kind) give the per-call breakdown
     graphs = {}
     for M in msw:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            issue_stack(M)
+        graphs[M] = g
         for gname, _ in groups:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -329,15 +347,14 @@ def run_gpu(args):
 
     def step(record):
         for M in msw:
-            for gname, _ in groups:
-                if record:
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    graphs[(M, gname)].replay()
-                    b.record(stream)
-                    ev.setdefault((M, gname), []).append((a, b))
-                else:
-                    graphs[(M, gname)].replay()
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graphs[M].replay()
+                b.record(stream)
+                ev.setdefault(M, []).append((a, b))
+            else:
+                graphs[M].replay()
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -363,16 +380,29 @@ def run_gpu(args):
     ms_per_step = ms / args.steps
     value = whole_job_gbs(step_wbytes, world, ms_per_step)
 
-    # per-(M, call) durations over the timed region: each graph replay is the
-    # `layers` calls of one kind, bracketed by events on the launching stream
+    # per-M durations over the timed region: each graph replay is the whole
+    # stack at one M, bracketed by events on the launching stream
+    per_stack = {M: sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) for M, pairs in ev.items()}  # ms
+    # per-call breakdown (outside the timed region): the per-kind graphs
     per = {}
-    for key, pairs in ev.items():
-        per[key] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) / layers  # ms per call
+    with torch.cuda.stream(stream):
+        for M in msw:
+            for gname, _ in groups:
+                graphs[(M, gname)].replay()
+                times = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    graphs[(M, gname)].replay()
+                    b.record(stream)
+                    b.synchronize()
+                    times.append(a.elapsed_time(b))
+                per[(M, gname)] = statistics.median(times) / layers  # ms per call
     peak, peak_kind = _peaks()
     # roofline over every launch of the step (one kernel function serves them all):
-    # algorithmic bytes per call / event-timed duration per call
-    tot_bytes = sum(algo_bytes(M, g) for M in msw for g, _ in groups)
-    tot_ms = sum(per[(M, g)] for M in msw for g, _ in groups)
+    # algorithmic bytes of all calls / event-timed duration of the stack graphs
+    tot_bytes = sum(algo_bytes(M, g) for M in msw for g, _ in groups) * layers
+    tot_ms = sum(per_stack[M] for M in msw)
     n_launch = sum(launches[(M, g)] for M in msw for g, _ in groups)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     traffic = None
@@ -382,7 +412,7 @@ def run_gpu(args):
         traffic = TRAFFIC.get("bytes_per_launch")
     per_m = {}
     for M in msw:
-        t = sum(per[(M, g)] * layers for g, _ in groups)
+        t = per_stack[M]
         b = sum(wbytes[n] * layers for n in TYPES)
         per_m[str(M)] = {
             "weight_gbs": b / (t * 1e-3) / 1e9,
@@ -420,6 +450,8 @@ def run_gpu(args):
                              % (sum(wbytes[n] * layers for n in TYPES) / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "calls_per_layer": [g for g, _ in groups],
+                       "graphs": "one CUDA graph per M holding the whole stack in layer order (programmatic "
+                                 "dependent launch between consecutive calls); call_us from per-kind graphs",
                        "mode": "batch-invariant" if args.batch_invariant else "default",
                        "m_threshold": q4.q4mm_get_m_threshold(),
                        "group_m_threshold": q4.q4mm_get_group_m_threshold()},
@@ -431,7 +463,7 @@ def run_gpu(args):
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "kernel": "q4mm kernels (mma_kernel below the M threshold, xop_kernel + tc_kernel "
                                    "from it), every launch of one step (%d launches)" % (n_launch * layers),
-                         "algorithmic_bytes_per_launch": tot_bytes / n_launch,
+                         "algorithmic_bytes_per_launch": tot_bytes / (n_launch * layers),
                          "algorithmic_bytes_rule": "0.5625*sum(N_i*K) + 4*M*K + 4*M*sum(N_i) per call"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms_per_step"],
@@ -695,6 +727,41 @@ def extra_configs(q4, torch, dev, stack, stream, args, with_oracle):
                          "gate_proj": gate, "stack": stk, "gate_proj_both_paths": paths,
                          "measured_crossover_gate": cross, "m_threshold": q4.q4mm_get_m_threshold(),
                          "group_m_threshold": q4.q4mm_get_group_m_threshold()}
+    # ---- the decoder layer with the gated step fused (gate/up -> h -> down), the
+    # whole stack in one graph, against the seven linears with g and u written
+    Lf = len(stack["gate_proj"])
+    fused = {}
+    for M in (1, 4, 8):
+        xa = torch.from_numpy(synthetic.normal(synthetic.act_seed(8, M), (M, 3584))).to(dev)
+        xb = torch.from_numpy(synthetic.normal(synthetic.act_seed(8, M) + 1, (M, 18944))).to(dev)
+        ys = {n: torch.empty((M, synthetic.QWEN7B_LINEARS[n][0]), device=dev) for n in TYPES}
+        h = torch.empty((M, 18944), device=dev)
+
+        def issue_fused():
+            for l in range(Lf):
+                q4.q4mm_forward_group([stack[n][l] for n in ("q_proj", "k_proj", "v_proj")], xa,
+                                      ys=[ys[n] for n in ("q_proj", "k_proj", "v_proj")], stream=stream)
+                q4.q4mm_forward(stack["o_proj"][l], xa, y=ys["o_proj"], stream=stream)
+                q4.q4mm_forward_gated(stack["gate_proj"][l], stack["up_proj"][l], xa, h=h, stream=stream)
+                q4.q4mm_forward(stack["down_proj"][l], h, y=ys["down_proj"], stream=stream)
+
+        def issue_plain():
+            for l in range(Lf):
+                q4.q4mm_forward_group([stack[n][l] for n in ("q_proj", "k_proj", "v_proj")], xa,
+                                      ys=[ys[n] for n in ("q_proj", "k_proj", "v_proj")], stream=stream)
+                q4.q4mm_forward(stack["o_proj"][l], xa, y=ys["o_proj"], stream=stream)
+                q4.q4mm_forward_group([stack["gate_proj"][l], stack["up_proj"][l]], xa,
+                                      ys=[ys["gate_proj"], ys["up_proj"]], stream=stream)
+                q4.q4mm_forward(stack["down_proj"][l], xb, y=ys["down_proj"], stream=stream)
+        uf = _graph_us(torch, stream, issue_fused, max(3, reps // 2), Lf)
+        up = _graph_us(torch, stream, issue_plain, max(3, reps // 2), Lf)
+        fused[str(M)] = {"fused_us_per_layer": uf, "seven_linears_us_per_layer": up,
+                         "fused_weight_gbs": lb / uf / 1e3, "fused_frac_of_measured_hbm": lb / uf / 1e3 / peak,
+                         "output_bytes_saved_per_layer": 4 * M * 18944}
+    out["next2_fused_gated_layer"] = {"workload": "the %d-layer 7B stack in one CUDA graph per M, each layer q/k/v "
+                                                  "(grouped), o, q4mm_forward_gated (gate, up -> h = SiLU(g)*u, "
+                                                  "only h written), down(h); against the same layer with gate/up "
+                                                  "as a grouped call writing g and u" % Lf, "per_M": fused}
     if with_oracle:
         out["oracle_single_core"] = _oracle_single_core()
     return out
