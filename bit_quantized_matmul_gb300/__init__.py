@@ -48,7 +48,7 @@ EXPORTS = (
     "q4_weight_device_bytes", "q4mm_forward", "q4mm_forward_ex", "q4mm_argmax", "q4mm_argmax_ex",
     "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_forward_gated", "q4mm_argmax_rows", "q4_verify_greedy",
     "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4mm_set_group_m_threshold",
-    "q4mm_get_group_m_threshold", "q4_device_status",
+    "q4mm_get_group_m_threshold", "q4_device_status", "q4mm_set_wait_limit_ns", "q4mm_set_stall_for_test",
     "q4_status_string",
     "q4_kv_append",
 )
@@ -87,6 +87,8 @@ _sig = {
     "q4mm_set_group_m_threshold": [_i64],
     "q4mm_get_group_m_threshold": [],
     "q4_device_status": [],
+    "q4mm_set_wait_limit_ns": [ctypes.c_uint64],
+    "q4mm_set_stall_for_test": [ctypes.c_int],
     "q4_status_string": [ctypes.c_int],
 }
 for _name, _args in _sig.items():
@@ -430,6 +432,16 @@ def q4mm_set_group_m_threshold(m: int):
 
 def q4mm_get_group_m_threshold() -> int:
     return int(_lib.q4mm_get_group_m_threshold())
+
+
+def q4mm_set_wait_limit_ns(ns: int):
+    """Bound of the kernels' waits in ns for later launches (0: the default, 1 s)."""
+    _check(_lib.q4mm_set_wait_limit_ns(int(ns)), "q4mm_set_wait_limit_ns")
+
+
+def q4mm_set_stall_for_test(on: bool):
+    """Test setting: later launches withhold their first hand-off so that waits run out."""
+    _check(_lib.q4mm_set_stall_for_test(1 if on else 0), "q4mm_set_stall_for_test")
 
 
 def q4_device_status() -> int:

@@ -54,6 +54,11 @@ std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 17;
 std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
+// Test settings (q4mm_set_wait_limit_ns, q4mm_set_stall_for_test).
+constexpr unsigned long long DEFAULT_WAIT_NS = 1000000000ull;  // 1 s
+std::atomic<unsigned long long> g_wait_ns{DEFAULT_WAIT_NS};
+std::atomic<int> g_stall{0};
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int init_device_locked(int dev, DeviceScratch& ds) {
@@ -233,6 +238,14 @@ int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace*
 }
 
 int device_num_sms(int device) { return g_dev[device].num_sms; }
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
+// one round of re-reads of a batch of partial sums takes about 1 us
+unsigned poll_rounds() {
+  const unsigned long long r = g_wait_ns.load() / 1024ull;
+  return (unsigned)(r < 16ull ? 16ull : (r > (1ull << 24) ? (1ull << 24) : r));
+}
+int stall_for_test() { return g_stall.load(); }
 
 }  // namespace q4
 
@@ -635,6 +648,16 @@ int q4mm_set_group_m_threshold(int64_t m) {
 
 int64_t q4mm_get_group_m_threshold(void) { return g_group_m_threshold.load(); }
 
+int q4mm_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? DEFAULT_WAIT_NS : (unsigned long long)ns);
+  return Q4_OK;
+}
+
+int q4mm_set_stall_for_test(int on) {
+  g_stall.store(on ? 1 : 0);
+  return Q4_OK;
+}
+
 int q4_device_status(void) {
   int dev;
   int st = current_device(&dev);
@@ -650,6 +673,17 @@ int q4_device_status(void) {
       if (v) {
         const unsigned zero = 0;
         if (cudaMemcpy(ds.ws.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess)
+          return Q4_ERR_CUDA;
+      }
+      if (v & STATUS_TIMEOUT) {
+        // a kernel gave up part-way: its split-K counters, partial-sum words and
+        // greedy-pick keys may be left mid-launch; the device is idle, so reset
+        // them to the state every launch expects
+        if (cudaMemset(ds.ws.argmax_done, 0, sizeof(unsigned)) != cudaSuccess ||
+            cudaMemset(ds.ws.keys, 0, Q4MM_M_MAX * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaMemset(ds.ws.counters, 0, MAX_COUNTERS * sizeof(unsigned)) != cudaSuccess ||
+            (ds.ws.partial && cudaMemset(ds.ws.partial, 0, ds.ws.partial_bytes) != cudaSuccess) ||
+            cudaDeviceSynchronize() != cudaSuccess)
           return Q4_ERR_CUDA;
       }
     }

@@ -41,6 +41,8 @@ struct EpiArgs {
   unsigned long long* keys;  // [M]
   unsigned int* argmax_done;
   int tiles;            // tiles x m-tiles of this launch (greedy-pick completion count)
+  unsigned poll_limit;  // rounds of re-reads of a batch of partial sums before giving up
+  int stall;            // test setting: CTAs that are not last leave their partial sums unstored
 };
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t n) {
@@ -64,7 +66,6 @@ __device__ __forceinline__ float key_value(unsigned long long k) {
 // never zero, and idle words are zero.
 constexpr int ARRIVAL_BITS = 10;
 constexpr int MAX_SPLITS = (1 << ARRIVAL_BITS) - 1;
-constexpr unsigned POLL_LIMIT = 1u << 20;  // rounds of re-reads of a batch of partial sums before giving up
 
 __device__ __forceinline__ unsigned split_arrive(unsigned* counter) {
   return atomicAdd(counter, 1u);
@@ -116,6 +117,7 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MT], 
     unsigned long long* pp = e.partial + ((m0 + mfirst) * e.N_pad + n);
     constexpr int64_t KSTEP = MSTRIDE;  // token rows between a thread's values
     if (!arrival_last(arrival, e.splits)) {
+      if (e.stall) return;  // (test setting) the last CTA then waits for words nothing writes
 #pragma unroll
       for (int k = 0; k < MT; ++k)
         if (owned(k)) st_flagged(pp + (int64_t)split * sstride + k * KSTEP * e.N_pad, flag, val[k]);
@@ -147,7 +149,7 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MT], 
 #pragma unroll
           for (int j = 0; j < SB; ++j)
             if (peer(k, j) && (unsigned)(t[k][j] >> 32) != flag) ready = false;
-        if (ready || rounds >= POLL_LIMIT) break;
+        if (ready || rounds >= e.poll_limit) break;
         ++rounds;
 #pragma unroll
         for (int k = 0; k < MT; ++k)
@@ -164,7 +166,7 @@ __device__ __forceinline__ void finish_tile(const EpiArgs& e, float (&val)[MT], 
             val[k] += (s0 + j == split) ? own[k] : __uint_as_float((uint32_t)t[k][j]);
         }
     }
-    if (rounds >= POLL_LIMIT) atomicOr(e.status, STATUS_TIMEOUT);
+    if (rounds >= e.poll_limit) atomicOr(e.status, STATUS_TIMEOUT);
     if (lead && row == 0 && counter_slot >= 0) e.counters[counter_slot] = arrival_next(arrival);
   }
 

@@ -176,6 +176,13 @@ int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx
               float* maxval, const TcPlan& plan, const Workspace& ws, cudaStream_t s);
 
 int device_num_sms(int device);
+// Test settings (q4mm_set_wait_limit_ns, q4mm_set_stall_for_test): the bound
+// of every wait a kernel makes on another role or CTA, in ns (default 1 s),
+// the split-K poll rounds that match it, and whether launches withhold their
+// first hand-off so that the waiting side times out.
+unsigned long long wait_limit_ns();
+unsigned poll_rounds();
+int stall_for_test();
 // Read and clear the status word of q4mm_forward_noalloc's fixed scratch on
 // `device` (0 if that call never ran there).
 int noalloc_status_take(int device, unsigned* bits);

@@ -171,6 +171,8 @@ struct MmaArgs {
   // weight 0's output (gate and up projections of a gated MLP)
   int gated;
   unsigned int* status; // device status word (bounded-wait expiry)
+  unsigned long long wait_ns;  // bound of the waits between roles
+  int stall;            // test setting: the converters hand over no chunk
   int cluster;          // 1: the K splits of a tile are one thread-block cluster
   EpiArgs e;
 };
@@ -348,10 +350,11 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait (1 s, or until another thread of the CTA reported an expiry);
-// returns false on expiry.  The timer is read only after many polls.
+// Bounded wait (limit_ns, 1 s by default, or until another thread of the CTA
+// reported an expiry); returns false on expiry.  The timer is read only after
+// many polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* err) {
+                                                  const volatile int* err, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (uint32_t n = 1;; ++n) {
@@ -360,7 +363,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       if (*err) return false;
       const unsigned long long now = globaltimer();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > 1000000000ull) return false;
+      else if (now - t0 > limit_ns) return false;
     }
   }
 }
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
       const int c = RG ? 2 * i + (sl >> 3) : (R1 ? (i >> 2) : (i >> 1));
       const int slot = UP ? c : (c & (NSLOT - 1));
       if (!UP && (RG || (R1 ? (i & 3) == 0 : (i & 1) == 0)) &&
-          !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err)) {
+          !mbar_wait_bounded(smem_u32(&bfull[slot]), (uint32_t)((c / NSLOT) & 1), &s_err, a.wait_ns)) {
         s_err = 1;
         break;
       }
@@ -815,6 +818,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
 #pragma unroll
     for (int c = 0; c < XLEAD; ++c) stage(c);
     for (int c = 0; c < nchunks; ++c) {
+      if (a.stall) break;  // (test setting) no chunk is handed over: the compute warps' waits run out
       const int slot = c & (NSLOT - 1);
       uint8_t* sb = smem + slot * S::SLOT;
       const uint8_t* xs = smem + S::XRAW_OFF + (c % S::XSTAGES) * S::XSLOT;
@@ -824,7 +828,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
       asm volatile("cp.async.wait_group %0;" ::"n"(XLEAD - 1) : "memory");
       stage(c + XLEAD);  // refills the slot read in the previous iteration
       if (c >= NSLOT &&
-          !mbar_wait_bounded(smem_u32(&bempty[slot]), (uint32_t)(((c / NSLOT) + 1) & 1), &s_err)) {
+          !mbar_wait_bounded(smem_u32(&bempty[slot]), (uint32_t)(((c / NSLOT) + 1) & 1), &s_err, a.wait_ns)) {
         s_err = 1;
         break;
       }
@@ -892,7 +896,12 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
   const bool failed = s_err != 0;
   // a CTA of a cluster stays for the cluster barriers below whatever happened
   if (failed && !a.cluster) {
-    if (tid == 0) atomicOr(a.status, STATUS_TIMEOUT);
+    if (tid == 0) {
+      atomicOr(a.status, STATUS_TIMEOUT);
+      // the split-K counter still moves on to the next launch's epoch
+      if (a.e.splits > 1 && arrival_last(s_arrival, a.e.splits))
+        a.e.counters[blockIdx.x] = arrival_next(s_arrival);
+    }
     return;
   }
 
@@ -1183,6 +1192,10 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.kbp_per_split = RG ? W0->KBP : plan.kbp_per_split;
   a.gated = L.gated ? (int)L.W[0]->tiles : 0;
   a.status = ws.status;
+  a.wait_ns = wait_limit_ns();
+  a.stall = stall_for_test();
+  a.e.poll_limit = poll_rounds();
+  a.e.stall = a.stall;
   a.e.N = W0->N;
   a.e.N_pad = (int64_t)tiles * TILE_N;
   a.e.M = mrows;

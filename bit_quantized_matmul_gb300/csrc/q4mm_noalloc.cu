@@ -86,6 +86,11 @@ int noalloc_status_take(int dev, unsigned* bits) {
     const unsigned zero = 0;
     if (cudaMemcpy(d.base, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess) return Q4_ERR_CUDA;
   }
+  if (v & STATUS_TIMEOUT) {
+    // a kernel gave up part-way: counters, keys and partial-sum words back to zero
+    if (cudaMemset(d.base + 4, 0, NA_TOTAL - 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return Q4_ERR_CUDA;
+  }
   *bits = v;
   return Q4_OK;
 }

@@ -200,6 +200,8 @@ int launch_simt(const Weight* W, const float* x, int64_t M, float* y, int32_t* i
     a.e.keys = ws.keys + mb;
     a.e.argmax_done = ws.argmax_done;
     a.e.tiles = (int)W->tiles;
+    a.e.poll_limit = poll_rounds();
+    a.e.stall = 0;
     dim3 grid((unsigned)W->tiles, (unsigned)plan.splits);
     if (mrows == 1) simt_kernel<1><<<grid, SIMT_THREADS, 0, s>>>(a);
     else if (mrows == 2) simt_kernel<2><<<grid, SIMT_THREADS, 0, s>>>(a);

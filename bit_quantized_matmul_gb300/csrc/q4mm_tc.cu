@@ -105,6 +105,8 @@ struct TcArgs {
   int mtiles;
   int rs;              // 1: split-K by reduce-scatter (every CTA of the launch resident at once)
   unsigned int* status;
+  unsigned long long wait_ns;  // bound of the waits between roles and CTAs
+  int stall;           // test setting: the producer issues no copy, so every wait runs out
   EpiArgs e;
 };
 
@@ -166,9 +168,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Bounded wait: false (and the CTA error flag raised) if the phase does not
-// complete within WAIT_NS, or if another role already gave up.  The timer is
-// read only after a try has expired, off the common path.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* err) {
+// complete within limit_ns (WAIT_NS by default), or if another role already
+// gave up.  The timer is read only after a try has expired, off the common
+// path.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* err,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (;;) {
@@ -177,7 +181,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     const unsigned long long now = globaltimer();
     if (t0 == 0) {
       t0 = now;
-    } else if (now - t0 > WAIT_NS) {
+    } else if (now - t0 > limit_ns) {
       *err = 1;
       return false;
     }
@@ -434,17 +438,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   if (warp == PROD_WARP) {
     // ---------------- producer ----------------
     if (lane == 0) {
+      int nunits_issue = nunits;
       asm volatile("griddepcontrol.wait;" ::: "memory");  // the activation operand of the pre-pass
+      if (a.stall) nunits_issue = 0;  // (test setting) nothing arrives: every consumer's wait runs out
       const uint8_t* nib_base = a.w[wi].nib + ((int64_t)tile * a.KBP + bp0) * PAIR_NIB_BYTES;
       const uint8_t* scl_base = a.w[wi].scl + ((int64_t)tile * a.KBP + bp0) * PAIR_SCL_BYTES;
       const uint8_t* bop_base = a.xop + ((int64_t)mt * a.KB2 + 2 * bp0) * (int64_t)C::BOP_BLOCK;
       int last = -1;
-      for (int u = 0; u < nunits; ++u) {
+      for (int u = 0; u < nunits_issue; ++u) {
         const int st = u % C::NST;
         const int ub = min(U, nblk - u * U);
         if (u >= C::NST) {  // stage reuse: unit u - NST must be consumed
           const int v = u - C::NST;
-          if (!mbar_wait(smem_u32(&empty[v % NBR]), (v / NBR) & 1, err)) break;
+          if (!mbar_wait(smem_u32(&empty[v % NBR]), (v / NBR) & 1, err, a.wait_ns)) break;
         }
         const uint32_t sb = smem_u32(stages + st * C::STAGE_BYTES);
         const uint32_t fb = smem_u32(&full[u % NBR]);
@@ -469,7 +475,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
         const int ub = min(U, nblk - u * U);
         const int bi = u % NBR;
         const uint32_t par = (u / NBR) & 1;
-        if (!mbar_wait(smem_u32(&full[bi]), par, err) || !mbar_wait(smem_u32(&afull[bi]), par, err)) {
+        if (!mbar_wait(smem_u32(&full[bi]), par, err, a.wait_ns) ||
+            !mbar_wait(smem_u32(&afull[bi]), par, err, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
       const int st = u % C::NST, sa = u % C::NA;
       const int ub = min(U, nblk - u * U);
       const int bi = u % NBR;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[bi]), (u / NBR) & 1, err))) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[bi]), (u / NBR) & 1, err, a.wait_ns))) break;
       const uint8_t* sp = stages + st * C::STAGE_BYTES;
       // Block b of the unit (pair b / 2, half b % 2): the row's 32 weights sit
       // in the words of lanes 4fg + tq (tq = 0..3), two k-steps each.
@@ -534,7 +541,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
       if (lane == 0) mbar_arrive(smem_u32(&empty[bi]));
       if (u >= C::NA) {  // A slot reuse: the MMAs of unit u - NA must be done
         const int w = u - C::NA;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&afree[w % NBR]), (w / NBR) & 1, err))) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&afree[w % NBR]), (w / NBR) & 1, err, a.wait_ns))) break;
       }
       const uint32_t acol = a_base + lane_off + (uint32_t)(sa * C::A_UNIT_COLS);
 #pragma unroll
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
   const bool skip = *err != 0;
   __syncthreads();  // every thread has read the flag before the epilogue can raise it
   if (warp < 8 && !skip) {
-    const bool ok = mbar_wait(smem_u32(dfull), 0, err);
+    const bool ok = mbar_wait(smem_u32(dfull), 0, err, a.wait_ns);
     // every epilogue thread takes the same decision
     uint32_t any_bad;
     asm volatile(
@@ -654,7 +661,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_kernel(const TcArgs a) {
               if ((n & 63u) == 0u) {
                 const unsigned long long now = globaltimer();
                 if (t_start == 0) t_start = now;
-                else if (now - t_start > WAIT_NS) {
+                else if (now - t_start > a.wait_ns) {
                   atomicOr(a.e.status, STATUS_TIMEOUT);
                   break;
                 }
@@ -805,6 +812,10 @@ int launch_nb(const MmaLaunch& L, const float* x, int64_t ml, int32_t* idx, floa
   a.kbp_per_split = plan.kbp_per_split;
   a.mtiles = mtiles;
   a.status = ws.status;
+  a.wait_ns = wait_limit_ns();
+  a.stall = stall_for_test();
+  a.e.poll_limit = poll_rounds();
+  a.e.stall = 0;
   a.e.N = W->N;
   a.e.N_pad = tiles * TILE_N;
   a.e.M = ml;

@@ -332,9 +332,28 @@ Q4_API int64_t q4mm_get_m_threshold(void);
 Q4_API int q4mm_set_group_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_group_m_threshold(void);
 
+/* Test settings for the bounded waits (process-wide; the defaults are the
+ * library's normal behaviour).  Every wait a kernel makes on another of its
+ * roles or CTAs gives up after a bound, 1 s by default, records
+ * Q4_ERR_TIMEOUT for q4_device_status and lets the kernel return instead of
+ * hanging.
+ *   q4mm_set_wait_limit_ns  sets that bound (0 restores 1 s) for later
+ *                           launches; the split-K polls scale with it.
+ *   q4mm_set_stall_for_test when on, later launches withhold their first
+ *                           hand-off (the converter warps hand over no chunk,
+ *                           the CTAs of a K split store no partial sum, the
+ *                           tensor-core producer issues no copy), so that the
+ *                           waiting side waits for something nothing sets and
+ *                           its bound runs out.  Outputs are then unspecified.
+ * Launches with no wait (one K split with the activations converted up front)
+ * are unaffected.  Only tests need these. */
+Q4_API int q4mm_set_wait_limit_ns(uint64_t ns);
+Q4_API int q4mm_set_stall_for_test(int on);
+
 /* Synchronize the current device and return (then clear) the device status
  * words (the library's scratch and, once q4mm_forward_noalloc has run on the
- * device, its fixed array): Q4_OK; Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out;
+ * device, its fixed array): Q4_OK; Q4_ERR_TIMEOUT if a bounded wait in a kernel ran out
+ * (the library's scratch words are then reset for the calls that follow);
  * Q4_ERR_INVALID_ARG if q4mm_argmax_rows met a row index out of range; or
  * Q4_ERR_CUDA if the device reports an error. */
 Q4_API int q4_device_status(void);
