@@ -527,21 +527,17 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
     ssrc += SSTEP;
     ++fnext;
   };
-  if (compute) {
+  // first weight pairs: at entry (weights never depend on an earlier kernel),
+  // or with up-front conversion once the activation loads are issued (ahead
+  // of them they delay the conversion)
+  if (!UP && compute) {
 #pragma unroll
     for (int u = 0; u < WD; ++u) fetch();
   }
 
-  // zero the B fragments of every slot when some columns are not written by
-  // a converter (fewer rows than the launch's column groups hold); the
-  // converters then overwrite the columns of the real rows
-  if (TERMS * mrows < 8 * C) {
-    constexpr int PER_SLOT = S::SIG_OFF / 16;  // uint4 of B fragments per slot
-    const int zslots = UP ? nchunks : NSLOT;
-    for (int j = tid; j < zslots * PER_SLOT; j += NT)
-      *reinterpret_cast<uint4*>(smem + (j / PER_SLOT) * S::SLOT + (j % PER_SLOT) * 16) =
-          make_uint4(0u, 0u, 0u, 0u);
-  }
+  // B columns of token rows beyond the launch's are never written: an MMA
+  // output column depends on its own B column only, and the outputs of those
+  // columns are never read
   if (tid == 0) {
     for (int b = 0; b < NSLOT; ++b) {
       mbar_init(smem_u32(&bfull[b]), CONV_THREADS);
@@ -577,8 +573,8 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
       return -1;
     };
     const float* xr = a.x + bp0 * 64 + 4 * ct;
-    // batches of (chunk, up to 4 rows); the next batch's loads are issued
-    // before the current one is converted
+    // batches of (chunk, up to 4 rows); every batch's loads are issued, then
+    // the first weight pairs, then the batches are converted
     constexpr int MG = MAXM < 4 ? MAXM : 4;
     constexpr int NB = PER * (MAXM / MG);
     auto load_batch = [&](int b, float4 (&v)[MG]) {
@@ -595,11 +591,16 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
         }
       }
     };
-    float4 vc[MG], vn[MG];
-    load_batch(0, vc);
+    float4 vall[NB][MG];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) load_batch(b, vall[b]);
+    if (compute) {
+#pragma unroll
+      for (int u = 0; u < WD; ++u) fetch();
+    }
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      if (b + 1 < NB) load_batch(b + 1, vn);
+      const float4 (&vc)[MG] = vall[b];
       const int q = b / (MAXM / MG), m0 = (b % (MAXM / MG)) * MG;
       const int c = cset + q * CSETS;
       if (c < nchunks && m0 < mrows) {  // the same for the whole warp
@@ -634,10 +635,6 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
             }
           }
         }
-      }
-      if (b + 1 < NB) {
-#pragma unroll
-        for (int mm = 0; mm < MG; ++mm) vc[mm] = vn[mm];
       }
     }
     __syncthreads();
