@@ -422,7 +422,7 @@ def run_gpu(args):
         }
 
     # ---- end to end through the C ABI: pinned host x in, every output out ----
-    e2e = e2e_c_abi(q4, torch, dev, stack, msw, layers, args.steps, stream, world)
+    e2e = e2e_c_abi(q4, torch, dev, stack, msw, layers, args.steps, stream, world, flags)
     e2e_value = whole_job_gbs(step_wbytes, world, e2e["ms_per_step"])
 
     configs = None
@@ -508,7 +508,7 @@ def _graph_us(torch, stream, issue, reps, calls, warm=3):
     return statistics.median(times)
 
 
-def e2e_c_abi(q4, torch, dev, stack, msw, layers, steps, stream, world):
+def e2e_c_abi(q4, torch, dev, stack, msw, layers, steps, stream, world, flags=0):
     """The step end to end through the library's C ABI: per M, x is copied in
     from pinned host memory, every call is made through the C entry points
     (argument checks, path choice and launches inside the timed region), and
@@ -542,13 +542,13 @@ def e2e_c_abi(q4, torch, dev, stack, msw, layers, steps, stream, world):
             for gname, names in GROUPS:
                 K = synthetic.QWEN7B_LINEARS[names[0]][1]
                 if len(names) == 1:
-                    ops.append((lib.q4mm_forward, (stack[names[0]][layer].handle, ctypes.c_void_p(xd[K].data_ptr()),
-                                                   ctypes.c_void_p(yp[names[0]]), M, sh)))
+                    ops.append((lib.q4mm_forward_ex, (stack[names[0]][layer].handle, ctypes.c_void_p(xd[K].data_ptr()),
+                                                      ctypes.c_void_p(yp[names[0]]), M, flags, sh)))
                 else:
                     hw = (ctypes.c_void_p * len(names))(*[stack[n][layer].handle.value for n in names])
                     hy = (ctypes.c_void_p * len(names))(*[yp[n] for n in names])
                     ops.append((lib.q4mm_forward_group, (hw, len(names), ctypes.c_void_p(xd[K].data_ptr()), hy, M,
-                                                         0, sh)))
+                                                         flags, sh)))
         calls += len(ops)
         per_m.append((xh, xd, arena, arena_h, ops))
 

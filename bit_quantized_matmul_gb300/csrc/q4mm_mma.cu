@@ -182,14 +182,16 @@ struct MmaArgs {
 // thread of the CTA, into one ring slot per chunk.
 constexpr int UP_CHUNKS = 8;
 
-template <int C, int TPC = 1, bool RG = false, bool UP = false>
+template <int C, int TPC = 1, bool RG = false, bool UP = false, bool R1F = false>
 struct MmaCfg {
   static constexpr int MAXM = C * 8 / TERMS;  // token rows per launch
   // three or four column groups (9 to 16 token rows): one row group per
   // compute warp, 8 row groups x 2 K slices, so that the accumulators fit;
   // a two-slot B ring and three x stages, so that the larger fragments fit in
   // shared memory
-  static constexpr bool R1 = !RG && TPC == 1 && C >= 3;
+  // (R1F: the same layout for one and two column groups, as batch-invariant
+  // launches of any row count take it)
+  static constexpr bool R1 = !RG && TPC == 1 && (C >= 3 || R1F);
   static constexpr int NSL = R1 ? 2 : SLICES;  // K slices of a tile's CTA
   static constexpr int NRG = R1 ? 1 : 2;       // row groups per compute warp
   // B ring depth (a power of two); row-group CTAs hold every chunk of their
@@ -428,9 +430,9 @@ __device__ __forceinline__ void split4(const float4& v, float s, uint32_t (&ta)[
 // reads its 512 contiguous bytes conflict-free in any slot order).  The slot
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
-template <int C, bool RG, int TPC, bool UP>
-__global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel(const MmaArgs a) {
-  using S = MmaCfg<C, TPC, RG, UP>;
+template <int C, bool RG, int TPC, bool UP, bool R1F = false>
+__global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_kernel(const MmaArgs a) {
+  using S = MmaCfg<C, TPC, RG, UP, R1F>;
   constexpr int NT = S::THREADS;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
@@ -1130,7 +1132,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
 
 // Clusters of `size` CTAs of this kernel that the device holds at once (0 if
 // none or unknown), per device, cached.
-template <int C, bool UP>
+template <int C, bool RG, int TPC, bool UP, bool R1F>
 int cluster_capacity(int device, int size) {
   static std::atomic<int> cache[64][9];  // value + 1; 0 = not yet asked
   if (size < 2 || size > 8) return 0;
@@ -1139,8 +1141,8 @@ int cluster_capacity(int device, int size) {
   if (c > 0) return c - 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
-  cfg.blockDim = dim3(MmaCfg<C, 1, false, UP>::THREADS);
-  cfg.dynamicSmemBytes = MmaCfg<C, 1, false, UP>::BYTES;
+  cfg.blockDim = dim3(MmaCfg<C, TPC, RG, UP, R1F>::THREADS);
+  cfg.dynamicSmemBytes = MmaCfg<C, TPC, RG, UP, R1F>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -1149,7 +1151,7 @@ int cluster_capacity(int device, int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, false, 1, UP>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, RG, TPC, UP, R1F>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -1157,11 +1159,11 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
-template <int C, bool RG, int TPC = 1, bool UP = false>
+template <int C, bool RG, int TPC = 1, bool UP = false, bool R1F = false>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
-  using S = MmaCfg<C, TPC, RG, UP>;
+  using S = MmaCfg<C, TPC, RG, UP, R1F>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
   int tiles = 0;
@@ -1210,7 +1212,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // different locks; setting the attribute twice is harmless)
   static std::atomic<bool> attr_set[64];
   if (!attr_set[W0->device & 63].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(mma_kernel<C, RG, TPC, UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, RG, TPC, UP, R1F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63].store(true, std::memory_order_release);
@@ -1222,7 +1224,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
   a.cluster = !RG && TPC == 1 && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
-              tiles <= cluster_capacity<C, UP>(W0->device, plan.splits);
+              tiles <= cluster_capacity<C, RG, TPC, UP, R1F>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
                    : L.gated ? dim3((unsigned)L.W[0]->tiles, 1, 1)
@@ -1239,7 +1241,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C, RG, TPC, UP>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, RG, TPC, UP, R1F>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 // Rows per launch: 16 (four column groups of two terms per row), in both
@@ -1325,9 +1327,16 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
     const int32_t* xr = xrows ? xrows + mb : nullptr;
     int st;
     if (batch_invariant) {
-      // one kernel for every row count: a row's operations and their order
-      // never depend on how many rows share its launch
-      st = launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      // one layout for every row count (one row group per warp, two K
+      // slices, the split plan of the shapes), as many column groups as the
+      // launch's rows need: a row's operations and their order never depend
+      // on how many rows share its launch (an MMA output column depends on
+      // its own B column only)
+      const int cgs = (TERMS * mrows + 7) / 8;
+      st = cgs == 1   ? launch_c<1, false, 1, false, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+           : cgs == 2 ? launch_c<2, false, 1, false, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+           : cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     } else {
       const int cgs = (TERMS * mrows + 7) / 8;  // column groups of this launch
       if (cgs >= 3) {  // 9 to 16 rows: one row group per warp, K splits
