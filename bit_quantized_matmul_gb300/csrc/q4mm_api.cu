@@ -617,8 +617,9 @@ int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int
   } else if (p == Q4MM_PATH_MMA) {
     const MmaPlan plan = mma_plan(&W->w, ds.num_sms);
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
-    l = mma_launch_count(M, inv);
-    const int64_t rows0 = M < mma_rows_per_launch(inv) ? M : mma_rows_per_launch(inv);  // first launch
+    const bool two = mma_two_tiles(plan, W->w.tiles, inv);
+    l = mma_launch_count(M, inv, two);
+    const int64_t rows0 = M < mma_rows_per_launch(inv, two) ? M : mma_rows_per_launch(inv, two);  // first launch
     sp = mma_row_groups(plan, W->w.K, inv, false, rows0) ? 1 : plan.splits;
   } else {
     const MmaPlan plan = simt_plan(&W->w, ds.num_sms);

@@ -116,11 +116,14 @@ MmaPlan mma_plan(const Weight* W, int num_sms);
 // launch has at most 8 rows, for y output in default mode.
 bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick,
                     int64_t launch_rows);
-int mma_rows_per_launch(bool batch_invariant);
+// Launches of more tiles than SMs with one K split run as two-tile CTAs in
+// default mode, and then take at most 8 token rows each (16 otherwise).
+bool mma_two_tiles(const MmaPlan& plan, int64_t tiles, bool batch_invariant);
+int mma_rows_per_launch(bool batch_invariant, bool two_tiles);
 MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms);
 size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant);
 size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant);
-int mma_launch_count(int64_t M, bool batch_invariant);
+int mma_launch_count(int64_t M, bool batch_invariant, bool two_tiles);
 int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
                const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,

@@ -1245,8 +1245,14 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
 }
 
 // Rows per launch: 16 (four column groups of two terms per row), in both
-// modes.
-int rows_per_launch(bool) { return MAX_CG * 8 / TERMS; }
+// modes; 8 for launches that run as two-tile CTAs (one or two column
+// groups), which stream two tiles per CTA in one wave where 16 rows would
+// need one tile per CTA in two waves.  Measured on GB300 for the gate/up
+// group of a 7B layer (two launches of 8 rows / one of 16): 42.6 / 53.0 us at
+// M = 16.
+int rows_per_launch(bool batch_invariant, bool two_tiles = false) {
+  return (two_tiles && !batch_invariant) ? 8 : MAX_CG * 8 / TERMS;
+}
 
 }  // namespace
 
@@ -1280,10 +1286,14 @@ size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batc
   return mma_partial_bytes_tiles(W->tiles, p, M, batch_invariant);
 }
 
-int mma_rows_per_launch(bool batch_invariant) { return rows_per_launch(batch_invariant); }
+bool mma_two_tiles(const MmaPlan& plan, int64_t tiles, bool batch_invariant) {
+  return Q4MM_TWO_TILES && !batch_invariant && plan.splits == 1 && plan.num_sms > 0 && tiles > plan.num_sms;
+}
 
-int mma_launch_count(int64_t M, bool batch_invariant) {
-  const int64_t rpl = rows_per_launch(batch_invariant);
+int mma_rows_per_launch(bool batch_invariant, bool two_tiles) { return rows_per_launch(batch_invariant, two_tiles); }
+
+int mma_launch_count(int64_t M, bool batch_invariant, bool two_tiles) {
+  const int64_t rpl = rows_per_launch(batch_invariant, two_tiles);
   return (int)((M + rpl - 1) / rpl);
 }
 
@@ -1300,7 +1310,6 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   for (int i = 0; i < L.count; ++i) tiles += L.W[i]->tiles;
   if (plan.splits > 1 && tiles > MAX_COUNTERS) return Q4_ERR_SHAPE;
   const int64_t K = L.W[0]->K;
-  const int64_t rpl = rows_per_launch(batch_invariant);
   // row-group CTAs (per launch, below): no K split and so no cross-CTA
   // exchange, when four CTAs per tile fit on the SMs (the split plan has at
   // least 4 splits), K is short and the launch has at most 8 rows; the plan
@@ -1308,8 +1317,8 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
   // two tiles per CTA (whole K, no split): launches of more tiles than SMs
   // run as CTAs that stream two tiles each, for one or two column groups (up
   // to 8 rows) in default mode (y output or the greedy pick)
-  const bool two = Q4MM_TWO_TILES && !batch_invariant && plan.splits == 1 && plan.num_sms > 0 &&
-                   tiles > plan.num_sms;
+  const bool two = mma_two_tiles(plan, tiles, batch_invariant);
+  const int64_t rpl = rows_per_launch(batch_invariant, two);
   // up-front conversion when every CTA's K range is at most UP_CHUNKS chunks
   // (row-group CTAs cover the whole K).  Measured on GB300 over the 7B layer
   // (8 layer copies per graph, us per call, up-front / converter warps):

@@ -158,8 +158,9 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
 
 /* y_i = x @ W_i^T for up to Q4MM_GROUP_MAX weights that share K and the same
  * activations (the q, k and v projections, or the gate and up projections, of
- * one decoder layer), in one kernel launch per 16 token rows instead of one per
- * weight: the activations are staged once and the fixed cost of a launch is
+ * one decoder layer), in one kernel launch per 16 token rows (8 when the
+ * group's tiles outnumber the SMs) instead of one per weight: the activations
+ * are staged once and the fixed cost of a launch is
  * paid once ("Why LLM Decoding Is Slow, and Why Batching Is (Almost) Free",
  * §4: every weight is still read exactly once per call).
  *   W       host array of `count` handles, all with the same K, on the current
@@ -326,7 +327,8 @@ Q4_API int q4mm_set_m_threshold(int64_t m);
 Q4_API int64_t q4mm_get_m_threshold(void);
 
 /* The M threshold of q4mm_forward_group: at or above it one tcgen05 launch
- * covers the whole group, below it one streaming launch per 16 token rows.
+ * covers the whole group, below it one streaming launch per 16 token rows (8
+ * when the group's tiles outnumber the SMs).
  * The default is the crossover measured on GB300 over a 7B layer's q/k/v and
  * gate/up groups.  Same range and errors as set_m_threshold. */
 Q4_API int q4mm_set_group_m_threshold(int64_t m);
