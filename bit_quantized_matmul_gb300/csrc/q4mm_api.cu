@@ -47,11 +47,12 @@ DeviceScratch g_dev[MAX_DEVICES];
 constexpr int64_t DEFAULT_M_THRESHOLD = 17;
 std::atomic<int64_t> g_m_threshold{DEFAULT_M_THRESHOLD};
 // Grouped calls (q4mm_forward_group) run one launch over the whole group on
-// either path.  Measured the same way over a layer's q/k/v and gate/up groups:
-// the streaming launches are faster up to M = 16 (66.3 against 84.4 us for
-// the two groups), the grouped tensor-core launches from M = 17 (84.6 against
-// 86.4 us).
-constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 17;
+// either path (the gate/up group's streaming launches take 8 rows each, as
+// two-tile CTAs).  Measured on GB300 over a layer's q/k/v and gate/up groups
+// (8 layer copies in a graph, us for the two groups, streaming / tensor
+// cores): 75.2 / 85.3 at M = 20, 83.7 / 85.3 at M = 24, 99.8 / 85.7 at
+// M = 25 and 109.2 / 86.0 at M = 32.
+constexpr int64_t DEFAULT_GROUP_M_THRESHOLD = 25;
 std::atomic<int64_t> g_group_m_threshold{DEFAULT_GROUP_M_THRESHOLD};
 
 // Test settings (q4mm_set_wait_limit_ns, q4mm_set_stall_for_test).
