@@ -665,17 +665,12 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_k
         asm volatile("cp.async.wait_group %0;" ::"n"(WD - 1) : "memory");
         __syncwarp();
       }
-      const uint32_t src = wring + (uint32_t)(i % WD) * (S::WSLOT * TPC) + (uint32_t)(tt * S::WSLOT);
+      const uint8_t* srcp = smem + S::WR_OFF + warp * (WD * S::WSLOT * TPC) + (i % WD) * (S::WSLOT * TPC) +
+                            tt * S::WSLOT;
 #pragma unroll
       for (int r = 0; r < NRG; ++r) {
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[r].x), "=r"(w[r].y), "=r"(w[r].z), "=r"(w[r].w)
-                     : "r"(src + r * 512u + lane * 16)
-                     : "memory");
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                     : "=r"(sv[r].x), "=r"(sv[r].y)
-                     : "r"(src + S::WSCL + r * 64u + g * 8)
-                     : "memory");
+        w[r] = *reinterpret_cast<const uint4*>(srcp + r * 512 + lane * 16);
+        sv[r] = *reinterpret_cast<const uint2*>(srcp + S::WSCL + r * 64 + g * 8);
       }
     };
 #if Q4MM_UNROLL == 2
@@ -697,7 +692,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_k
       // {1/s, 1/s} and {1/(16 s), 1/(16 s)} of token row 4 cg + tq (the
       // lane's two columns are that row's two terms; rows beyond the launch's
       // are not written: their columns are never read back)
-      const uint32_t sig = smem_u32(sb + S::SIG_OFF + (pc * MAXM + tq) * 16);
+      const uint8_t* sigp = sb + S::SIG_OFF + (pc * MAXM + tq) * 16;
 #pragma unroll
       for (int tt = 0; tt < TPC; ++tt) {
         if (tt == 1 && !has1) break;  // the same for every thread of the CTA
@@ -752,7 +747,11 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_k
 #pragma unroll
         for (int cg = 0; cg < C; ++cg) {
           unsigned long long s0, s1;
-          asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(s0), "=l"(s1) : "r"(sig + cg * 64u) : "memory");
+          {
+            const ulonglong2 sg = *reinterpret_cast<const ulonglong2*>(sigp + cg * 64);
+            s0 = sg.x;
+            s1 = sg.y;
+          }
 #pragma unroll
           for (int r = 0; r < NRG; ++r) {
             ffma2p(acc[tt][r][cg][0], s0, pp[r][cg][0]);
