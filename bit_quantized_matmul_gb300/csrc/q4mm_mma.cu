@@ -182,16 +182,14 @@ struct MmaArgs {
 // thread of the CTA, into one ring slot per chunk.
 constexpr int UP_CHUNKS = 8;
 
-template <int C, int TPC = 1, bool RG = false, bool UP = false, bool R1F = false>
+template <int C, int TPC = 1, bool RG = false, bool UP = false>
 struct MmaCfg {
   static constexpr int MAXM = C * 8 / TERMS;  // token rows per launch
   // three or four column groups (9 to 16 token rows): one row group per
   // compute warp, 8 row groups x 2 K slices, so that the accumulators fit;
   // a two-slot B ring and three x stages, so that the larger fragments fit in
   // shared memory
-  // (R1F: the same layout for one and two column groups, as batch-invariant
-  // launches of any row count take it)
-  static constexpr bool R1 = !RG && TPC == 1 && (C >= 3 || R1F);
+  static constexpr bool R1 = !RG && TPC == 1 && C >= 3;
   static constexpr int NSL = R1 ? 2 : SLICES;  // K slices of a tile's CTA
   static constexpr int NRG = R1 ? 1 : 2;       // row groups per compute warp
   // B ring depth (a power of two); row-group CTAs hold every chunk of their
@@ -430,9 +428,9 @@ __device__ __forceinline__ void split4(const float4& v, float s, uint32_t (&ta)[
 // reads its 512 contiguous bytes conflict-free in any slot order).  The slot
 // holds {b0, b1} of k-step 0 and {b0, b1} of k-step 1 for column g.
 // ----------------------------------------------------------------------------
-template <int C, bool RG, int TPC, bool UP, bool R1F = false>
-__global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_kernel(const MmaArgs a) {
-  using S = MmaCfg<C, TPC, RG, UP, R1F>;
+template <int C, bool RG, int TPC, bool UP>
+__global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel(const MmaArgs a) {
+  using S = MmaCfg<C, TPC, RG, UP>;
   constexpr int NT = S::THREADS;
   constexpr int MAXM = S::MAXM;
   constexpr int WD = S::WD;
@@ -1131,7 +1129,7 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP, R1F>::THREADS, 1) mma_k
 
 // Clusters of `size` CTAs of this kernel that the device holds at once (0 if
 // none or unknown), per device, cached.
-template <int C, bool RG, int TPC, bool UP, bool R1F>
+template <int C, bool RG, int TPC, bool UP>
 int cluster_capacity(int device, int size) {
   static std::atomic<int> cache[64][9];  // value + 1; 0 = not yet asked
   if (size < 2 || size > 8) return 0;
@@ -1140,8 +1138,8 @@ int cluster_capacity(int device, int size) {
   if (c > 0) return c - 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)size, 1);
-  cfg.blockDim = dim3(MmaCfg<C, TPC, RG, UP, R1F>::THREADS);
-  cfg.dynamicSmemBytes = MmaCfg<C, TPC, RG, UP, R1F>::BYTES;
+  cfg.blockDim = dim3(MmaCfg<C, TPC, RG, UP>::THREADS);
+  cfg.dynamicSmemBytes = MmaCfg<C, TPC, RG, UP>::BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -1150,7 +1148,7 @@ int cluster_capacity(int device, int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, RG, TPC, UP, R1F>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<C, RG, TPC, UP>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -1158,11 +1156,11 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
-template <int C, bool RG, int TPC = 1, bool UP = false, bool R1F = false>
+template <int C, bool RG, int TPC = 1, bool UP = false>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
              const int32_t* xrows, int64_t x_rows) {
-  using S = MmaCfg<C, TPC, RG, UP, R1F>;
+  using S = MmaCfg<C, TPC, RG, UP>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
   int tiles = 0;
@@ -1211,7 +1209,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // different locks; setting the attribute twice is harmless)
   static std::atomic<bool> attr_set[64];
   if (!attr_set[W0->device & 63].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(mma_kernel<C, RG, TPC, UP, R1F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mma_kernel<C, RG, TPC, UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::BYTES) != cudaSuccess)
       return Q4_ERR_CUDA;
     attr_set[W0->device & 63].store(true, std::memory_order_release);
@@ -1223,7 +1221,7 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   // the 7B decoder layers: clusters of 4 beat the global-memory exchange,
   // clusters of 5 lost to it.)
   a.cluster = !RG && TPC == 1 && plan.splits > 1 && plan.splits <= Q4MM_CLUSTER_MAX && idx == nullptr &&
-              tiles <= cluster_capacity<C, RG, TPC, UP, R1F>(W0->device, plan.splits);
+              tiles <= cluster_capacity<C, RG, TPC, UP>(W0->device, plan.splits);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = RG ? dim3((unsigned)tiles * 4u, 1, 1)
                    : L.gated ? dim3((unsigned)L.W[0]->tiles, 1, 1)
@@ -1240,17 +1238,18 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, mma_kernel<C, RG, TPC, UP, R1F>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, mma_kernel<C, RG, TPC, UP>, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
-// Rows per launch: 16 (four column groups of two terms per row), in both
-// modes; 8 for launches that run as two-tile CTAs (one or two column
-// groups), which stream two tiles per CTA in one wave where 16 rows would
-// need one tile per CTA in two waves.  Measured on GB300 for the gate/up
-// group of a 7B layer (two launches of 8 rows / one of 16): 42.6 / 53.0 us at
-// M = 16.
+// Rows per launch: 16 (four column groups of two terms per row) in default
+// mode; 8 for launches that run as two-tile CTAs (one or two column groups),
+// which stream two tiles per CTA in one wave where 16 rows would need one tile
+// per CTA in two waves (measured on GB300 for the gate/up group of a 7B layer,
+// two launches of 8 rows / one of 16: 42.6 / 53.0 us at M = 16); 8 for every
+// batch-invariant launch (one or two column groups, so that every row count
+// runs the same layout).
 int rows_per_launch(bool batch_invariant, bool two_tiles = false) {
-  return (two_tiles && !batch_invariant) ? 8 : MAX_CG * 8 / TERMS;
+  return (two_tiles || batch_invariant) ? 8 : MAX_CG * 8 / TERMS;
 }
 
 }  // namespace
@@ -1285,8 +1284,8 @@ size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batc
   return mma_partial_bytes_tiles(W->tiles, p, M, batch_invariant);
 }
 
-bool mma_two_tiles(const MmaPlan& plan, int64_t tiles, bool batch_invariant) {
-  return Q4MM_TWO_TILES && !batch_invariant && plan.splits == 1 && plan.num_sms > 0 && tiles > plan.num_sms;
+bool mma_two_tiles(const MmaPlan& plan, int64_t tiles, bool) {
+  return Q4MM_TWO_TILES && plan.splits == 1 && plan.num_sms > 0 && tiles > plan.num_sms;
 }
 
 int mma_rows_per_launch(bool batch_invariant, bool two_tiles) { return rows_per_launch(batch_invariant, two_tiles); }
@@ -1298,8 +1297,8 @@ int mma_launch_count(int64_t M, bool batch_invariant, bool two_tiles) {
 
 bool mma_row_groups(const MmaPlan& plan, int64_t K, bool batch_invariant, bool greedy_pick,
                     int64_t launch_rows) {
-  return !batch_invariant && !greedy_pick && launch_rows <= Q4MM_RG_MAX_ROWS && plan.splits >= 4 &&
-         K <= Q4MM_RG_MAX_K;
+  (void)batch_invariant;
+  return !greedy_pick && launch_rows <= Q4MM_RG_MAX_ROWS && plan.splits >= 4 && K <= Q4MM_RG_MAX_K;
 }
 
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,
@@ -1334,42 +1333,35 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
     const float* xs = xrows ? x : x + mb * K;
     const int32_t* xr = xrows ? xrows + mb : nullptr;
     int st;
-    if (batch_invariant) {
-      // one layout for every row count (one row group per warp, two K
-      // slices, the split plan of the shapes), as many column groups as the
-      // launch's rows need: a row's operations and their order never depend
-      // on how many rows share its launch (an MMA output column depends on
-      // its own B column only)
-      const int cgs = (TERMS * mrows + 7) / 8;
-      st = cgs == 1   ? launch_c<1, false, 1, false, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-           : cgs == 2 ? launch_c<2, false, 1, false, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-           : cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                      : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+    // batch-invariant mode takes the same kernels as the default mode in
+    // launches of at most 8 rows (one or two column groups): their layout
+    // depends on the shapes only (row-group, two-tile or split CTAs, the K
+    // partition of the shapes), every MMA output column depends on its own B
+    // column only, and a column's scaling, slice and split sums are the same
+    // operations in the same order whatever the column count
+    const int cgs = (TERMS * mrows + 7) / 8;  // column groups of this launch
+    if (cgs >= 3) {  // 9 to 16 rows: one row group per warp, K splits
+      st = cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                    : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+    } else if (rg) {
+      if (up_rg) st = cgs == 1 ? launch_c<1, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                               : launch_c<2, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                         : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+    } else if (two) {
+      if (Q4MM_UP_TWO && up_two)
+        st = cgs == 1 ? launch_c<1, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<2, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      else
+        st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     } else {
-      const int cgs = (TERMS * mrows + 7) / 8;  // column groups of this launch
-      if (cgs >= 3) {  // 9 to 16 rows: one row group per warp, K splits
-        st = cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                      : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-      } else if (rg) {
-        if (up_rg) st = cgs == 1 ? launch_c<1, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                                 : launch_c<2, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-        else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                           : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-      } else if (two) {
-        if (Q4MM_UP_TWO && up_two)
-          st = cgs == 1 ? launch_c<1, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                        : launch_c<2, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-        else
-          st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                        : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-      } else {
-        if (up_split)
-          st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                        : launch_c<2, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-        else
-          st = cgs == 1 ? launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                        : launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-      }
+      if (up_split)
+        st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<2, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      else
+        st = cgs == 1 ? launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
+                      : launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     }
     if (st) return st;
   }

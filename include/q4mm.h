@@ -79,11 +79,12 @@ extern "C" {
 
 /* ---- flags for the _ex entry points ---- */
 /* Bit-identical output rows: row r of y depends only on x[r,:] and W, never on
- * M, on r's position in the batch or on the other rows' values.  The kernel
- * family, the K partition and each row's MMA column positions are then fixed
- * per weight shape, independent of M (§"The Other Request Already Finished":
- * a 120-prefill + 4-verify batch crossed the kernel-switch threshold and
- * changed the cached numbers). */
+ * M, on r's position in the batch or on the other rows' values.  The calls
+ * then run the streaming kernel for every M, in launches of at most 8 rows,
+ * with the CTA layout and the K partition fixed per weight shape; a row's
+ * operations do not depend on the MMA column it occupies (§"The Other Request
+ * Already Finished": a 120-prefill + 4-verify batch crossed the kernel-switch
+ * threshold and changed the cached numbers). */
 #define Q4MM_BATCH_INVARIANT 0x1u
 /* Force the CUDA-core streaming kernel (no tensor cores). */
 #define Q4MM_FORCE_SIMT 0x2u
