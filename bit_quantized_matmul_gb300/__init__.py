@@ -49,7 +49,7 @@ EXPORTS = (
     "q4mm_forward_noalloc", "q4mm_forward_group", "q4mm_forward_gated", "q4mm_argmax_rows", "q4_verify_greedy",
     "q4mm_select_path", "q4mm_plan_info", "q4mm_set_m_threshold", "q4mm_get_m_threshold", "q4mm_set_group_m_threshold",
     "q4mm_get_group_m_threshold", "q4_device_status", "q4mm_set_wait_limit_ns", "q4mm_set_stall_for_test",
-    "q4_status_string",
+    "q4_status_string", "q4_scratch_bytes",
     "q4_kv_append",
 )
 
@@ -90,6 +90,7 @@ _sig = {
     "q4mm_set_wait_limit_ns": [ctypes.c_uint64],
     "q4mm_set_stall_for_test": [ctypes.c_int],
     "q4_status_string": [ctypes.c_int],
+    "q4_scratch_bytes": [ctypes.POINTER(ctypes.c_size_t)] * 3,
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -446,6 +447,13 @@ def q4mm_set_stall_for_test(on: bool):
 
 def q4_device_status() -> int:
     return int(_lib.q4_device_status())
+
+
+def q4_scratch_bytes() -> tuple:
+    """(partial, xop, gu): bytes of the library's scratch now held on the current device."""
+    v = [ctypes.c_size_t(0) for _ in range(3)]
+    _check(_lib.q4_scratch_bytes(*[ctypes.byref(a) for a in v]), "q4_scratch_bytes")
+    return tuple(int(a.value) for a in v)
 
 
 def raw_library() -> ctypes.CDLL:

@@ -10,6 +10,7 @@
 // Effect?").
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -238,6 +239,30 @@ int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace*
   return Q4_OK;
 }
 
+// The largest scratch any single-weight call on W can ask for, reserved when W
+// is created (a synchronous step) so that q4mm_forward / q4mm_argmax on a
+// created weight never allocate or synchronize.  Every path's scratch stops
+// growing at its rows per launch (16 streaming, 256 tensor-core, the SIMT
+// launch size), so the maxima are taken at M = Q4MM_M_MAX, and over all
+// tensor-core launch sizes since its K partition depends on the token tiles.
+// Caller holds g_dev[device].mu.
+int workspace_reserve_for(int device, const Weight* W) {
+  const DeviceScratch& ds = g_dev[device];
+  size_t partial = mma_partial_bytes(W, mma_plan(W, ds.num_sms), Q4MM_M_MAX, false);
+  partial = std::max(partial, simt_partial_bytes(W, simt_plan(W, ds.num_sms), Q4MM_M_MAX));
+  size_t xop = 0;
+  if (tc_supported(ds)) {
+    for (int inv = 0; inv < 2; ++inv)
+      for (int64_t m = 1; m <= tc_rows_per_launch(); ++m) {
+        const TcPlan plan = tc_plan(W, m, ds.num_sms, inv != 0);
+        partial = std::max(partial, tc_partial_bytes(W, plan, m));
+        xop = std::max(xop, tc_xop_bytes(W, plan, m));
+      }
+  }
+  Workspace ws;
+  return workspace_get(device, partial, xop, &ws);
+}
+
 int device_num_sms(int device) { return g_dev[device].num_sms; }
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
@@ -290,6 +315,7 @@ int q4_quantize(const float* w, int64_t N, int64_t K, q4_weight** out, cudaStrea
   if (!st && cudaStreamSynchronize(stream) != cudaSuccess) st = Q4_ERR_CUDA;
   cudaFree(canon);
   if (!st) st = quantize_flag_status(flag);
+  if (!st) st = workspace_reserve_for(dev, &h->w);
   if (st) {
     cudaFree(h->w.alloc);
     delete h;
@@ -337,6 +363,7 @@ int q4_import_blocks(const void* host_blocks, int64_t N, int64_t K, q4_weight** 
   if (!st && cudaStreamSynchronize(stream) != cudaSuccess) st = Q4_ERR_CUDA;
   cudaFree(staging);
   if (!st) st = quantize_flag_status(flag);
+  if (!st) st = workspace_reserve_for(dev, &h->w);
   if (st) {
     cudaFree(h->w.alloc);
     delete h;
@@ -657,6 +684,19 @@ int q4mm_set_wait_limit_ns(uint64_t ns) {
 
 int q4mm_set_stall_for_test(int on) {
   g_stall.store(on ? 1 : 0);
+  return Q4_OK;
+}
+
+int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu) {
+  if (!partial || !xop || !gu) return Q4_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  DeviceScratch& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  *partial = ds.ws.partial_bytes;
+  *xop = ds.ws.xop_bytes;
+  *gu = ds.ws.gu_bytes;
   return Q4_OK;
 }
 

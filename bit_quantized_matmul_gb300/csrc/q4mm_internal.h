@@ -175,6 +175,7 @@ int launch_tc_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx,
 size_t tc_partial_bytes(const Weight* W, const TcPlan& p, int64_t M);
 size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M);
 int tc_launch_count(const TcPlan& p, int64_t M);
+int64_t tc_rows_per_launch();  // token rows per launch pair
 int launch_tc(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx,
               float* maxval, const TcPlan& plan, const Workspace& ws, cudaStream_t s);
 

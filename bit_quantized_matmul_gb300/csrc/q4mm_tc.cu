@@ -906,6 +906,8 @@ size_t tc_xop_bytes_kbp(int64_t KBP, const TcPlan& p, int64_t M) {
 
 size_t tc_xop_bytes(const Weight* W, const TcPlan& p, int64_t M) { return tc_xop_bytes_kbp(W->KBP, p, M); }
 
+int64_t tc_rows_per_launch() { return TC_M_LAUNCH; }
+
 int tc_launch_count(const TcPlan&, int64_t M) {
   return 2 * (int)((M + TC_M_LAUNCH - 1) / TC_M_LAUNCH);
 }

@@ -40,8 +40,13 @@
  *    call surfaces as Q4_ERR_CUDA on a later call.
  *  - Compute calls use a per-device scratch area owned by the library (split-K
  *    partial sums, the activation operand of the tensor-core path, argmax
- *    keys).  It is allocated (or grown) on the first call that needs it, so
- *    make one call of each shape before capturing a CUDA graph.  Calls that
+ *    keys).  Creating a weight (q4_quantize, q4_import_blocks) reserves the
+ *    largest scratch that any single-weight call on it can need, at any M and
+ *    with any flags, so q4mm_forward, q4mm_forward_ex and q4mm_argmax on a
+ *    created weight never allocate.  A grouped or gated call (its weights'
+ *    tiles summed) grows the scratch on its first call of a larger shape
+ *    (cudaFree, cudaMalloc, a device synchronize): make one such call of each
+ *    shape before capturing a CUDA graph.  Calls that
  *    share that scratch must be ordered on one stream; calls on different
  *    streams that overlap on the GPU race on it.
  *  - Every device-side wait in the kernels is bounded; a wait that runs out
@@ -112,12 +117,14 @@ typedef struct q4_weight q4_weight;
  *   N, K   N >= 1 output rows; K >= 32 and a multiple of 32.
  *   out    receives a new handle (library-owned) on Q4_OK; untouched otherwise.
  * Synchronizes `stream` to report Q4_ERR_NONFINITE / Q4_ERR_RANGE (this is an
- * off-step operation).  The blocks are byte-identical to the canonical rule in
- * the file header. */
+ * off-step operation), and reserves the device scratch of the single-weight
+ * calls on the new weight (Q4_ERR_NOMEM, with no handle, if that fails).  The
+ * blocks are byte-identical to the canonical rule in the file header. */
 Q4_API int q4_quantize(const float* w, int64_t N, int64_t K, q4_weight** out, cudaStream_t stream);
 
 /* Create a handle from canonical blocks in host memory (N*K/32*18 bytes).
- * Rejects blocks whose scale is not finite (Q4_ERR_NONFINITE).  Synchronous. */
+ * Rejects blocks whose scale is not finite (Q4_ERR_NONFINITE).  Synchronous;
+ * reserves scratch as q4_quantize does. */
 Q4_API int q4_import_blocks(const void* host_blocks, int64_t N, int64_t K, q4_weight** out,
                      cudaStream_t stream);
 
@@ -209,11 +216,12 @@ Q4_API int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const fl
 /* y = x @ W^T without allocating any device memory.  (The pages have no
  * counterpart: this is a library concern.)
  *
- * The other compute calls create and grow their scratch with cudaMalloc and
- * cudaFree on the first call that needs more.  Callers that cannot allocate
- * at that moment use this call instead: a serving process that gave all free
- * device memory to its own pool (the allocation would fail), or a step that
- * must not wait for the whole device, as cudaFree does.  Its scratch is one
+ * The other compute calls draw on a library scratch that is reserved with
+ * cudaMalloc when a weight is created and, for grouped and gated calls, grown
+ * (cudaFree, cudaMalloc) on the first call that needs more.  Callers that
+ * cannot allocate at those moments use this call instead: a serving process
+ * that gave all free device memory to its own pool (the allocation would
+ * fail), or a step that must not wait for the whole device, as cudaFree does.  Its scratch is one
  * fixed device array in the library (about 2.5 MB per device, created when the
  * library's device code is loaded), so this call allocates nothing.  (As for
  * any CUDA library, the runtime may still load kernel code on first use.)
@@ -360,6 +368,12 @@ Q4_API int q4mm_set_stall_for_test(int on);
  * Q4_ERR_INVALID_ARG if q4mm_argmax_rows met a row index out of range; or
  * Q4_ERR_CUDA if the device reports an error. */
 Q4_API int q4_device_status(void);
+
+/* Bytes of the library's device scratch on the current device, as now held:
+ * split-K partial sums, the tensor-core activation operand and the grouped or
+ * gated calls' g/u outputs.  All three pointers must be non-null (else
+ * Q4_ERR_INVALID_ARG); zeros before the device's first call.  Host-only. */
+Q4_API int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu);
 
 /* Human-readable name of a status code (static storage). */
 Q4_API const char* q4_status_string(int status);
