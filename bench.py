@@ -43,13 +43,15 @@ BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
 # DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
 # hash of the kernel source it was taken on (null once the kernel changes).
 TRAFFIC = {
-    "source_hash": "c8f84294342e0e47",
+    "source_hash": "c2ebeff34d8cc7a3",
     "grouped": True,
     "m_sweep": [1, 2, 3, 4, 5, 8],
-    "bytes_per_launch": 32945416,  # dram__bytes_read.sum + dram__bytes_write.sum, mean of 96 launches
+    # dram__bytes_read.sum + dram__bytes_write.sum, mean of the step's 96 mma_kernel launches
+    "bytes_per_launch": 32947616,
     "capture": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
-               "--clock-control none -k regex:mma_kernel -s 96 -c 96 python bench.py --layers 4 "
-               "--steps 2 --warmup 3 --no-cpu-baseline --no-configs (one step: 4 layers x 4 calls x 6 M)",
+               "--clock-control none -k regex:\"mma_kernel|xpre_kernel\" -s 120 -c 120 python bench.py "
+               "--layers 4 --steps 2 --warmup 3 --no-cpu-baseline --no-configs (one step: 4 layers x 4 calls "
+               "x 6 M, 96 mma_kernel launches and 24 activation pre-conversion passes)",
 }
 
 
@@ -403,7 +405,7 @@ def run_gpu(args):
     # algorithmic bytes of all calls / event-timed duration of the stack graphs
     tot_bytes = sum(algo_bytes(M, g) for M in msw for g, _ in groups) * layers
     tot_ms = sum(per_stack[M] for M in msw)
-    n_launch = sum(launches[(M, g)] for M in msw for g, _ in groups)
+    n_calls = len(msw) * len(groups)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     traffic = None
     if TRAFFIC and TRAFFIC.get("source_hash") == _kernel_source_hash() and \
@@ -461,9 +463,12 @@ def run_gpu(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "kernel": "q4mm kernels (mma_kernel below the M threshold, xop_kernel + tc_kernel "
-                                   "from it), every launch of one step (%d launches)" % (n_launch * layers),
-                         "algorithmic_bytes_per_launch": tot_bytes / (n_launch * layers),
+                         "kernel": "q4mm kernels (mma_kernel below the M threshold, with the activation "
+                                   "pre-conversion pass of row-group launches of 4-8 rows; xop_kernel + "
+                                   "tc_kernel from the threshold), every "
+                                   "call of one step (%d calls, %d kernel launches)"
+                                   % (n_calls * layers, launches_per_step),
+                         "algorithmic_bytes_per_call": tot_bytes / (n_calls * layers),
                          "algorithmic_bytes_rule": "0.5625*sum(N_i*K) + 4*M*K + 4*M*sum(N_i) per call"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms_per_step"],

@@ -90,7 +90,7 @@ _sig = {
     "q4mm_set_wait_limit_ns": [ctypes.c_uint64],
     "q4mm_set_stall_for_test": [ctypes.c_int],
     "q4_status_string": [ctypes.c_int],
-    "q4_scratch_bytes": [ctypes.POINTER(ctypes.c_size_t)] * 3,
+    "q4_scratch_bytes": [ctypes.POINTER(ctypes.c_size_t)] * 4,
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -450,8 +450,8 @@ def q4_device_status() -> int:
 
 
 def q4_scratch_bytes() -> tuple:
-    """(partial, xop, gu): bytes of the library's scratch now held on the current device."""
-    v = [ctypes.c_size_t(0) for _ in range(3)]
+    """(partial, xop, gu, xpre): bytes of the library's scratch now held on the current device."""
+    v = [ctypes.c_size_t(0) for _ in range(4)]
     _check(_lib.q4_scratch_bytes(*[ctypes.byref(a) for a in v]), "q4_scratch_bytes")
     return tuple(int(a.value) for a in v)
 

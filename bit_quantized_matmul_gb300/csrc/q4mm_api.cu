@@ -173,7 +173,7 @@ int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxv
   if (path == Q4MM_PATH_MMA) {
     const MmaPlan plan = mma_plan(W, ds.num_sms);
     Workspace ws;
-    st = workspace_get(dev, mma_partial_bytes(W, plan, M, inv), 0, &ws);
+    st = workspace_get(dev, mma_partial_bytes(W, plan, M, inv), 0, &ws, 0, mma_xpre_bytes(W->KBP, plan));
     if (st) return st;
     return launch_mma(W, x, M, y, idx, maxval, plan, inv, ws, s);
   }
@@ -197,8 +197,20 @@ int run(const q4_weight* Wh, const float* x, float* y, int32_t* idx, float* maxv
 }  // namespace
 
 // Caller holds g_dev[device].mu.
-int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* out, size_t gu_bytes) {
+int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* out, size_t gu_bytes,
+                  size_t xpre_bytes) {
   DeviceScratch& ds = g_dev[device];
+  if (xpre_bytes > ds.ws.xpre_bytes) {
+    size_t want = xpre_bytes + xpre_bytes / 2;
+    if (ds.ws.xpre) cudaFree(ds.ws.xpre);
+    ds.ws.xpre = nullptr;
+    ds.ws.xpre_bytes = 0;
+    if (cudaMalloc(&ds.ws.xpre, want) != cudaSuccess) {
+      cudaGetLastError();
+      return Q4_ERR_NOMEM;
+    }
+    ds.ws.xpre_bytes = want;
+  }
   if (gu_bytes > ds.ws.gu_bytes) {
     size_t want = gu_bytes + gu_bytes / 2;
     if (ds.ws.gu) cudaFree(ds.ws.gu);
@@ -260,7 +272,7 @@ int workspace_reserve_for(int device, const Weight* W) {
       }
   }
   Workspace ws;
-  return workspace_get(device, partial, xop, &ws);
+  return workspace_get(device, partial, xop, &ws, 0, mma_xpre_bytes(W->KBP, mma_plan(W, ds.num_sms)));
 }
 
 int device_num_sms(int device) { return g_dev[device].num_sms; }
@@ -461,7 +473,7 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
     Workspace ws;
     if (streaming) {
       const MmaPlan plan = mma_plan_tiles(tiles, W[0]->w.KBP, ds.num_sms);
-      st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws);
+      st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws, 0, mma_xpre_bytes(W[0]->w.KBP, plan));
       if (st) return st;
       return launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
     }
@@ -496,7 +508,10 @@ int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x,
   Workspace ws;
   if (streaming && !inv) {
     // fused: the gate and up tiles of a row range in one CTA, h written directly
-    st = workspace_get(dev, 0, 0, &ws);
+    MmaPlan whole;  // one K split: the gated launches cover the whole K
+    whole.splits = 1;
+    whole.kbp_per_split = Wg->w.KBP;
+    st = workspace_get(dev, 0, 0, &ws, 0, mma_xpre_bytes(Wg->w.KBP, whole));
     if (st) return st;
     return launch_mma_gated(&Wg->w, &Wu->w, x, M, h, ws, stream);
   }
@@ -509,7 +524,8 @@ int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x,
   const int64_t tiles = Wg->w.tiles + Wu->w.tiles;
   if (streaming) {
     const MmaPlan plan = mma_plan_tiles(tiles, Wg->w.KBP, ds.num_sms);
-    st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws, 2 * out_bytes);
+    st = workspace_get(dev, mma_partial_bytes_tiles(tiles, plan, M, inv), 0, &ws, 2 * out_bytes,
+                       mma_xpre_bytes(Wg->w.KBP, plan));
     if (st) return st;
     L.y[0] = ws.gu;
     L.y[1] = ws.gu + M * Wg->w.N;
@@ -646,7 +662,7 @@ int q4mm_plan_info(const q4_weight* W, int64_t M, uint32_t flags, int* path, int
     const MmaPlan plan = mma_plan(&W->w, ds.num_sms);
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
     const bool two = mma_two_tiles(plan, W->w.tiles, inv);
-    l = mma_launch_count(M, inv, two);
+    l = mma_call_launches(W->w.tiles, W->w.KBP, W->w.K, plan, M, inv, false);
     const int64_t rows0 = M < mma_rows_per_launch(inv, two) ? M : mma_rows_per_launch(inv, two);  // first launch
     sp = mma_row_groups(plan, W->w.K, inv, false, rows0) ? 1 : plan.splits;
   } else {
@@ -687,8 +703,8 @@ int q4mm_set_stall_for_test(int on) {
   return Q4_OK;
 }
 
-int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu) {
-  if (!partial || !xop || !gu) return Q4_ERR_INVALID_ARG;
+int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu, size_t* xpre) {
+  if (!partial || !xop || !gu || !xpre) return Q4_ERR_INVALID_ARG;
   int dev;
   int st = current_device(&dev);
   if (st) return st;
@@ -697,6 +713,7 @@ int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu) {
   *partial = ds.ws.partial_bytes;
   *xop = ds.ws.xop_bytes;
   *gu = ds.ws.gu_bytes;
+  *xpre = ds.ws.xpre_bytes;
   return Q4_OK;
 }
 

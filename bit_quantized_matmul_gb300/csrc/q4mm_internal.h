@@ -73,6 +73,8 @@ struct Workspace {
   size_t xop_bytes = 0;
   float* gu = nullptr;                 // gate and up outputs of an unfused gated call
   size_t gu_bytes = 0;
+  uint8_t* xpre = nullptr;             // chunk-slot image of the pre-conversion pass
+  size_t xpre_bytes = 0;
 };
 constexpr int MAX_COUNTERS = 1 << 16;
 
@@ -82,7 +84,8 @@ constexpr unsigned STATUS_BAD_ROW = 2u;   // a row index of q4mm_argmax_rows was
 constexpr unsigned STATUS_KV_RANGE = 4u;  // a q4_kv_append request was out of range (not written)
 
 // Returns Q4_OK and fills *ws with at least the requested capacities.
-int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws, size_t gu_bytes = 0);
+int workspace_get(int device, size_t partial_bytes, size_t xop_bytes, Workspace* ws, size_t gu_bytes = 0,
+                  size_t xpre_bytes = 0);
 
 // ---- launchers (return a Q4 status; launch errors map to Q4_ERR_CUDA) ----
 // Quantize fp32 W (device) into canonical blocks in canon_dev, then repack.
@@ -110,6 +113,9 @@ struct MmaLaunch {
   bool gated = false;  // W[0], W[1] = gate, up: y[0] = SiLU(x W0^T) * (x W1^T)
 };
 MmaPlan mma_plan(const Weight* W, int num_sms);
+// Bytes of the pre-conversion image for any launch of this plan (whole K or
+// its K splits); 0 when the pass is built out.
+size_t mma_xpre_bytes(int64_t KBP, const MmaPlan& p);
 // True when a launch of `launch_rows` token rows with this plan uses row-group
 // CTAs (one 32-row group pair of a tile over the whole K, no K split) instead
 // of the split plan: four CTAs per tile fit on the SMs, K is short and the
@@ -124,6 +130,10 @@ MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms);
 size_t mma_partial_bytes(const Weight* W, const MmaPlan& p, int64_t M, bool batch_invariant);
 size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant);
 int mma_launch_count(int64_t M, bool batch_invariant, bool two_tiles);
+// Kernel launches of a streaming call over `tiles` tiles (main launches and
+// their pre-conversion passes), as launch_mma_group makes them.
+int mma_call_launches(int64_t tiles, int64_t KBP, int64_t K, const MmaPlan& plan, int64_t M, bool batch_invariant,
+                      bool greedy_pick);
 int launch_mma(const Weight* W, const float* x, int64_t M, float* y, int32_t* idx, float* maxval,
                const MmaPlan& plan, bool batch_invariant, const Workspace& ws, cudaStream_t s);
 int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx, float* maxval,

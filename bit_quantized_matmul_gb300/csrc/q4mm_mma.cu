@@ -138,6 +138,32 @@ constexpr int CHUNK_K = CHUNK_PAIRS * 64;
 #ifndef Q4MM_TWO_TILES
 #define Q4MM_TWO_TILES 1
 #endif
+// Up-front launches take their activations from a pre-conversion pass (one
+// small kernel converts x once into the chunk-slot image that every CTA
+// copies in) instead of converting the whole x in every CTA, from these row
+// counts on (0: never).  Measured on GB300 over the 7B layer (8 layer copies
+// per graph, us per call, without / with the pass): row-group CTAs q/k/v
+// 7.95 / 6.58 and o 7.84 / 6.34 at M = 8, 5.30 / 5.06 and 5.28 / 5.05 at
+// M = 4, even at M = 3 and slower at M = 2; two-tile CTAs (gate/up) slower at
+// every M (22.04 / 22.30 at M = 8, 15.35 / 16.39 at M = 2); K-split CTAs
+// (down) 17.39 / 17.00 at M = 8, 16.32 / 16.22 at M = 5 and slower at M <= 4,
+// but slower in a batch-invariant M = 124 step (16 launches of 8 rows on one
+// L2-resident weight: 600 / 621 us per layer for gate/up and down), so off.
+#ifndef Q4MM_XPRE_RG_ROWS
+#define Q4MM_XPRE_RG_ROWS 4
+#endif
+#ifndef Q4MM_XPRE_SPLIT_ROWS
+#define Q4MM_XPRE_SPLIT_ROWS 0
+#endif
+#ifndef Q4MM_XPRE_TWO_ROWS
+#define Q4MM_XPRE_TWO_ROWS 0
+#endif
+// and only for activations of at least this many chunks (512 k each): a
+// short K converts quickly in the kernel, and an extra launch costs more
+// (Q4_0 896 x 896, 400 copies per graph: 2.69 / 3.21 us per call at M = 4)
+#ifndef Q4MM_XPRE_MIN_CHUNKS
+#define Q4MM_XPRE_MIN_CHUNKS 4
+#endif
 constexpr int RG_LD = 36;  // row stride of the row-group slice sums (32 rows + 4)
 constexpr int T2_LD = 2 * TILE_N + 4;  // row stride of the two-tile slice sums (256 rows + 4)
 // row stride of the slice sums in shared memory: 4 (mod 32 banks), so that
@@ -174,6 +200,10 @@ struct MmaArgs {
   unsigned long long wait_ns;  // bound of the waits between roles
   int stall;            // test setting: the converters hand over no chunk
   int cluster;          // 1: the K splits of a tile are one thread-block cluster
+  // up-front launches: null, or the chunk-slot image written by the
+  // pre-conversion pass ([split][chunk] slots, xpre_stride bytes per split)
+  const uint8_t* xpre;
+  int64_t xpre_stride;
   EpiArgs e;
 };
 
@@ -225,6 +255,8 @@ struct MmaCfg {
   static constexpr int THREADS = (UP && TPC == 2) ? COMPUTE_THREADS : KERNEL_THREADS;
   static_assert(BYTES <= 227 * 1024 - 1024, "shared memory of one CTA");
   static_assert(SLOT % 16 == 0 && XSLOT % 16 == 0, "16-byte aligned ring slots");
+  static_assert(SIG_OFF == CHUNK_PAIRS * C * 1024 && SLOT == CHUNK_PAIRS * C * 1024 + CHUNK_PAIRS * MAXM * 16,
+                "chunk slot layout of the up-front conversion");
 };
 
 // The four A-fragment registers of one 32-bit fragment word (nibble pairs
@@ -421,6 +453,47 @@ __device__ __forceinline__ void split4(const float4& v, float s, uint32_t (&ta)[
   tb[1] = pack_f16x2(r2, r3);
 }
 
+// Bytes of one chunk slot of C column groups: the B fragments of 8 block
+// pairs, then per (pair, token row) {1/s, 1/s, 1/(16 s), 1/(16 s)}.
+template <int C>
+__host__ __device__ constexpr int chunk_slot_bytes() { return CHUNK_PAIRS * C * 1024 + CHUNK_PAIRS * (C * 8 / TERMS) * 16; }
+
+// Up-front conversion of four activations (k .. k + 3, this thread's) of
+// token row m into chunk slot sb: the largest |x| of the row over the warp's
+// 128 elements (two block pairs) sets the power-of-two scale s, the two
+// binary16 terms go to the row's B columns, and the pair's first thread
+// writes 1/s and 1/(16 s).  sb is shared memory or the global image of the
+// pre-conversion pass: the same operations either way, so the slot bytes are
+// the same.  Every lane of the warp calls it with the same m (the reduction).
+template <int C>
+__device__ __forceinline__ void convert_row4(const float4& v, int m, uint8_t* sb, int kbase, int s2, int oa,
+                                             int ob, int pc, bool sig_lane, bool pair_ok) {
+  constexpr int MAXM = C * 8 / TERMS;
+  constexpr int SIG_OFF = CHUNK_PAIRS * C * 1024;
+  uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u));
+  int e = 14 - ((int)(u >> 23) - 127);
+  e = max(-120, min(120, e));
+  const float sc = __int_as_float((e + 127) << 23);
+  if (pair_ok) {
+    uint32_t ta[TERMS], tb[TERMS];
+    split4(v, sc, ta, tb);
+#pragma unroll
+    for (int t = 0; t < TERMS; ++t) {
+      const int col = TERMS * m + t;
+      const int cg = col >> 3, gl = col & 7;
+      uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
+      *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
+      *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
+    }
+    if (sig_lane) {
+      const float r1 = __int_as_float((127 - e) << 23);
+      const float r16 = __int_as_float((123 - e) << 23);
+      *reinterpret_cast<float4*>(sb + SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Shared-memory B fragments of one block pair: [cg][h][32 slots] x 16 bytes,
 // slot of lane L = 4g + tq at L ^ sw with sw = 4 (pair & 1) + h, so that the
@@ -552,6 +625,22 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
   __syncthreads();
 
   if constexpr (UP) {
+   if (a.xpre != nullptr) {
+    // ---- activations converted by the pre-conversion pass ----
+    // weight pairs first (they never depend on an earlier kernel), then this
+    // split's chunk slots of the image, copied as they are
+    if (compute) {
+#pragma unroll
+      for (int u = 0; u < WD; ++u) fetch();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the image comes from the previous kernel
+    const uint8_t* src = a.xpre + (int64_t)split * a.xpre_stride;
+    const int nbytes = nchunks * S::SLOT;
+    for (int o = tid * 16; o < nbytes; o += NT * 16) cp_async16(smem_u32(smem + o), src + o);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+   } else {
     // ---- every thread: the activations of all chunks, straight from x ----
     // 128 threads per chunk (k = 4ct .. 4ct + 3), five chunk sets; every load
     // is issued before any is used
@@ -610,34 +699,12 @@ __global__ void __launch_bounds__(MmaCfg<C, TPC, RG, UP>::THREADS, 1) mma_kernel
         for (int mm = 0; mm < MG; ++mm) {
           const int m = m0 + mm;
           if (m >= mrows) break;  // the same for every thread of the CTA
-          // largest |x| of row m over the warp's 128 elements (two block pairs)
-          uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(vc[mm].x), fabsf(vc[mm].y)),
-                                             fmaxf(fabsf(vc[mm].z), fabsf(vc[mm].w))));
-          asm volatile("redux.sync.max.u32 %0, %0, 0xffffffff;" : "+r"(u));
-          int e = 14 - ((int)(u >> 23) - 127);
-          e = max(-120, min(120, e));
-          const float sc = __int_as_float((e + 127) << 23);
-          if (pair_ok) {
-            uint32_t ta[TERMS], tb[TERMS];
-            split4(vc[mm], sc, ta, tb);
-#pragma unroll
-            for (int t = 0; t < TERMS; ++t) {
-              const int col = TERMS * m + t;
-              const int cg = col >> 3, gl = col & 7;
-              uint8_t* base = sb + kbase + cg * 1024 + (gl ^ s2) * 64;
-              *reinterpret_cast<uint32_t*>(base + oa) = ta[t];
-              *reinterpret_cast<uint32_t*>(base + ob) = tb[t];
-            }
-            if ((ct & 15) == 0) {
-              const float r1 = __int_as_float((127 - e) << 23);
-              const float r16 = __int_as_float((123 - e) << 23);
-              *reinterpret_cast<float4*>(sb + S::SIG_OFF + (pc * MAXM + m) * 16) = make_float4(r1, r1, r16, r16);
-            }
-          }
+          convert_row4<C>(vc[mm], m, sb, kbase, s2, oa, ob, pc, (ct & 15) == 0, pair_ok);
         }
       }
     }
     __syncthreads();
+   }
   }
 
   // accumulators [tile][rg][cg][row R0 / R1] as {column 2tq, column 2tq + 1}
@@ -1156,10 +1223,100 @@ int cluster_capacity(int device, int size) {
   return n;
 }
 
+// ---- pre-conversion pass ----
+// Converts the activations of one launch once, into the chunk-slot image that
+// the up-front launches copy into shared memory: CTA (c, split) writes chunk c
+// of K split `split`, with the thread mapping and the operations of the
+// up-front conversion (convert_row4), so the image holds the bytes every CTA
+// would otherwise compute for itself.
+struct XpreArgs {
+  const float* x;       // [mrows, K] activations of the launch
+  uint8_t* img;         // [splits][chunks] slots, `stride` bytes per split
+  int64_t K, KBP, kbp_per_split, stride;
+  int mrows;
+};
+
+template <int C>
+__global__ void __launch_bounds__(128) xpre_kernel(const XpreArgs a) {
+  constexpr int MAXM = C * 8 / TERMS;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int ct = threadIdx.x;
+  const int c = blockIdx.x, split = blockIdx.y;
+  const int64_t bp0 = (int64_t)split * a.kbp_per_split;
+  const int64_t bp1 = min(a.KBP, bp0 + a.kbp_per_split);
+  const int npairs = (int)(bp1 - bp0);
+  const int pc = ct >> 4, h = (ct >> 3) & 1, j = (ct >> 1) & 3, tql = 2 * (ct & 1);
+  const int kbase = (pc * C * 2 + h) * 512 + j * 4;
+  const int s2 = pc & 1;
+  const int oa = ((tql) ^ h) * 16, ob = ((tql + 1) ^ h) * 16;
+  const bool pair_ok = c * CHUNK_PAIRS + pc < npairs;
+  const bool k_ok = pair_ok && (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct < a.K;
+  uint8_t* sb = a.img + split * a.stride + (int64_t)c * chunk_slot_bytes<C>();
+  const float* xr = a.x + (bp0 + (int64_t)c * CHUNK_PAIRS) * 64 + 4 * ct;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+  float4 v[MAXM];
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    v[m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (k_ok && m < a.mrows) v[m] = __ldg(reinterpret_cast<const float4*>(xr + (int64_t)m * a.K));
+  }
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    if (m >= a.mrows) break;  // the same for every thread
+    convert_row4<C>(v[m], m, sb, kbase, s2, oa, ob, pc, (ct & 15) == 0, pair_ok);
+  }
+}
+
+// The image of a launch of `splits` K splits of `kbp` block pairs each.
+int64_t xpre_split_bytes(int64_t kbp, int C) {
+  const int64_t chunks = (kbp + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
+  return chunks * (C == 1 ? chunk_slot_bytes<1>() : chunk_slot_bytes<2>());
+}
+
+int launch_xpre(int C, const float* x, int mrows, int64_t K, int64_t KBP, int64_t kbp, int splits, uint8_t* img,
+                cudaStream_t s) {
+  XpreArgs a;
+  a.x = x;
+  a.img = img;
+  a.K = K;
+  a.KBP = KBP;
+  a.kbp_per_split = kbp;
+  a.stride = xpre_split_bytes(kbp, C);
+  a.mrows = mrows;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((kbp + CHUNK_PAIRS - 1) / CHUNK_PAIRS), (unsigned)splits, 1);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = C == 1 ? cudaLaunchKernelEx(&cfg, xpre_kernel<1>, a) : cudaLaunchKernelEx(&cfg, xpre_kernel<2>, a);
+  return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+// True when a launch of `mrows` token rows takes its activations from the
+// pre-conversion pass (given scratch for the image): an up-front launch of
+// one or two column groups reading x in row order, with at least the rows
+// set for its kind.  rg / two: row-group or two-tile CTAs (whole K).
+bool takes_xpre(int64_t KBP, const MmaPlan& plan, bool rg, bool two, int mrows, bool row_list) {
+  const int cgs = (TERMS * mrows + 7) / 8;
+  const int64_t chunks_split = (plan.kbp_per_split + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
+  const int64_t chunks_all = (KBP + CHUNK_PAIRS - 1) / CHUNK_PAIRS;
+  if (!Q4MM_UPFRONT || cgs > 2 || row_list) return false;
+  const int from = rg ? Q4MM_XPRE_RG_ROWS : (two ? Q4MM_XPRE_TWO_ROWS : Q4MM_XPRE_SPLIT_ROWS);
+  const bool up = rg ? chunks_all <= UP_CHUNKS
+                     : (two ? (Q4MM_UP_TWO && chunks_all <= UP_CHUNKS) : chunks_split <= UP_CHUNKS);
+  const int64_t chunks = (rg || two) ? chunks_all : chunks_split;
+  return up && from > 0 && mrows >= from && chunks >= Q4MM_XPRE_MIN_CHUNKS;
+}
+
 template <int C, bool RG, int TPC = 1, bool UP = false>
 int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float* maxval,
              const MmaPlan& plan, const Workspace& ws, int64_t mb, cudaStream_t s,
-             const int32_t* xrows, int64_t x_rows) {
+             const int32_t* xrows, int64_t x_rows, const uint8_t* xpre = nullptr, int64_t xpre_stride = 0) {
   using S = MmaCfg<C, TPC, RG, UP>;
   const Weight* W0 = L.W[0];
   MmaArgs a;
@@ -1187,6 +1344,8 @@ int launch_c(const MmaLaunch& L, const float* x, int mrows, int32_t* idx, float*
   a.mrows = mrows;
   a.kbp_per_split = RG ? W0->KBP : plan.kbp_per_split;
   a.gated = L.gated ? (int)L.W[0]->tiles : 0;
+  a.xpre = UP ? xpre : nullptr;
+  a.xpre_stride = xpre_stride;
   a.status = ws.status;
   a.wait_ns = wait_limit_ns();
   a.stall = stall_for_test();
@@ -1273,6 +1432,13 @@ MmaPlan mma_plan_tiles(int64_t tiles, int64_t KBP, int num_sms) {
 
 MmaPlan mma_plan(const Weight* W, int num_sms) { return mma_plan_tiles(W->tiles, W->KBP, num_sms); }
 
+size_t mma_xpre_bytes(int64_t KBP, const MmaPlan& p) {
+  if (Q4MM_XPRE_RG_ROWS <= 0 && Q4MM_XPRE_SPLIT_ROWS <= 0 && Q4MM_XPRE_TWO_ROWS <= 0) return 0;
+  const int64_t whole = xpre_split_bytes(KBP, 2);
+  const int64_t split = (int64_t)p.splits * xpre_split_bytes(p.kbp_per_split, 2);
+  return (size_t)(whole > split ? whole : split);
+}
+
 size_t mma_partial_bytes_tiles(int64_t tiles, const MmaPlan& p, int64_t M, bool batch_invariant) {
   if (p.splits <= 1) return 0;
   const int64_t rpl = rows_per_launch(batch_invariant);
@@ -1289,6 +1455,19 @@ bool mma_two_tiles(const MmaPlan& plan, int64_t tiles, bool) {
 }
 
 int mma_rows_per_launch(bool batch_invariant, bool two_tiles) { return rows_per_launch(batch_invariant, two_tiles); }
+
+int mma_call_launches(int64_t tiles, int64_t KBP, int64_t K, const MmaPlan& plan, int64_t M, bool batch_invariant,
+                      bool greedy_pick) {
+  const bool two = mma_two_tiles(plan, tiles, batch_invariant);
+  const int64_t rpl = rows_per_launch(batch_invariant, two);
+  int n = 0;
+  for (int64_t mb = 0; mb < M; mb += rpl) {
+    const int mrows = (int)((M - mb) < rpl ? (M - mb) : rpl);
+    const bool rg = mma_row_groups(plan, K, batch_invariant, greedy_pick, mrows);
+    n += 1 + (takes_xpre(KBP, plan, rg, two, mrows, false) ? 1 : 0);
+  }
+  return n;
+}
 
 int mma_launch_count(int64_t M, bool batch_invariant, bool two_tiles) {
   const int64_t rpl = rows_per_launch(batch_invariant, two_tiles);
@@ -1340,25 +1519,41 @@ int launch_mma_group(const MmaLaunch& L, const float* x, int64_t M, int32_t* idx
     // column only, and a column's scaling, slice and split sums are the same
     // operations in the same order whatever the column count
     const int cgs = (TERMS * mrows + 7) / 8;  // column groups of this launch
+    // up-front launches take their activations from the pre-conversion pass
+    // (takes_xpre) when the scratch holds its image; the slot bytes are the
+    // same either way
+    const uint8_t* xp = nullptr;
+    int64_t xstride = 0;
+    if (takes_xpre(L.W[0]->KBP, plan, rg, two, mrows, xrows != nullptr) && ws.xpre != nullptr) {
+      const int64_t kbp = (rg || two) ? L.W[0]->KBP : plan.kbp_per_split;
+      const int sp = (rg || two) ? 1 : plan.splits;
+      const int64_t stride = xpre_split_bytes(kbp, cgs);
+      if ((size_t)(stride * sp) <= ws.xpre_bytes) {
+        st = launch_xpre(cgs, xs, mrows, K, L.W[0]->KBP, kbp, sp, ws.xpre, s);
+        if (st) return st;
+        xp = ws.xpre;
+        xstride = stride;
+      }
+    }
     if (cgs >= 3) {  // 9 to 16 rows: one row group per warp, K splits
       st = cgs == 3 ? launch_c<3, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
                     : launch_c<4, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     } else if (rg) {
-      if (up_rg) st = cgs == 1 ? launch_c<1, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                               : launch_c<2, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
-      else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                         : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+      if (up_rg) st = cgs == 1 ? launch_c<1, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride)
+                               : launch_c<2, true, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride);
+      else st = cgs == 1 ? launch_c<1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride)
+                         : launch_c<2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride);
     } else if (two) {
       if (Q4MM_UP_TWO && up_two)
-        st = cgs == 1 ? launch_c<1, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                      : launch_c<2, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        st = cgs == 1 ? launch_c<1, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride)
+                      : launch_c<2, false, 2, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride);
       else
         st = cgs == 1 ? launch_c<1, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
                       : launch_c<2, false, 2>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
     } else {
       if (up_split)
-        st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
-                      : launch_c<2, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
+        st = cgs == 1 ? launch_c<1, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride)
+                      : launch_c<2, false, 1, true>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows, xp, xstride);
       else
         st = cgs == 1 ? launch_c<1, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows)
                       : launch_c<2, false>(L, xs, mrows, idx, maxval, plan, ws, mb, s, xr, x_rows);
@@ -1386,8 +1581,19 @@ int launch_mma_gated(const Weight* Wg, const Weight* Wu, const float* x, int64_t
   for (int64_t mb = 0; mb < M; mb += 8) {
     const int mrows = (int)((M - mb) < 8 ? (M - mb) : 8);
     const float* xs = x + mb * Wg->K;
-    const int st = mrows <= 4 ? launch_c<1, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0)
-                              : launch_c<2, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0);
+    const int cgs = mrows <= 4 ? 1 : 2;
+    const uint8_t* xp = nullptr;
+    int64_t xstride = 0;
+    if (takes_xpre(Wg->KBP, plan, false, true, mrows, false) && ws.xpre != nullptr &&
+        (size_t)xpre_split_bytes(Wg->KBP, cgs) <= ws.xpre_bytes) {
+      const int st = launch_xpre(cgs, xs, mrows, Wg->K, Wg->KBP, Wg->KBP, 1, ws.xpre, s);
+      if (st) return st;
+      xp = ws.xpre;
+      xstride = xpre_split_bytes(Wg->KBP, cgs);
+    }
+    const int st = cgs == 1
+        ? launch_c<1, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0, xp, xstride)
+        : launch_c<2, false, 2, true>(L, xs, mrows, nullptr, nullptr, plan, ws, mb, s, nullptr, 0, xp, xstride);
     if (st) return st;
   }
   return Q4_OK;

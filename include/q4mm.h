@@ -320,7 +320,9 @@ Q4_API int q4mm_select_path(const q4_weight* W, int64_t M, uint32_t flags);
 
 /* Plan of a call with these arguments, without running it: *path receives
  * the Q4MM_PATH_* value, *launches the number of kernel launches the call
- * makes, *splits the K partition count of the first launch of a
+ * makes (on the streaming path including the passes that convert the
+ * activations of a launch once for all its CTAs), *splits the K partition
+ * count of the first launch of a
  * q4mm_forward_ex call (1 when the streaming kernel gives each CTA one 32-row
  * group pair over the whole K, which it does for launches of up to 8 rows).
  * Any output pointer may be NULL. */
@@ -370,10 +372,11 @@ Q4_API int q4mm_set_stall_for_test(int on);
 Q4_API int q4_device_status(void);
 
 /* Bytes of the library's device scratch on the current device, as now held:
- * split-K partial sums, the tensor-core activation operand and the grouped or
- * gated calls' g/u outputs.  All three pointers must be non-null (else
- * Q4_ERR_INVALID_ARG); zeros before the device's first call.  Host-only. */
-Q4_API int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu);
+ * split-K partial sums, the tensor-core activation operand, the grouped or
+ * gated calls' g/u outputs and the streaming kernel's pre-converted
+ * activations.  All four pointers must be non-null (else Q4_ERR_INVALID_ARG);
+ * zeros before the device's first call.  Host-only. */
+Q4_API int q4_scratch_bytes(size_t* partial, size_t* xop, size_t* gu, size_t* xpre);
 
 /* Human-readable name of a status code (static storage). */
 Q4_API const char* q4_status_string(int status);

@@ -46,13 +46,18 @@ def _partial_need(W, M):
 
 
 # (N, K, token-row counts): ragged tiles, a many-way K split with launches
-# of 16 + ... rows, the largest scratch of a 7B layer (q_proj at M >= 16), and a
-# one-split shape.
+# of 16 + ... rows, the largest scratch of a 7B layer (q_proj at M >= 16), a
+# one-split shape and a 7B down projection (five K splits).  The ordinary
+# entry point converts the activations of row-group launches of 4 to 8 rows
+# in a separate pre-conversion pass; this entry point converts them inside
+# the kernel, so the bit-for-bit check below also pins that the pass writes
+# the same bytes.
 CASES = [
     (300, 1024, (1, 5, 17)),
-    (512, 3584, (1, 4, 16, 40)),
+    (512, 3584, (1, 4, 8, 16, 40)),
     (3584, 3584, (16,)),
     (18944, 3584, (3,)),
+    (3584, 18944, (5, 8)),
 ]
 
 
@@ -81,6 +86,21 @@ def test_noalloc_matches_existing_entry_point_twice(N, K, Ms):
             assert np.all(np.abs(got.astype(np.float64) - ref_fwd) <= 2 * bound), what
             assert np.array_equal(got.view(np.uint32), ref_mma.view(np.uint32)), what
     W.free()
+
+
+def test_pre_conversion_pass_is_launched():
+    # a 152-SM device: 512 x 3584 runs as row-group CTAs up to 8 rows (the
+    # pass from 4 rows adds one launch per main launch), 3584 x 18944 as five
+    # K splits (no pass)
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("launch plan measured for 152 SMs")
+    for (N, K), with_pass, without in (((512, 3584), (4, 8), (1, 3)), ((3584, 18944), (), (1, 5, 8))):
+        W, _ = _setup(N, K, 94, 0)
+        for M in with_pass:
+            assert q4.q4mm_plan_info(W, M, q4.Q4MM_FORCE_MMA)[1] == 2, (N, K, M)
+        for M in without:
+            assert q4.q4mm_plan_info(W, M, q4.Q4MM_FORCE_MMA)[1] == 1, (N, K, M)
+        W.free()
 
 
 def test_noalloc_allocates_no_device_memory():
