@@ -662,20 +662,29 @@ def extra_configs(q4, torch, dev, stack, stream, args, with_oracle):
     wb3 = sum(synthetic.QWEN7B_LINEARS[n][0] * synthetic.QWEN7B_LINEARS[n][1]
               for n in ("gate_proj", "up_proj", "down_proj")) * BLOCK_BYTES_PER_WEIGHT
     c3 = {}
-    for mode, fl in (("default", 0), ("batch_invariant", q4.Q4MM_BATCH_INVARIANT)):
-        def issue():
-            for l in range(L3):
-                q4.q4mm_forward_group([stack["gate_proj"][l], stack["up_proj"][l]], x1, ys=[yg, yu], flags=fl,
-                                      stream=stream)
-                q4.q4mm_forward_ex(stack["down_proj"][l], x2, fl, y=yd, stream=stream)
-        us = _graph_us(torch, stream, issue, reps, L3)
-        _, lg, _ = q4.q4mm_plan_info(stack["gate_proj"][0], M, fl)
-        _, ld, _ = q4.q4mm_plan_info(stack["down_proj"][0], M, fl)
-        c3[mode] = {"us_per_layer": us, "weight_gbs": wb3 / us / 1e3, "token_rows_per_s": M / us * 1e6,
-                    "launches_gate_up_down": [lg, ld]}
+    decode = {}
+    inv_tc = q4.Q4MM_BATCH_INVARIANT | q4.Q4MM_FORCE_TC
+    for mode, fl in (("default", 0), ("batch_invariant", q4.Q4MM_BATCH_INVARIANT),
+                     ("batch_invariant_tc", inv_tc)):
+        for rows, res in ((M, c3), (1, decode)):
+            def issue():
+                for l in range(L3):
+                    q4.q4mm_forward_group([stack["gate_proj"][l], stack["up_proj"][l]], x1[:rows],
+                                          ys=[yg[:rows], yu[:rows]], flags=fl, stream=stream)
+                    q4.q4mm_forward_ex(stack["down_proj"][l], x2[:rows], fl, y=yd[:rows], stream=stream)
+            us = _graph_us(torch, stream, issue, reps, L3)
+            _, lg, _ = q4.q4mm_plan_info(stack["gate_proj"][0], rows, fl)
+            _, ld, _ = q4.q4mm_plan_info(stack["down_proj"][0], rows, fl)
+            res[mode] = {"us_per_layer": us, "weight_gbs": wb3 / us / 1e3, "token_rows_per_s": rows / us * 1e6,
+                         "launches_gate_up_down": [lg, ld]}
     c3["batch_invariant_over_default"] = c3["batch_invariant"]["us_per_layer"] / c3["default"]["us_per_layer"]
+    c3["batch_invariant_tc_over_default"] = \
+        c3["batch_invariant_tc"]["us_per_layer"] / c3["default"]["us_per_layer"]
     out["c3_mixed_m124"] = {"workload": "M = 124 (120 prefill + 4 verify rows) through gate/up (one grouped call) "
-                                        "and down, %d layers of the 7B stack in one CUDA graph" % L3, "modes": c3}
+                                        "and down, %d layers of the 7B stack in one CUDA graph; the same layers "
+                                        "at M = 1 in each mode (decode_m1)" % L3,
+                            "modes": c3, "decode_m1": decode,
+                            "launches": "q4mm_plan_info of gate_proj and down_proj alone"}
 
     # ---- LM head, fused greedy pick
     out["c4_lm_head"] = lm_head_cases(q4, torch, dev, stream, reps)

@@ -439,7 +439,8 @@ int q4mm_forward_ex(const q4_weight* W, const float* x, float* y, int64_t M, uin
 int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, float* const* y,
                        int64_t M, uint32_t flags, cudaStream_t stream) {
   if (!W || !x || !y || count < 1 || count > Q4MM_GROUP_MAX) return Q4_ERR_INVALID_ARG;
-  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA)) return Q4_ERR_INVALID_ARG;
+  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA | Q4MM_FORCE_TC)) return Q4_ERR_INVALID_ARG;
+  if ((flags & Q4MM_FORCE_MMA) && (flags & Q4MM_FORCE_TC)) return Q4_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     if (!W[i] || !y[i]) return Q4_ERR_INVALID_ARG;
     if (W[i]->w.K != W[0]->w.K || W[i]->w.device != W[0]->w.device) return Q4_ERR_INVALID_ARG;
@@ -460,8 +461,10 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
     st = init_device_locked(dev, ds);
     if (st) return st;
     const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
-    const bool streaming = (flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 ||
-                           !tc_supported(ds) || M < g_group_m_threshold.load();
+    const bool force_tc = (flags & Q4MM_FORCE_TC) != 0;
+    if (force_tc && !tc_supported(ds)) return Q4_ERR_UNSUPPORTED;
+    const bool streaming = !force_tc && ((flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 ||
+                                         !tc_supported(ds) || M < g_group_m_threshold.load());
     MmaLaunch L;
     L.count = count;
     int64_t tiles = 0;
@@ -477,8 +480,9 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
       if (st) return st;
       return launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
     }
-    // tensor-core path: one launch pair over the tiles of the whole group
-    const TcPlan plan = tc_plan_tiles(tiles, W[0]->w.KBP, M, ds.num_sms, false);
+    // tensor-core path: one launch pair over the tiles of the whole group (in
+    // batch-invariant mode with the plan of one token tile, as single calls)
+    const TcPlan plan = tc_plan_tiles(tiles, W[0]->w.KBP, M, ds.num_sms, inv);
     st = workspace_get(dev, tc_partial_bytes_tiles(tiles, plan, M), tc_xop_bytes_kbp(W[0]->w.KBP, plan, M), &ws);
     if (st) return st;
     return launch_tc_group(L, x, M, nullptr, nullptr, plan, ws, stream);
@@ -488,7 +492,8 @@ int q4mm_forward_group(const q4_weight* const* W, int count, const float* x, flo
 int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x, float* h, int64_t M,
                        uint32_t flags, cudaStream_t stream) {
   if (!Wg || !Wu || !x || !h) return Q4_ERR_INVALID_ARG;
-  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA)) return Q4_ERR_INVALID_ARG;
+  if (flags & ~(Q4MM_BATCH_INVARIANT | Q4MM_FORCE_MMA | Q4MM_FORCE_TC)) return Q4_ERR_INVALID_ARG;
+  if ((flags & Q4MM_FORCE_MMA) && (flags & Q4MM_FORCE_TC)) return Q4_ERR_INVALID_ARG;
   if (Wg->w.N != Wu->w.N || Wg->w.K != Wu->w.K || Wg->w.device != Wu->w.device) return Q4_ERR_INVALID_ARG;
   if (M < 0) return Q4_ERR_INVALID_ARG;
   if (M > Q4MM_M_MAX) return Q4_ERR_SHAPE;
@@ -503,8 +508,10 @@ int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x,
   st = init_device_locked(dev, ds);
   if (st) return st;
   const bool inv = (flags & Q4MM_BATCH_INVARIANT) != 0;
-  const bool streaming = (flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 || !tc_supported(ds) ||
-                         M < g_group_m_threshold.load();
+  const bool force_tc = (flags & Q4MM_FORCE_TC) != 0;
+  if (force_tc && !tc_supported(ds)) return Q4_ERR_UNSUPPORTED;
+  const bool streaming = !force_tc && ((flags & (Q4MM_FORCE_MMA | Q4MM_BATCH_INVARIANT)) != 0 ||
+                                       !tc_supported(ds) || M < g_group_m_threshold.load());
   Workspace ws;
   if (streaming && !inv) {
     // fused: the gate and up tiles of a row range in one CTA, h written directly
@@ -531,7 +538,7 @@ int q4mm_forward_gated(const q4_weight* Wg, const q4_weight* Wu, const float* x,
     L.y[1] = ws.gu + M * Wg->w.N;
     st = launch_mma_group(L, x, M, nullptr, nullptr, plan, inv, ws, stream);
   } else {
-    const TcPlan plan = tc_plan_tiles(tiles, Wg->w.KBP, M, ds.num_sms, false);
+    const TcPlan plan = tc_plan_tiles(tiles, Wg->w.KBP, M, ds.num_sms, inv);
     st = workspace_get(dev, tc_partial_bytes_tiles(tiles, plan, M), tc_xop_bytes_kbp(Wg->w.KBP, plan, M), &ws,
                        2 * out_bytes);
     if (st) return st;

@@ -746,8 +746,16 @@ constexpr int64_t TC_M_LAUNCH = 256;  // rows per launch pair (pre-pass + main)
 // MMA N (3 x token rows per CTA) for a launch of ml rows: as few token tiles
 // as the largest N (80 rows) needs, each as small as that count allows.
 // Forced with the batch-invariant flag: always NB = 96, independent of M.
+// Batch-invariant mode: one token tile of 64 rows (B rows = 3 terms x 64) for
+// every M.  Measured on GB300 (gate/up group + down of a 7B layer, 8 layers
+// per graph, us per layer at M = 1 / 32 / 124; the default mode 27.5 / 109.5 /
+// 250.3): 32-row tiles 105.3 / 109.5 / 402.5, 48 rows 106.1 / 110.1 / 318.9,
+// 64 rows 123.3 / 128.1 / 250.1, 80 rows 166.8 / 170.8 / 347.1.
+#ifndef Q4MM_TC_BI_NB
+#define Q4MM_TC_BI_NB 192
+#endif
 int nb_for(int64_t ml, bool batch_invariant) {
-  if (batch_invariant) return 96;
+  if (batch_invariant) return Q4MM_TC_BI_NB;
   const int64_t passes = (ml + 79) / 80;
   const int64_t r = (ml + passes - 1) / passes;
   if (r <= 16) return 48;
@@ -860,7 +868,7 @@ TcPlan tc_plan_tiles(int64_t wtiles, int64_t KBP, int64_t M, int num_sms, bool b
   const int64_t mtiles = (ml + p.m_tile / 3 - 1) / (p.m_tile / 3);
   // K partition: fill the SMs, balancing waves against units per CTA (+ a
   // fixed per-CTA cost in unit terms).  It depends on M through the token
-  // tiles, except in batch-invariant mode (one token tile of 32 rows assumed).
+  // tiles, except in batch-invariant mode (one token tile assumed).
   const int64_t tiles = wtiles * (batch_invariant ? 1 : mtiles);
   // at least 16 blocks (four units) per split: the split-K epilogue runs once
   // per 16 token rows of every CTA, so very short K ranges cost more than

@@ -89,7 +89,13 @@ extern "C" {
  * with the CTA layout and the K partition fixed per weight shape; a row's
  * operations do not depend on the MMA column it occupies (§"The Other Request
  * Already Finished": a 120-prefill + 4-verify batch crossed the kernel-switch
- * threshold and changed the cached numbers). */
+ * threshold and changed the cached numbers).
+ * With Q4MM_FORCE_TC as well, the calls run the tensor-core kernel for every
+ * M instead, with one instruction shape (token tiles of 64 rows) and a K
+ * partition fixed per weight shape: rows are again bit-identical whatever M
+ * is (but not equal to the streaming mode's), large batches read the weights
+ * once per 256 rows instead of once per 8, and small ones pay the tensor-core
+ * kernel's fixed cost. */
 #define Q4MM_BATCH_INVARIANT 0x1u
 /* Force the CUDA-core streaming kernel (no tensor cores). */
 #define Q4MM_FORCE_SIMT 0x2u
@@ -176,7 +182,9 @@ Q4_API int q4mm_argmax_ex(const q4_weight* W, const float* x, int32_t* idx, floa
  *   x       device, fp32 [M, K] row-major, 16-byte aligned.
  *   y       host array of `count` device pointers, y[i] fp32 [M, N_i],
  *           16-byte aligned, fully overwritten; distinct, non-overlapping.
- *   flags   0, Q4MM_FORCE_MMA or Q4MM_BATCH_INVARIANT (others: INVALID_ARG).
+ *   flags   0, Q4MM_FORCE_MMA, Q4MM_FORCE_TC and/or Q4MM_BATCH_INVARIANT
+ *           (others, or FORCE_MMA with FORCE_TC: INVALID_ARG; FORCE_TC off
+ *           sm_103: UNSUPPORTED).
  * Each y_i is within the q4mm_forward tolerance.  The K partition depends on
  * the group's shapes (not on M), so in batch-invariant mode row r of every y_i
  * is bit-identical whatever M is; it may differ in the last bits from a
@@ -201,7 +209,7 @@ Q4_API int q4mm_forward_group(const q4_weight* const* W, int count, const float*
  * and u never reach memory.  On the tensor-core path and in batch-invariant
  * mode the grouped call writes g and u to library scratch and one elementwise
  * pass forms h.
- *   flags   0, Q4MM_FORCE_MMA or Q4MM_BATCH_INVARIANT (others: INVALID_ARG).
+ *   flags   as for q4mm_forward_group.
  * Each element is within the gate and up tolerances propagated through SiLU
  * (SiLU is 1.1-Lipschitz) plus fp32 rounding; in batch-invariant mode row r
  * of h is bit-identical whatever M is.  The streaming path takes up to 8

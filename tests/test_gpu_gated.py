@@ -62,11 +62,15 @@ def test_gated_small_shapes_full_elementwise(q4, N, K, Ms):
         xd = torch.from_numpy(x).to(DEV)
         _, g64, bg = oracle.matmul(bg_blocks, x)
         _, u64, bu = oracle.matmul(bu_blocks, x)
-        for flags in (0, q4.Q4MM_BATCH_INVARIANT, q4.Q4MM_FORCE_MMA):
+        inv_tc = q4.Q4MM_BATCH_INVARIANT | q4.Q4MM_FORCE_TC
+        for flags in (0, q4.Q4MM_BATCH_INVARIANT, q4.Q4MM_FORCE_MMA, inv_tc):
             h = q4.q4mm_forward_gated(Wg, Wu, xd, flags=flags).cpu().numpy()
             _check_h(h, g64, bg, u64, bu, "N=%d M=%d flags=%d" % (N, M, flags))
-            if flags == q4.Q4MM_BATCH_INVARIANT:  # the same grouped call, then SiLU * up
+            if flags in (q4.Q4MM_BATCH_INVARIANT, inv_tc):  # the same grouped call, then SiLU * up
                 _check_against_group(q4, Wg, Wu, xd, h, flags)
+                if M > 1:  # and row 1 alone gives the same bits
+                    h1 = q4.q4mm_forward_gated(Wg, Wu, xd[1:2].contiguous(), flags=flags).cpu().numpy()
+                    assert np.array_equal(h1[0].view(np.uint32), h[1].view(np.uint32)), (M, flags)
     assert q4.q4_device_status() == q4.Q4_OK
     Wg.free()
     Wu.free()
@@ -119,8 +123,10 @@ def test_gated_argument_errors(q4):
     lib = q4.raw_library()
     s = torch.cuda.current_stream().cuda_stream
     assert lib.q4mm_forward_gated(Wg.handle, Wo.handle, x.data_ptr(), h.data_ptr(), 4, 0, s) == q4.Q4_ERR_INVALID_ARG
-    assert lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr(), h.data_ptr(), 4, q4.Q4MM_FORCE_TC, s) == \
+    assert lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr(), h.data_ptr(), 4, q4.Q4MM_FORCE_SIMT, s) == \
         q4.Q4_ERR_INVALID_ARG
+    assert lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr(), h.data_ptr(), 4,
+                                  q4.Q4MM_FORCE_TC | q4.Q4MM_FORCE_MMA, s) == q4.Q4_ERR_INVALID_ARG
     assert lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr() + 4, h.data_ptr(), 4, 0, s) == q4.Q4_ERR_ALIGN
     assert lib.q4mm_forward_gated(Wg.handle, Wu.handle, x.data_ptr(), h.data_ptr(), 0, 0, s) == q4.Q4_OK
     for W in (Wg, Wu, Wo):

@@ -51,15 +51,23 @@ def test_group_of_one_equals_single_call():
     Ws[0].free()
 
 
-def test_group_batch_invariant_rows():
-    Ws, _ = _group([(3584, 3584), (512, 3584), (512, 3584)], 97)
-    inv = q4.Q4MM_BATCH_INVARIANT
-    big = torch.from_numpy(acts(97, 7, 3584)).cuda()
-    y7 = q4.q4mm_forward_group(Ws, big, flags=inv)
-    for r in (0, 3, 6):
+@pytest.mark.parametrize("force_tc", [False, True])
+def test_group_batch_invariant_rows(force_tc):
+    Ws, blocks = _group([(3584, 3584), (512, 3584), (512, 3584)], 97)
+    inv = q4.Q4MM_BATCH_INVARIANT | (q4.Q4MM_FORCE_TC if force_tc else 0)
+    x_np = acts(97, 40, 3584)
+    big = torch.from_numpy(x_np).cuda()
+    y40 = q4.q4mm_forward_group(Ws, big, flags=inv)
+    y7 = q4.q4mm_forward_group(Ws, big[:7].contiguous(), flags=inv)
+    for r in (0, 3, 6, 33, 39):
         y1 = q4.q4mm_forward_group(Ws, big[r:r + 1].contiguous(), flags=inv)
-        for a, b in zip(y7, y1):
+        for a, b in zip(y40, y1):
             assert torch.equal(a[r].view(torch.int32), b[0].view(torch.int32)), r
+    for a, b in zip(y40, y7):
+        assert torch.equal(a[:7].view(torch.int32), b.view(torch.int32))
+    for y, b in zip(y40, blocks):
+        _, y64, bound = oracle.matmul(b, x_np)
+        assert_within_bound(y.cpu().numpy(), y64, bound, "group invariant tc=%s" % force_tc)
     for W in Ws:
         W.free()
 
@@ -113,6 +121,7 @@ def test_group_argument_errors():
     assert call(hs, [ps[0], None]) == q4.Q4_ERR_INVALID_ARG                 # null output
     assert call(hs, [ps[0], ps[1] + 4]) == q4.Q4_ERR_ALIGN
     assert call(hs, ps, flags=q4.Q4MM_FORCE_SIMT) == q4.Q4_ERR_INVALID_ARG
+    assert call(hs, ps, flags=q4.Q4MM_FORCE_TC | q4.Q4MM_FORCE_MMA) == q4.Q4_ERR_INVALID_ARG
     assert call(hs, ps, M=q4.Q4MM_M_MAX + 1) == q4.Q4_ERR_SHAPE
     assert call(hs, ps, M=0) == q4.Q4_OK
     torch.cuda.synchronize()

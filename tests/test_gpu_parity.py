@@ -173,11 +173,15 @@ def test_special_inputs(q4):
 
 # ------------------------------------------------------------------ batch invariance
 
+# streaming: Q4MM_BATCH_INVARIANT alone; tensor_core: with Q4MM_FORCE_TC (one
+# instruction shape and K partition for every M, 64 token rows per tile, so
+# the 124 rows run as two tiles and a single row as one)
+@pytest.mark.parametrize("mode", ["streaming", "tensor_core"])
 @pytest.mark.parametrize("N,K", [(300, 1024), (260, 3584)])
-def test_batch_invariant_rows_bit_identical(q4, N, K):
+def test_batch_invariant_rows_bit_identical(q4, N, K, mode):
     w = weights(54, 0, N, K)
     W = q4.q4_quantize(torch.from_numpy(w).to(DEV))
-    inv = q4.Q4MM_BATCH_INVARIANT
+    inv = q4.Q4MM_BATCH_INVARIANT | (q4.Q4MM_FORCE_TC if mode == "tensor_core" else 0)
     big = acts(54, 124, K)
     xb = torch.from_numpy(big).to(DEV)
     y124 = q4.q4mm_forward_ex(W, xb, inv).cpu().numpy()
@@ -191,6 +195,9 @@ def test_batch_invariant_rows_bit_identical(q4, N, K):
     other[17] = big[17]
     y_other = q4.q4mm_forward_ex(W, torch.from_numpy(other).to(DEV), inv).cpu().numpy()
     assert np.array_equal(y_other[17].view(np.uint32), y124[17].view(np.uint32))
+    # every row is also within the oracle's bound
+    _, y64, bound = oracle.matmul(oracle.quantize(w), big)
+    assert_within_bound(y124, y64, bound, "%s invariant M=124" % mode)
     W.free()
 
 
