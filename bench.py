@@ -43,11 +43,11 @@ BLOCK_BYTES_PER_WEIGHT = 18.0 / 32.0
 # DRAM traffic of the dominant kernel from one ncu capture, per launch, with the
 # hash of the kernel source it was taken on (null once the kernel changes).
 TRAFFIC = {
-    "source_hash": "c2ebeff34d8cc7a3",
+    "source_hash": "a66b813a87e0b4b9",
     "grouped": True,
     "m_sweep": [1, 2, 3, 4, 5, 8],
     # dram__bytes_read.sum + dram__bytes_write.sum, mean of the step's 96 mma_kernel launches
-    "bytes_per_launch": 32947616,
+    "bytes_per_launch": 32947672,
     "capture": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                "--clock-control none -k regex:\"mma_kernel|xpre_kernel\" -s 120 -c 120 python bench.py "
                "--layers 4 --steps 2 --warmup 3 --no-cpu-baseline --no-configs (one step: 4 layers x 4 calls "

@@ -250,9 +250,13 @@ struct MmaCfg {
   static constexpr int BYTES = BAR_OFF + 2 * NSLOT * 8;
   static_assert(!R1 || TPC == 1, "one row group per warp: one tile per CTA");
   static_assert(!UP || C <= 2, "up-front conversion: one or two column groups");
-  // threads: two-tile CTAs that convert up front need no converter warps
-  // (and get the register file of 512 threads: 128 registers each)
-  static constexpr int THREADS = (UP && TPC == 2) ? COMPUTE_THREADS : KERNEL_THREADS;
+  // threads: CTAs that convert up front need no converter warps and get the
+  // register file of 512 threads (128 registers each, where 640 threads get
+  // 96), except row-group CTAs of two column groups.  Measured on GB300 over
+  // the 7B layer (us per call, 640 / 512 threads): down 12.11 / 11.73 at M = 1,
+  // 17.41 / 16.81 at M = 8; o 4.20 / 4.05 at M = 1; q/k/v and o at M = 8
+  // 6.45 / 6.65 and 6.39 / 6.55 (row-group, two column groups).
+  static constexpr int THREADS = (UP && !(RG && C == 2)) ? COMPUTE_THREADS : KERNEL_THREADS;
   static_assert(BYTES <= 227 * 1024 - 1024, "shared memory of one CTA");
   static_assert(SLOT % 16 == 0 && XSLOT % 16 == 0, "16-byte aligned ring slots");
   static_assert(SIG_OFF == CHUNK_PAIRS * C * 1024 && SLOT == CHUNK_PAIRS * C * 1024 + CHUNK_PAIRS * MAXM * 16,
