@@ -58,6 +58,7 @@ CASES = [
     (3584, 3584, (16,)),
     (18944, 3584, (3,)),
     (3584, 18944, (5, 8)),
+    (384, 2080, (4, 7)),      # 65 blocks: an odd count and a partial last chunk of the pass
 ]
 
 
@@ -89,12 +90,14 @@ def test_noalloc_matches_existing_entry_point_twice(N, K, Ms):
 
 
 def test_pre_conversion_pass_is_launched():
-    # a 152-SM device: 512 x 3584 runs as row-group CTAs up to 8 rows (the
-    # pass from 4 rows adds one launch per main launch), 3584 x 18944 as five
-    # K splits (no pass)
+    # a 152-SM device: 512 x 3584 and 384 x 2080 run as row-group CTAs up to 8
+    # rows (the pass from 4 rows adds one launch per main launch), 3584 x 18944
+    # as five K splits (no pass), 300 x 1024 as row-group CTAs with a K too
+    # short for the pass
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("launch plan measured for 152 SMs")
-    for (N, K), with_pass, without in (((512, 3584), (4, 8), (1, 3)), ((3584, 18944), (), (1, 5, 8))):
+    for (N, K), with_pass, without in (((512, 3584), (4, 8), (1, 3)), ((3584, 18944), (), (1, 5, 8)),
+                                       ((384, 2080), (4, 7), (3,)), ((300, 1024), (), (4, 8))):
         W, _ = _setup(N, K, 94, 0)
         for M in with_pass:
             assert q4.q4mm_plan_info(W, M, q4.Q4MM_FORCE_MMA)[1] == 2, (N, K, M)
