@@ -98,17 +98,20 @@ def test_896_config_full_elementwise(q4):
             assert_within_bound(y, y64, bound, "896 M=%d" % M)
 
 
+@pytest.mark.parametrize("mode", ["streaming", "tensor_core"])
 @pytest.mark.parametrize("name", ["gate_proj", "up_proj", "down_proj"])
-def test_mixed_step_m124_parity_and_invariance(q4, name):
-    """120 prefill rows + 4 verify rows in one call (continuous batching)."""
+def test_mixed_step_m124_parity_and_invariance(q4, name, mode):
+    """120 prefill rows + 4 verify rows in one call (continuous batching), in
+    the batch-invariant mode of the streaming kernel or of the tensor cores."""
     W, blocks = _weight(q4, 3, name)
     rng = np.random.default_rng(124)
     K = W.K
     prefill = acts(3, 120, K)
     verify = acts(3, 4, K, salt=1)
     x = np.concatenate([prefill, verify])
-    _sampled_check(q4, W, blocks, x, 0, rng, n_per_row=256, what="%s M=124" % name)
-    inv = q4.Q4MM_BATCH_INVARIANT
+    if mode == "streaming":  # the default mode once, on the same batch
+        _sampled_check(q4, W, blocks, x, 0, rng, n_per_row=256, what="%s M=124" % name)
+    inv = q4.Q4MM_BATCH_INVARIANT | (q4.Q4MM_FORCE_TC if mode == "tensor_core" else 0)
     xd = torch.from_numpy(x).to(DEV)
     y124 = q4.q4mm_forward_ex(W, xd, inv).cpu().numpy()
     y4 = q4.q4mm_forward_ex(W, xd[120:].contiguous(), inv).cpu().numpy()
@@ -123,7 +126,7 @@ def test_mixed_step_m124_parity_and_invariance(q4, name):
     cols = rng.choice(W.N, size=256, replace=False)
     pairs = np.array([(m, n) for m in (0, 119, 120, 123) for n in cols], np.int64)
     _, y64, bound = oracle.matmul_pairs(blocks, x, pairs)
-    assert_within_bound(y124[pairs[:, 0], pairs[:, 1]], y64, bound, "%s invariant M=124" % name)
+    assert_within_bound(y124[pairs[:, 0], pairs[:, 1]], y64, bound, "%s %s invariant M=124" % (name, mode))
 
 
 def test_gate_m_sweep_parity(q4):

@@ -27,6 +27,7 @@ def q4():
 def _flags(q4):
     return {"auto": 0, "simt": q4.Q4MM_FORCE_SIMT, "mma": q4.Q4MM_FORCE_MMA,
             "tc": q4.Q4MM_FORCE_TC, "invariant": q4.Q4MM_BATCH_INVARIANT,
+            "invariant_tc": q4.Q4MM_BATCH_INVARIANT | q4.Q4MM_FORCE_TC,
             "row_by_row": q4.Q4MM_ROW_BY_ROW}
 
 
@@ -203,7 +204,7 @@ def test_batch_invariant_rows_bit_identical(q4, N, K, mode):
 
 # ------------------------------------------------------------------ argmax
 
-@pytest.mark.parametrize("mode", ["auto", "simt", "mma", "tc", "invariant"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "mma", "tc", "invariant", "invariant_tc"])
 def test_argmax_matches_oracle(q4, mode):
     N, K = 1000, 512
     w = weights(55, 0, N, K)
