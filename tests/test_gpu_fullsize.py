@@ -68,6 +68,36 @@ def test_qwen7b_linear_decode_parity(q4, name):
     assert q4.q4_device_status() == q4.Q4_OK
 
 
+@pytest.mark.parametrize("group", [("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj")])
+def test_qwen7b_grouped_calls_as_benchmarked(q4, group):
+    """The grouped calls of the benchmark step (q/k/v: row-group CTAs, with the
+    activation pre-conversion pass from M = 4; gate/up: two-tile CTAs) at the
+    7B shapes and the step's M, on sampled outputs of every weight."""
+    cache = {}
+    for i, name in enumerate(group):
+        N, K = LIN[name]
+        w = weights(6, MATRIX_ID[name], N, K)
+        cache[name] = (q4.q4_quantize(torch.from_numpy(w).to(DEV)), oracle.quantize(w))
+        del w
+    Ws = [cache[n][0] for n in group]
+    rng = np.random.default_rng(len(group))
+    K = Ws[0].K
+    for M in (1, 2, 3, 4, 5, 8):
+        x = acts(6, M, K, salt=M)
+        ys = q4.q4mm_forward_group(Ws, torch.from_numpy(x).to(DEV))
+        for name, y in zip(group, ys):
+            blocks = cache[name][1]
+            N = blocks.shape[0]
+            cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=min(512, N), replace=False)]))
+            pairs = np.array([(m, n) for m in range(M) for n in cols], np.int64)
+            _, y64, bound = oracle.matmul_pairs(blocks, x, pairs)
+            got = y.cpu().numpy()[pairs[:, 0], pairs[:, 1]]
+            assert_within_bound(got, y64, bound, "group %s M=%d" % (name, M))
+    assert q4.q4_device_status() == q4.Q4_OK
+    for W in Ws:
+        W.free()
+
+
 def test_qwen7b_kv_full_elementwise(q4):
     W, blocks = _weight(q4, 2, "v_proj")
     for M in (1, 5, 8):
